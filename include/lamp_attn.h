@@ -1,0 +1,164 @@
+/*
+ * lamp_attn.h -- C ABI of the GB300 (sm_103a) LampAttention forward pass.
+ *
+ * Operation: the forward pass of look-ahead mixed-precision FlashAttention
+ * described in "LampAttention: Look-Ahead Mixed-Precision FlashAttention for
+ * Dedicated Accelerators" (arXiv 2609.39361), abstract: the key-query
+ * products are accumulated, and their exponentials evaluated, in 8-bit
+ * formats; sensitive sub-blocks are identified adaptively and recomputed in
+ * 16-bit formats; the thresholds delta (first stage, default 2^-8, can be
+ * disabled) and tau (recompute threshold, default 2^-1) and the per-tile
+ * count of 16-bit sub-blocks (0 / 1 / 2+) follow Table 1's caption and
+ * header and the captions of Figures 1-8.
+ *
+ * The paper gives no formulas; this library implements these readings:
+ *   - 8-bit format FP8 E4M3 (OCP "fn": max 448, RNE, saturating);
+ *   - S8 = fl8(sigma * sum_t fl8(q_t) fl8(k_t)), the sum taken exactly;
+ *   - running max m_j of S8 over 64-key tiles in ascending key order;
+ *   - x8 = fl8(S8 - m_j), P8 = fl8(exp(x8));
+ *   - tiles of 64 queries x 64 keys, sub-blocks of 16 queries x 64 keys;
+ *   - stage 1 of a sub-block: some visible entry has P8 >= delta;
+ *     flagged: some visible entry has P8 >= delta and half-ulp8(S8) >= tau;
+ *   - flagged rows: S16 = sigma * sum bf16(q) bf16(k) (FP32 accumulation),
+ *     P16 = fp16(exp(S16 - m_j)); other rows use P8;
+ *   - P.V in FP16 operands (V16 = fp16(v), saturating) with FP32
+ *     accumulation; out = O / l, LSE = m + ln l.
+ * The mask bytes and the histogram are bit-identical to a CPU statement of
+ * these readings; out and LSE agree with it to 2e-3 / 1e-3 (plus the final
+ * rounding of out to its dtype).
+ *
+ * All tensor pointers are DEVICE pointers owned by the caller; the library
+ * keeps no reference after the call returns.  Work is enqueued on
+ * `shapes->stream` and the call returns without synchronising.
+ */
+#ifndef LAMP_ATTN_H
+#define LAMP_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LAMP_OK = 0,
+  LAMP_ERR_INVALID_ARG = 1,  /* bad pointer, shape, stride, dtype or threshold */
+  LAMP_ERR_UNSUPPORTED = 2,  /* head_dim not in {64,128,256}, or not an sm_103 device */
+  LAMP_ERR_CUDA = 3,         /* a CUDA runtime / driver call failed */
+  LAMP_ERR_TIMEOUT = 4,      /* a device-side wait hit its time limit (status word) */
+  LAMP_ERR_WORKSPACE = 5     /* caller workspace smaller than lamp_attn_workspace_bytes() */
+} lamp_status;
+
+typedef enum {
+  LAMP_MASK_NONE = 0,    /* every key visible to every query */
+  LAMP_MASK_CAUSAL = 1,  /* key c visible to query r iff c <= r */
+  LAMP_MASK_SLIDING = 2  /* key c visible to query r iff r - window < c <= r */
+} lamp_mask_kind;
+
+typedef enum { LAMP_DT_BF16 = 0, LAMP_DT_FP32 = 1 } lamp_dtype;
+
+typedef enum {
+  LAMP_FORCE_OFF = 0,    /* the detector decides which sub-blocks run in 16 bits */
+  LAMP_FORCE_ALL16 = 1,  /* every visible sub-block is recomputed in 16 bits */
+  LAMP_FORCE_ALL8 = 2    /* no sub-block is recomputed (plain 8-bit path) */
+} lamp_force;
+
+/* Counter slots of lamp_stats.counters (uint64 each). */
+enum {
+  LAMP_CNT_TILES = 0,       /* visited 64x64 tiles (>= 1 visible entry) */
+  LAMP_CNT_HIST0 = 1,       /* visited tiles with 0 flagged sub-blocks */
+  LAMP_CNT_HIST1 = 2,       /*                    1 flagged sub-block */
+  LAMP_CNT_HIST2 = 3,       /*                    2 or more           */
+  LAMP_CNT_STRIPS = 4,      /* visited sub-blocks (>= 1 visible entry) */
+  LAMP_CNT_STAGE1 = 5,      /* sub-blocks passing the first stage */
+  LAMP_CNT_FLAGGED = 6,     /* sub-blocks recomputed in 16 bits */
+  LAMP_CNT_SAT = 7,         /* visible logits with |S8| = 448 */
+  LAMP_CNT_FIXUPS = 8,      /* logits re-derived exactly (near an 8-bit rounding boundary) */
+  LAMP_CNT_STATUS = 9,      /* device-side status (lamp_status), 0 = ok */
+  LAMP_CNT_RECOMP_STEPS = 10, /* 128x64 kernel steps that ran the 16-bit recompute MMA */
+  LAMP_NUM_COUNTERS = 16
+};
+
+typedef struct {
+  int32_t batch, seqlen, heads_q, heads_kv, head_dim;
+  /* strides in ELEMENTS for the (batch, sequence, head) dimensions of the
+   * BSHD tensors; the head_dim dimension is contiguous.  q/out are
+   * [B, N, Hq, d], k/v are [B, N, Hkv, d].  Byte strides must be multiples
+   * of 16 and the base pointers 16-byte aligned. */
+  int64_t q_stride[3], k_stride[3], v_stride[3], o_stride[3];
+  int32_t window;        /* LAMP_MASK_SLIDING: window length W >= 1 */
+  float softmax_scale;   /* sigma; 0 -> 1/sqrt(head_dim) (rounded once from double) */
+  int32_t in_dtype;      /* lamp_dtype of q, k, v */
+  int32_t out_dtype;     /* lamp_dtype of out */
+  int32_t force;         /* lamp_force */
+  void* workspace;       /* device scratch, >= lamp_attn_workspace_bytes(); NULL ->
+                            the call allocates and frees it stream-ordered */
+  size_t workspace_bytes;
+  void* stream;          /* cudaStream_t; NULL = legacy default stream */
+  void* stage_events[3]; /* optional cudaEvent_t, recorded on `stream` before the
+                            pre-pass, between it and the fused kernel, and after
+                            the fused kernel (per-stage timing); NULL = none */
+} lamp_shapes;
+
+typedef struct {
+  uint8_t* mask;  /* DEVICE [B][Hq][T][T], T = ceil(seqlen/64), or NULL.
+                     Byte (b,h,i,j): bit s (0..3) = sub-block s of tile (i,j)
+                     flagged; bit 4+s = it passed stage 1; 0 for tiles that are
+                     not visited.  Written in full by every call. */
+  uint64_t* counters; /* DEVICE [LAMP_NUM_COUNTERS] or NULL; zeroed, then
+                         accumulated, by every call (stream-ordered). */
+} lamp_stats;
+
+/*
+ * lamp_attn_fwd: out = LampAttention(q, k, v) and lse (natural log,
+ * [B, Hq, N] fp32, contiguous; may be NULL).
+ *   q, k, v   DEVICE, BSHD with the strides above, dtype shapes->in_dtype.
+ *   out       DEVICE, BSHD [B, N, Hq, d] with o_stride, dtype shapes->out_dtype.
+ *   mask_kind lamp_mask_kind; causal and sliding use the same N for queries
+ *             and keys.
+ *   delta     first-stage threshold (>= 0; 0 disables the first stage).
+ *   tau       recompute threshold (<= 0 flags every stage-1 sub-block).
+ *   stats     may be NULL.
+ * Returns LAMP_OK or an error code.  Argument errors are detected before
+ * any launch and nothing is enqueued.  A device-side failure (a wait that
+ * exceeded its time limit, 2 s by default, LAMP_WAIT_TIMEOUT_NS in the
+ * environment overrides it) ends the kernel early: it is written to
+ * counters[LAMP_CNT_STATUS] when counters are given and is visible after the
+ * stream is synchronised; out / lse / mask are then incomplete.
+ * head_dim must be 64, 128 or 256; seqlen >= 1 (any value, not only
+ * multiples of 64); heads_q a multiple of heads_kv.
+ */
+int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out,
+                  float* lse, const lamp_shapes* shapes, int mask_kind,
+                  float delta, float tau, lamp_stats* stats);
+
+/* Bytes of device workspace lamp_attn_fwd needs for these shapes (E4M3
+ * copies of q and k, an fp16 copy of v, bf16 copies of fp32 inputs, and
+ * per-row norms).  0 on invalid shapes. */
+size_t lamp_attn_workspace_bytes(const lamp_shapes* shapes);
+
+/* Static, human-readable text for a lamp_status value. */
+const char* lamp_strerror(int status);
+
+/* Library version string, e.g. "lamp-attn 0.1 sm_103a". */
+const char* lamp_version(void);
+
+/*
+ * lamp_selftest: device checks of the tensor-core building blocks used by
+ * lamp_attn_fwd (no counterpart in the paper), run on caller data with the
+ * same shared-memory layouts and instruction sequences:
+ *   which 0: out[128 x 64]    = A . B^T, A [128 x d], B [64 x d] E4M3 codes (uint8)
+ *   which 1: out[128 x 64]    = A . B^T, A [128 x d], B [64 x d] BF16
+ *   which 2: out[128 x (d+16)] = P . [V | 1], P [128 x 64], V [64 x d] FP16
+ * a, b: DEVICE, row-major as listed; out: DEVICE float32, row-major.
+ * Returns LAMP_OK or an error code after synchronising `stream`.
+ */
+int lamp_selftest(int which, const void* a, const void* b, float* out, int d,
+                  void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAMP_ATTN_H */

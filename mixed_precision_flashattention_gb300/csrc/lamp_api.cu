@@ -1,0 +1,252 @@
+// lamp_api.cu -- the C ABI: argument checks, workspace layout, TMA tensor
+// maps, and the two launches (pre-pass, fused forward kernel).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/lamp_attn.h"
+#include "lamp_common.cuh"
+
+namespace lamp {
+cudaError_t launch_prep(const PrepParams& p, int d, cudaStream_t st);
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st);
+
+// Relative bound on |A_tc - A| / (||q8|| ||k8||) of the FP8 tensor-core
+// accumulation, with margin, plus the float rounding of A*sigma and of
+// y +- G (see the guard in lamp_fwd.cu).  The exact path keeps results
+// right whenever the bound holds; the self-test measures the real error.
+constexpr float kGuard = 0x1p-14f;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait
+
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeFn)f;
+  });
+  return fn;
+}
+
+// 4-D map over a BSHD-like tensor: dims (d, N, H, B) with byte strides for
+// N, H and B; the box is (box_d, box_rows, 1, 1) with the given swizzle.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, int d, int n, int heads,
+              int batch, long long s_n, long long s_h, long long s_b, int box_d, int box_rows,
+              CUtensorMapSwizzle swz) {
+  EncodeFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)heads, (cuuint64_t)batch};
+  cuuint64_t strides[3] = {(cuuint64_t)(s_n * esize), (cuuint64_t)(s_h * esize), (cuuint64_t)(s_b * esize)};
+  cuuint32_t box[4] = {(cuuint32_t)box_d, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct WsLayout {
+  size_t q8, k8, v16, q16, k16, nq, nk, abort, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(const lamp_shapes& s) {
+  const size_t B = s.batch, N = s.seqlen, Hq = s.heads_q, Hkv = s.heads_kv, D = s.head_dim;
+  const size_t T = (N + kBN - 1) / kBN;
+  WsLayout w{};
+  size_t o = 0;
+  w.q8 = o; o = align256(o + B * Hq * N * D);
+  w.k8 = o; o = align256(o + B * Hkv * N * D);
+  w.v16 = o; o = align256(o + B * Hkv * N * D * 2);
+  if (s.in_dtype == LAMP_DT_FP32) {
+    w.q16 = o; o = align256(o + B * Hq * N * D * 2);
+    w.k16 = o; o = align256(o + B * Hkv * N * D * 2);
+  }
+  w.nq = o; o = align256(o + B * Hq * N * 4);
+  w.nk = o; o = align256(o + B * Hkv * T * 4);
+  w.abort = o; o = align256(o + 4);
+  w.total = o;
+  return w;
+}
+
+bool shapes_ok(const lamp_shapes* s) {
+  if (!s) return false;
+  if (s->batch < 1 || s->seqlen < 1 || s->heads_q < 1 || s->heads_kv < 1) return false;
+  if (s->heads_q % s->heads_kv) return false;
+  if (s->in_dtype != LAMP_DT_BF16 && s->in_dtype != LAMP_DT_FP32) return false;
+  if (s->out_dtype != LAMP_DT_BF16 && s->out_dtype != LAMP_DT_FP32) return false;
+  if (s->force < LAMP_FORCE_OFF || s->force > LAMP_FORCE_ALL8) return false;
+  if (!(s->softmax_scale >= 0.0f) || std::isinf(s->softmax_scale)) return false;
+  return true;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int device_check() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LAMP_ERR_CUDA;
+  int maj = 0, min = 0;
+  if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return LAMP_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return LAMP_ERR_CUDA;
+  if (maj != 10 || min != 3) return LAMP_ERR_UNSUPPORTED;
+  return LAMP_OK;
+}
+
+}  // namespace
+}  // namespace lamp
+
+using namespace lamp;
+
+extern "C" {
+
+const char* lamp_strerror(int status) {
+  switch (status) {
+    case LAMP_OK: return "ok";
+    case LAMP_ERR_INVALID_ARG: return "invalid argument (pointer, shape, stride, dtype or threshold)";
+    case LAMP_ERR_UNSUPPORTED: return "unsupported (head_dim must be 64/128/256 on an sm_103 GPU)";
+    case LAMP_ERR_CUDA: return "CUDA runtime or driver error";
+    case LAMP_ERR_TIMEOUT: return "a device-side wait exceeded its time limit";
+    case LAMP_ERR_WORKSPACE: return "workspace smaller than lamp_attn_workspace_bytes()";
+    default: return "unknown status";
+  }
+}
+
+const char* lamp_version(void) { return "lamp-attn 0.1 sm_103a"; }
+
+size_t lamp_attn_workspace_bytes(const lamp_shapes* shapes) {
+  if (!shapes_ok(shapes)) return 0;
+  if (shapes->head_dim != 64 && shapes->head_dim != 128 && shapes->head_dim != 256) return 0;
+  return ws_layout(*shapes).total;
+}
+
+int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const lamp_shapes* shapes,
+                  int mask_kind, float delta, float tau, lamp_stats* stats) {
+  if (!q || !k || !v || !out || !shapes_ok(shapes)) return LAMP_ERR_INVALID_ARG;
+  const lamp_shapes& s = *shapes;
+  const int D = s.head_dim;
+  if (D != 64 && D != 128 && D != 256) return LAMP_ERR_UNSUPPORTED;
+  if (mask_kind < LAMP_MASK_NONE || mask_kind > LAMP_MASK_SLIDING) return LAMP_ERR_INVALID_ARG;
+  if (mask_kind == LAMP_MASK_SLIDING && s.window < 1) return LAMP_ERR_INVALID_ARG;
+  if (!(delta >= 0.0f) || std::isnan(tau)) return LAMP_ERR_INVALID_ARG;
+  const int es_in = s.in_dtype == LAMP_DT_FP32 ? 4 : 2;
+  const int es_out = s.out_dtype == LAMP_DT_FP32 ? 4 : 2;
+  const int64_t* strides[4] = {s.q_stride, s.k_stride, s.v_stride, s.o_stride};
+  for (int t = 0; t < 4; ++t)
+    for (int i = 0; i < 3; ++i) {
+      const int es = t == 3 ? es_out : es_in;
+      if (strides[t][i] < D || (strides[t][i] * es) % 16) return LAMP_ERR_INVALID_ARG;
+    }
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || ((uintptr_t)lse & 3u))
+    return LAMP_ERR_INVALID_ARG;
+  int st = device_check();
+  if (st != LAMP_OK) return st;
+
+  cudaStream_t stream = (cudaStream_t)s.stream;
+  const WsLayout w = ws_layout(s);
+  uint8_t* ws = (uint8_t*)s.workspace;
+  bool own_ws = false;
+  if (!ws) {
+    if (cudaMallocAsync((void**)&ws, w.total, stream) != cudaSuccess) return LAMP_ERR_CUDA;
+    own_ws = true;
+  } else if (s.workspace_bytes < w.total || !aligned16(ws)) {
+    return LAMP_ERR_WORKSPACE;
+  }
+  auto fail = [&](int code) {
+    if (own_ws) cudaFreeAsync(ws, stream);
+    return code;
+  };
+
+  const int B = s.batch, N = s.seqlen, Hq = s.heads_q, Hkv = s.heads_kv;
+  const int T = (N + kBN - 1) / kBN;
+  if (stats && stats->counters &&
+      cudaMemsetAsync(stats->counters, 0, LAMP_NUM_COUNTERS * sizeof(uint64_t), stream) != cudaSuccess)
+    return fail(LAMP_ERR_CUDA);
+  if (stats && stats->mask &&
+      cudaMemsetAsync(stats->mask, 0, (size_t)B * Hq * T * T, stream) != cudaSuccess)
+    return fail(LAMP_ERR_CUDA);
+  // norms of the key tiles and the abort word are contiguous: one memset
+  if (cudaMemsetAsync(ws + w.nk, 0, w.total - w.nk, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
+
+  PrepParams pp{};
+  pp.q = q; pp.k = k; pp.v = v;
+  for (int i = 0; i < 3; ++i) { pp.qs[i] = s.q_stride[i]; pp.ks[i] = s.k_stride[i]; pp.vs[i] = s.v_stride[i]; }
+  pp.q8 = ws + w.q8; pp.k8 = ws + w.k8; pp.v16 = ws + w.v16;
+  pp.q16 = s.in_dtype == LAMP_DT_FP32 ? (void*)(ws + w.q16) : nullptr;
+  pp.k16 = s.in_dtype == LAMP_DT_FP32 ? (void*)(ws + w.k16) : nullptr;
+  pp.nq = (float*)(ws + w.nq); pp.nkmax = (float*)(ws + w.nk);
+  pp.B = B; pp.N = N; pp.Hq = Hq; pp.Hkv = Hkv; pp.T = T; pp.in_f32 = s.in_dtype == LAMP_DT_FP32;
+  auto mark = [&](int i) {
+    return !s.stage_events[i] || cudaEventRecord((cudaEvent_t)s.stage_events[i], stream) == cudaSuccess;
+  };
+  if (!mark(0)) return fail(LAMP_ERR_CUDA);
+  if (launch_prep(pp, D, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
+  if (!mark(1)) return fail(LAMP_ERR_CUDA);
+
+  FwdParams fp;
+  memset(&fp, 0, sizeof(fp));
+  const int f8box = D == 64 ? 64 : 128;
+  const CUtensorMapSwizzle f8swz = D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  const long long NDq = (long long)N * D, NDk = (long long)N * D;
+  bool ok = true;
+  ok &= make_map(&fp.tmQ8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ws + w.q8, D, N, Hq, B, D, NDq, NDq * Hq, f8box, kBM, f8swz);
+  ok &= make_map(&fp.tmK8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ws + w.k8, D, N, Hkv, B, D, NDk, NDk * Hkv, f8box, kBN, f8swz);
+  ok &= make_map(&fp.tmV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws + w.v16, D, N, Hkv, B, D, NDk, NDk * Hkv, 64, kBN,
+                 CU_TENSOR_MAP_SWIZZLE_128B);
+  if (s.in_dtype == LAMP_DT_FP32) {
+    ok &= make_map(&fp.tmQ16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + w.q16, D, N, Hq, B, D, NDq, NDq * Hq, 64, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&fp.tmK16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + w.k16, D, N, Hkv, B, D, NDk, NDk * Hkv, 64,
+                   kBN, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    ok &= make_map(&fp.tmQ16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, D, N, Hq, B, s.q_stride[1], s.q_stride[2],
+                   s.q_stride[0], 64, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&fp.tmK16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, D, N, Hkv, B, s.k_stride[1], s.k_stride[2],
+                   s.k_stride[0], 64, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (!ok) return fail(LAMP_ERR_CUDA);
+
+  const double sigma_d = s.softmax_scale > 0.0f ? (double)s.softmax_scale : 1.0 / std::sqrt((double)D);
+  fp.out = out;
+  fp.lse = lse;
+  fp.mask = stats ? stats->mask : nullptr;
+  fp.counters = stats ? (unsigned long long*)stats->counters : nullptr;
+  fp.nq = (const float*)(ws + w.nq);
+  fp.nkmax = (const float*)(ws + w.nk);
+  for (int i = 0; i < 3; ++i) fp.o_stride[i] = s.o_stride[i];
+  fp.B = B; fp.N = N; fp.Hq = Hq; fp.Hkv = Hkv; fp.T = T;
+  fp.nqb = (N + kBM - 1) / kBM;
+  fp.window = s.window;
+  fp.mask_kind = mask_kind;
+  fp.force = s.force;
+  fp.out_f32 = s.out_dtype == LAMP_DT_FP32;
+  fp.sigma_f = (float)sigma_d;
+  fp.sigma_d = sigma_d;
+  fp.guard = kGuard;
+  fp.tau_abs = host_tau_abs(tau);
+  fp.delta_code = host_delta_code(delta);
+  fp.timeout_ns = kTimeoutNs;
+  if (const char* e = getenv("LAMP_WAIT_TIMEOUT_NS")) fp.timeout_ns = strtoull(e, nullptr, 10);
+  fp.gabort = (unsigned int*)(ws + w.abort);
+  if (launch_fwd(fp, D, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
+  if (!mark(2)) return fail(LAMP_ERR_CUDA);
+  if (own_ws && cudaFreeAsync(ws, stream) != cudaSuccess) return LAMP_ERR_CUDA;
+  return LAMP_OK;
+}
+
+}  // extern "C"

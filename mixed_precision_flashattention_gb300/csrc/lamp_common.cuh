@@ -1,0 +1,171 @@
+// lamp_common.cuh -- shapes, shared-memory layout arithmetic and exact
+// 8-bit helpers shared by the LampAttention kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "lamp_ptx.cuh"
+
+namespace lamp {
+
+constexpr int kBM = 128;        // query rows per CTA (one TMEM lane per row)
+constexpr int kBN = 64;         // keys per step = one 64-key tile of the method
+constexpr int kStrip = 16;      // query rows per sub-block
+constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = 192;   // 4 softmax warps + TMA warp + MMA warp
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Kernel parameters (passed by value as a __grid_constant__).
+struct FwdParams {
+  CUtensorMap tmQ8, tmQ16, tmK8, tmK16, tmV;
+  void* out;
+  float* lse;
+  uint8_t* mask;
+  unsigned long long* counters;
+  const float* nq;     // [B, Hq, N]   ||fl8(q_r)||_2 (upper bound)
+  const float* nkmax;  // [B, Hkv, T]  max over the tile of ||fl8(k_c)||_2
+  long long o_stride[3];
+  int B, N, Hq, Hkv, T, nqb;
+  int window, mask_kind, force, out_f32;
+  float sigma_f;       // softmax scale rounded to float
+  double sigma_d;      // softmax scale in double (exact re-derivation)
+  float guard;         // relative bound on |y_tc - y| per unit sigma*|q|*|k|
+  float tau_abs;       // flag iff |S8| >= tau_abs (derived from tau)
+  uint32_t delta_code; // stage 1 iff P8 code >= delta_code
+  unsigned long long timeout_ns;  // a wait gives up after this long
+  unsigned int* gabort;           // grid-wide abort word (workspace, zeroed per call)
+};
+
+// Pre-pass parameters (see lamp_prep.cu).
+struct PrepParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  long long qs[3], ks[3], vs[3];  // element strides (B, S, H)
+  uint8_t* q8;                    // [B, Hq, N, D]  E4M3
+  uint8_t* k8;                    // [B, Hkv, N, D] E4M3
+  void* v16;                      // [B, Hkv, N, D] fp16
+  void* q16;                      // [B, Hq, N, D]  bf16 (fp32 input only)
+  void* k16;                      // [B, Hkv, N, D] bf16 (fp32 input only)
+  float* nq;                      // [B, Hq, N]
+  float* nkmax;                   // [B, Hkv, T] (zeroed before the launch)
+  int B, N, Hq, Hkv, T, in_f32;
+};
+
+// Byte offset of byte `x` (0 <= x < row_bytes) of row `r` in a K-major
+// tile whose rows are `row_bytes` long, stored as 128-byte (or 64-byte when
+// row_bytes == 64) swizzled atoms: 8 rows per atom, atoms stacked along the
+// rows, columns of atoms (each 128 B of the row) stacked after all rows.
+__device__ __forceinline__ uint32_t swz_offset(int r, int x, int rows, int row_bytes) {
+  if (row_bytes == 64) {
+    int chunk = (x >> 4) ^ ((r >> 1) & 3);
+    return (uint32_t)((r >> 3) * 512 + (r & 7) * 64 + chunk * 16 + (x & 15));
+  }
+  int col = x >> 7, w = x & 127;
+  int chunk = (w >> 4) ^ (r & 7);
+  return (uint32_t)(col * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + chunk * 16 + (w & 15));
+}
+
+// E4M3 code -> exact integer value * 2^9 (so every finite code is an integer).
+__device__ __forceinline__ int e4m3_to_int512(uint32_t b) {
+  int e = (b >> 3) & 15, m = b & 7;
+  int v = e ? ((8 + m) << (e - 1)) : m;
+  return (b & 0x80) ? -v : v;
+}
+
+// Round a double to E4M3 (round to nearest even, saturating to +-448).
+// Used only on the rare exact path, so it is written for clarity.
+__device__ __forceinline__ float e4m3_rne_from_double(double y) {
+  double a = fabs(y);
+  float r = 0.0f;
+  if (a > 0.0) {
+    int e = ilogb(a);
+    int E = e < -6 ? -6 : e;
+    double n = rint(ldexp(a, 3 - E));  // multiples of the E4M3 spacing at a
+    double v = ldexp(n, E - 3);
+    r = (float)(v > 448.0 ? 448.0 : v);
+  }
+  return y < 0.0 ? -r : r;
+}
+
+// Smallest non-negative E4M3 magnitude whose half-spacing is >= tau
+// (+inf if none).  half-spacing(v) = 2^(max(floor(log2 v), -6) - 4), and
+// 2^-10 at v = 0.
+inline float host_tau_abs(float tau) {
+  if (!(tau > 0.0f)) return 0.0f;
+  if (tau <= 0x1p-10f) return 0.0f;
+  for (int e = -6; e <= 8; ++e) {
+    float half = ldexpf(1.0f, e - 4);
+    if (half >= tau) return e == -6 ? 0x1p-9f : ldexpf(1.0f, e);
+  }
+  return __builtin_inff();
+}
+
+// Code of the smallest non-negative E4M3 value >= delta (0xFF if none),
+// so that P8 >= delta iff code(P8) >= that code (codes of non-negative
+// values are ordered like the values).
+inline uint32_t host_delta_code(float delta) {
+  if (!(delta > 0.0f)) return 0u;
+  for (uint32_t c = 0; c <= 0x7E; ++c) {
+    uint32_t e = c >> 3, m = c & 7;
+    float v = e ? ldexpf(1.0f + m / 8.0f, (int)e - 7) : ldexpf((float)m, -9);
+    if (v >= delta) return c;
+  }
+  return 0xFFu;
+}
+
+// ---------------------------------------------------------------- MMA issue
+// Shared-memory operand layouts (all 1024-byte aligned):
+//   F8 tiles  [rows x D] E4M3, K-major: 128-byte swizzled atom columns of
+//             [rows x 128 B] (D = 64: one column of 64-byte swizzled rows).
+//   16-bit    [rows x D] BF16/FP16, K-major: D/64 atom columns of
+//             [rows x 128 B], 128-byte swizzle.
+//   V         [64 keys x D] FP16, MN-major: D/64 regions of [64 keys x 128 B]
+//             (64 values of d per key row), then one region of ones.
+template <int D>
+struct Mma {
+  static constexpr int F8_ROW = (D == 64) ? 64 : 128;
+  // S[128 x 64] (fp32, TMEM) = Q8[128 x D] . K8[64 x D]^T
+  static __device__ __forceinline__ void qk8(uint32_t tmem_d, uint32_t q8, uint32_t k8) {
+    constexpr uint32_t idesc = make_idesc(0, 0, 0, 128, 64);
+    const uint32_t layout = (F8_ROW == 64) ? kLayoutSW64 : kLayoutSW128;
+    const uint32_t sbo = (F8_ROW == 64) ? 512u : 1024u;
+#pragma unroll
+    for (int kk = 0; kk < D / 32; ++kk) {
+      const int col = (kk * 32) / F8_ROW, off = (kk * 32) % F8_ROW;
+      const uint64_t ad = make_sdesc(q8 + col * 128 * 128 + off, 16, sbo, layout);
+      const uint64_t bd = make_sdesc(k8 + col * 64 * 128 + off, 16, sbo, layout);
+      mma_f8(tmem_d, ad, bd, idesc, kk > 0);
+    }
+  }
+  // S16[128 x 64] = Q16[128 x D] . K16[64 x D]^T (BF16)
+  static __device__ __forceinline__ void qk16(uint32_t tmem_d, uint32_t q16, uint32_t k16) {
+    constexpr uint32_t idesc = make_idesc(1, 1, 0, 128, 64);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int col = kk / 4, off = (kk % 4) * 32;
+      const uint64_t ad = make_sdesc(q16 + col * 128 * 128 + off, 16, 1024, kLayoutSW128);
+      const uint64_t bd = make_sdesc(k16 + col * 64 * 128 + off, 16, 1024, kLayoutSW128);
+      mma_f16(tmem_d, ad, bd, idesc, kk > 0);
+    }
+  }
+  // O[128 x (D+16)] (+)= P[128 x 64] . [V | 1][64 x (D+16)]  (FP16)
+  static __device__ __forceinline__ void pv(uint32_t tmem_o, uint32_t pbase, uint32_t vbase, bool acc) {
+    constexpr int N1 = (D + 16 <= 256) ? D + 16 : 256;
+    constexpr uint32_t idesc1 = make_idesc(0, 0, 1, 128, N1);
+    constexpr uint32_t idesc2 = make_idesc(0, 0, 1, 128, 16);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t ad = make_sdesc(pbase + kk * 32, 16, 1024, kLayoutSW128);
+      const uint64_t bd = make_sdesc(vbase + kk * 16 * 128, 64 * 128, 1024, kLayoutSW128);
+      mma_f16(tmem_o, ad, bd, idesc1, acc || kk > 0);
+      if (D + 16 > 256) {
+        const uint64_t bd2 = make_sdesc(vbase + (D / 64) * 64 * 128 + kk * 16 * 128, 64 * 128, 1024, kLayoutSW128);
+        mma_f16(tmem_o + 256, ad, bd2, idesc2, acc || kk > 0);
+      }
+    }
+  }
+};
+
+}  // namespace lamp

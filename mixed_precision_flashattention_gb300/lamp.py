@@ -1,0 +1,163 @@
+"""ctypes binding of the LampAttention C ABI (include/lamp_attn.h).
+
+Argument marshalling only: torch supplies device memory and the current
+stream; every step of the forward pass runs in the CUDA library.  There is
+no fallback: if the library is missing or the device is not an sm_103 GPU,
+calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+LAMP_OK, LAMP_ERR_INVALID_ARG, LAMP_ERR_UNSUPPORTED, LAMP_ERR_CUDA, LAMP_ERR_TIMEOUT, LAMP_ERR_WORKSPACE = range(6)
+MASK = {"none": 0, "causal": 1, "sliding": 2}
+FORCE = {"off": 0, "all16": 1, "all8": 2}
+DT = {torch.bfloat16: 0, torch.float32: 1}
+NUM_COUNTERS = 16
+COUNTER_NAMES = ["tiles", "hist0", "hist1", "hist2p", "strips", "stage1", "flagged",
+                 "s8_saturated", "fixups", "status", "recompute_steps"]
+EXPORTS = ["lamp_attn_fwd", "lamp_attn_workspace_bytes", "lamp_strerror", "lamp_version",
+           "lamp_selftest"]
+
+
+class LampShapes(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("seqlen", ctypes.c_int32), ("heads_q", ctypes.c_int32),
+        ("heads_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3),
+        ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
+        ("window", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
+        ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32), ("force", ctypes.c_int32),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("stream", ctypes.c_void_p), ("stage_events", ctypes.c_void_p * 3),
+    ]
+
+
+class LampStats(ctypes.Structure):
+    _fields_ = [("mask", ctypes.c_void_p), ("counters", ctypes.c_void_p)]
+
+
+class LampError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the CUDA library."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise LampError(f"LampAttention CUDA library not built: {path}")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    lib.lamp_attn_fwd.restype = ctypes.c_int
+    lib.lamp_attn_fwd.argtypes = [ctypes.c_void_p] * 4 + [
+        ctypes.c_void_p, ctypes.POINTER(LampShapes), ctypes.c_int, ctypes.c_float, ctypes.c_float,
+        ctypes.POINTER(LampStats)]
+    lib.lamp_attn_workspace_bytes.restype = ctypes.c_size_t
+    lib.lamp_attn_workspace_bytes.argtypes = [ctypes.POINTER(LampShapes)]
+    lib.lamp_strerror.restype = ctypes.c_char_p
+    lib.lamp_strerror.argtypes = [ctypes.c_int]
+    lib.lamp_version.restype = ctypes.c_char_p
+    lib.lamp_selftest.restype = ctypes.c_int
+    lib.lamp_selftest.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                  ctypes.c_int, ctypes.c_void_p]
+    _lib = lib
+    return lib
+
+
+def _check(code: int):
+    if code != LAMP_OK:
+        raise LampError(f"lamp status {code}: {load().lamp_strerror(code).decode()}")
+
+
+def make_shapes(q, k, v, out, *, window=0, scale=0.0, force="off", workspace=None, stream=None,
+                stage_events=None):
+    B, N, Hq, d = q.shape
+    sh = LampShapes()
+    sh.batch, sh.seqlen, sh.heads_q, sh.heads_kv, sh.head_dim = B, N, Hq, k.shape[2], d
+    for name, t in (("q_stride", q), ("k_stride", k), ("v_stride", v), ("o_stride", out)):
+        st = t.stride()
+        if st[3] != 1:
+            raise LampError(f"{name}: head_dim must be contiguous")
+        getattr(sh, name)[:] = [st[0], st[1], st[2]]
+    sh.window = int(window)
+    sh.softmax_scale = float(scale)
+    sh.in_dtype = DT[q.dtype]
+    sh.out_dtype = DT[out.dtype]
+    sh.force = FORCE[force]
+    if workspace is not None:
+        sh.workspace = workspace.data_ptr()
+        sh.workspace_bytes = workspace.numel() * workspace.element_size()
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    sh.stream = s.cuda_stream
+    if stage_events is not None:
+        for i, ev in enumerate(stage_events):
+            sh.stage_events[i] = ev.cuda_event
+    return sh
+
+
+def workspace_bytes(q, k, v, out=None, **kw) -> int:
+    out = q if out is None else out
+    return int(load().lamp_attn_workspace_bytes(ctypes.byref(make_shapes(q, k, v, out, **kw))))
+
+
+def lamp_attn_fwd(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -8, tau=2.0 ** -1,
+                  force="off", out=None, out_dtype=None, lse=None, want_lse=True, mask_bytes=None,
+                  counters=None, workspace=None, stream=None, stage_events=None):
+    """Forward pass.  q [B, N, Hq, d], k/v [B, N, Hkv, d] CUDA tensors (bf16
+    or fp32, d contiguous).  Returns (out, lse, mask_bytes, counters); the
+    last three may be None when not requested.  Asynchronous on ``stream``
+    (default: torch's current stream).  ``stage_events``: three
+    torch.cuda.Event recorded around the pre-pass and the fused kernel."""
+    lib = load()
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise LampError("q, k, v must be CUDA tensors")
+    if q.dtype != k.dtype or q.dtype != v.dtype or q.dtype not in DT:
+        raise LampError("q, k, v must share a dtype in {bfloat16, float32}")
+    B, N, Hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, N, Hq, d), device=q.device, dtype=out_dtype or q.dtype)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, N), device=q.device, dtype=torch.float32)
+    sh = make_shapes(q, k, v, out, window=window, scale=scale, force=force, workspace=workspace,
+                     stream=stream, stage_events=stage_events)
+    stats = LampStats()
+    stats.mask = mask_bytes.data_ptr() if mask_bytes is not None else None
+    stats.counters = counters.data_ptr() if counters is not None else None
+    code = lib.lamp_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             lse.data_ptr() if lse is not None else None, ctypes.byref(sh),
+                             MASK[mask], float(delta), float(tau), ctypes.byref(stats))
+    _check(code)
+    return out, lse, mask_bytes, counters
+
+
+def new_stats(B, Hq, N, device="cuda"):
+    """Device buffers for the mask bytes [B, Hq, T, T] and the counters."""
+    T = (N + 63) // 64
+    return (torch.zeros((B, Hq, T, T), dtype=torch.uint8, device=device),
+            torch.zeros(NUM_COUNTERS, dtype=torch.int64, device=device))
+
+
+def selftest(which: int, a, b, d: int):
+    """Run a tcgen05 building-block check; returns the float32 result."""
+    lib = load()
+    ncols = d + 16 if which == 2 else 64
+    out = torch.full((128, ncols), float("nan"), dtype=torch.float32, device=a.device)
+    s = torch.cuda.current_stream(a.device)
+    _check(lib.lamp_selftest(which, a.data_ptr(), b.data_ptr(), out.data_ptr(), d, s.cuda_stream))
+    return out

@@ -1,0 +1,93 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every entry
+point the header declares; argument errors are reported before any launch
+(no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixed_precision_flashattention_gb300 import build, lamp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "lamp_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(lamp_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return lamp.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert set(names) >= {"lamp_attn_fwd", "lamp_attn_workspace_bytes", "lamp_strerror"}
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(lamp.EXPORTS)
+
+
+def test_strerror_and_version(lib):
+    for code in range(6):
+        assert lib.lamp_strerror(code)
+    assert b"sm_103a" in lib.lamp_version()
+
+
+def _shapes(B=4, N=4096, Hq=32, Hkv=8, d=128, dtype=0):
+    sh = lamp.LampShapes()
+    sh.batch, sh.seqlen, sh.heads_q, sh.heads_kv, sh.head_dim = B, N, Hq, Hkv, d
+    sh.q_stride[:] = [N * Hq * d, Hq * d, d]
+    sh.o_stride[:] = [N * Hq * d, Hq * d, d]
+    sh.k_stride[:] = [N * Hkv * d, Hkv * d, d]
+    sh.v_stride[:] = [N * Hkv * d, Hkv * d, d]
+    sh.in_dtype = dtype
+    sh.out_dtype = 0
+    return sh
+
+
+def test_workspace_bytes(lib):
+    sh = _shapes()
+    n = lib.lamp_attn_workspace_bytes(ctypes.byref(sh))
+    B, N, Hq, Hkv, d = 4, 4096, 32, 8, 128
+    expect = B * Hq * N * d + B * Hkv * N * d + 2 * B * Hkv * N * d + 4 * B * Hq * N + 4 * B * Hkv * 64
+    assert expect <= n <= expect + 4096
+    sh.head_dim = 96
+    assert lib.lamp_attn_workspace_bytes(ctypes.byref(sh)) == 0
+    sh = _shapes(dtype=1)
+    assert lib.lamp_attn_workspace_bytes(ctypes.byref(sh)) > n
+
+
+def _call(lib, sh, ptrs=(16, 32, 48, 64), mask=1, delta=2 ** -8, tau=0.5):
+    st = lamp.LampStats()
+    return lib.lamp_attn_fwd(*ptrs, None, ctypes.byref(sh), mask, delta, tau, ctypes.byref(st))
+
+
+def test_argument_errors_before_launch(lib):
+    assert _call(lib, _shapes(), ptrs=(None, 32, 48, 64)) == lamp.LAMP_ERR_INVALID_ARG
+    sh = _shapes(Hq=6, Hkv=4)
+    assert _call(lib, sh) == lamp.LAMP_ERR_INVALID_ARG
+    assert _call(lib, _shapes(d=96)) == lamp.LAMP_ERR_UNSUPPORTED
+    assert _call(lib, _shapes(), mask=7) == lamp.LAMP_ERR_INVALID_ARG
+    assert _call(lib, _shapes(), mask=2) == lamp.LAMP_ERR_INVALID_ARG  # window 0
+    assert _call(lib, _shapes(), delta=-1.0) == lamp.LAMP_ERR_INVALID_ARG
+    assert _call(lib, _shapes(), tau=float("nan")) == lamp.LAMP_ERR_INVALID_ARG
+    sh = _shapes()
+    sh.q_stride[1] = 4097  # not a multiple of 16 bytes
+    assert _call(lib, sh) == lamp.LAMP_ERR_INVALID_ARG
+    assert _call(lib, _shapes(), ptrs=(17, 32, 48, 64)) == lamp.LAMP_ERR_INVALID_ARG
+    sh = _shapes()
+    sh.seqlen = 0
+    assert _call(lib, sh) == lamp.LAMP_ERR_INVALID_ARG
+
+
+def test_no_device_is_an_error_not_a_fallback(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid arguments on a machine without an sm_103 GPU: error, no CPU path
+    assert _call(lib, _shapes()) in (lamp.LAMP_ERR_CUDA, lamp.LAMP_ERR_UNSUPPORTED)

@@ -1,0 +1,126 @@
+"""GPU path vs the CPU oracle on identical seeded inputs: mask bytes and
+counters bit-exact, out within 2e-3 (plus half an output ulp for bf16
+output) and LSE within 1e-3; FP64 attention errors reported."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixed_precision_flashattention_gb300 import synth
+from tests import golden_inputs
+from tests.gpu_helpers import assert_close, run_gpu, to_device, values
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare(q, k, v, dtype, out_dtype=None, mask="causal", window=0, delta=2.0 ** -8, tau=0.5,
+             force="off", fp64_gate=False):
+    out_dtype = out_dtype or dtype
+    qd, kd, vd = to_device(q, k, v, dtype)
+    go, gl, gm, gc = run_gpu(qd, kd, vd, mask=mask, window=window, delta=delta, tau=tau, force=force,
+                             out_dtype=gpu_dt(out_dtype))
+    qv, kv, vv = values(qd), values(kd), values(vd)
+    ref = oracle.lamp_forward(qv, kv, vv, mask=mask, window=window, delta=delta, tau=tau, force=force,
+                              out_dtype=out_dtype)
+    assert gc[9] == 0, f"device status {gc[9]}"
+    mism = np.argwhere(gm != ref.mask)
+    assert mism.size == 0, f"{len(mism)} mask bytes differ, first {mism[:5].tolist()} " \
+                           f"gpu {[int(gm[tuple(i)]) for i in mism[:5]]} ref {[int(ref.mask[tuple(i)]) for i in mism[:5]]}"
+    assert list(gc[:8]) == list(ref.counters[:8]), (gc[:11], ref.counters[:8])
+    eo, el = assert_close(go, gl, ref, out_dtype)
+    o64, l64 = oracle.fp64_attention(qv, kv, vv, mask=mask, window=window)
+    e64o = float(np.abs(go - o64).max())
+    fin = np.isfinite(l64)
+    e64l = float(np.abs(gl[fin] - l64[fin]).max())
+    print(f"vs oracle: out {eo:.2e} lse {el:.2e} | vs fp64: out {e64o:.2e} lse {e64l:.2e} | "
+          f"fixups {gc[8]} flagged {gc[6]}/{gc[4]}")
+    if fp64_gate:
+        assert e64o <= 2e-3 + (2.0 ** -8 if out_dtype == "bf16" else 0.0) and e64l <= 1e-3
+    return gc, ref
+
+
+def gpu_dt(name):
+    return {"bf16": torch.bfloat16, "fp32": torch.float32}[name]
+
+
+def test_golden_detector_example():
+    fx = golden_inputs.load("detector_2tile.json")
+    q, k, v = golden_inputs.detector_2tile_inputs(fx)
+    for case in fx["cases"]:
+        qd, kd, vd = to_device(q, k, v, "fp32")
+        go, gl, gm, gc = run_gpu(qd, kd, vd, mask="none", delta=case["delta"], tau=case["tau"],
+                                 out_dtype=torch.float32)
+        for i in range(2):
+            assert list(gm[0, 0, i]) == case["mask"], case
+        assert list(gc[1:4]) == [2 * h for h in case["hist"]]
+
+
+@pytest.mark.parametrize("force", ["off", "all16", "all8"])
+def test_tiny_workload(force):
+    q, k, v = synth.make("tiny")
+    _compare(q, k, v, "fp32", force=force)
+
+
+@pytest.mark.parametrize("t", range(6))
+def test_tau_sweep_outlier_sink(t):
+    q, k, v = synth.gen_outlier_sink(1, 512, 4, 1, 128, seed=21)
+    _compare(q, k, v, "bf16", tau=2.0 ** -t)
+
+
+@pytest.mark.parametrize("delta", [2.0 ** -4, 0.0])
+def test_delta_and_disabled_first_stage(delta):
+    q, k, v = synth.gen_outlier_sink(1, 384, 2, 1, 128, seed=22)
+    _compare(q, k, v, "bf16", delta=delta)
+
+
+CASES = [
+    # N, Hq, Hkv, d, mask, window, dtype, out_dtype, generator
+    (200, 2, 1, 64, "causal", 0, "fp32", "fp32", "tiny"),
+    (130, 4, 2, 128, "none", 0, "bf16", "bf16", "iid"),
+    (333, 2, 2, 128, "sliding", 70, "bf16", "fp32", "outlier_sink"),
+    (65, 2, 1, 256, "causal", 0, "bf16", "bf16", "outlier_sink"),
+    (300, 2, 1, 256, "sliding", 100, "bf16", "fp32", "outlier_sink"),
+    (1, 1, 1, 128, "causal", 0, "bf16", "bf16", "iid"),
+    (64, 1, 1, 64, "causal", 0, "fp32", "fp32", "iid"),
+    (129, 3, 1, 64, "none", 0, "bf16", "fp32", "tiny"),
+    (512, 2, 1, 128, "causal", 0, "bf16", "bf16", "clustered"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
+def test_shapes_masks_dtypes(case):
+    N, Hq, Hkv, d, mask, window, dtype, out_dtype, gen = case
+    q, k, v = synth.GENERATORS[gen](2 if N < 200 else 1, N, Hq, Hkv, d, seed=N + d)
+    _compare(q, k, v, dtype, out_dtype=out_dtype, mask=mask, window=window)
+
+
+def test_all16_matches_fp64_on_iid():
+    q, k, v = synth.gen_iid(1, 256, 2, 1, 128, seed=31)
+    _compare(q, k, v, "bf16", out_dtype="fp32", force="all16", fp64_gate=True)
+
+
+def test_qwen3_8b_full_size_sampled():
+    """The bench's launch (B4 N4096 Hq32 Hkv8 d128 causal bf16) checked on
+    sampled query tiles the oracle computes one by one."""
+    w = synth.WORKLOADS["qwen3_8b"]
+    q, k, v = synth.make(w)
+    qd, kd, vd = to_device(q, k, v, "bf16")
+    go, gl, gm, gc = run_gpu(qd, kd, vd, mask="causal", tau=0.5)
+    assert gc[9] == 0
+    rng = np.random.default_rng(5)
+    T = w.seqlen // 64
+    tiles = [(0, 0, 0), (3, 31, T - 1), (1, 7, T // 2), (2, 16, 1)]
+    tiles += [(int(rng.integers(w.batch)), int(rng.integers(w.heads_q)), int(rng.integers(T))) for _ in range(8)]
+    qv, kv, vv = values(qd), values(kd), values(vd)
+    ref = oracle.lamp_forward(qv, kv, vv, mask="causal", tau=0.5, tiles=tiles)
+    for b, h, i in tiles:
+        assert np.array_equal(gm[b, h, i], ref.mask[b, h, i]), (b, h, i)
+        rows = slice(64 * i, 64 * i + 64)
+        sub = type("R", (), {})()
+        sub.out = ref.out[b, rows, h][None]
+        sub.lse = ref.lse[b, h, rows][None]
+        assert_close(go[b, rows, h][None], gl[b, h, rows][None], sub, "bf16")
+    # totals that hold at any size: the histogram partitions the visited tiles
+    assert gc[0] == gc[1] + gc[2] + gc[3] == w.batch * w.heads_q * T * (T + 1) // 2
+    assert gc[4] == 4 * gc[0] and gc[6] <= gc[5] <= gc[4]
+    print("qwen3_8b counters", gc[:11].tolist())
