@@ -47,8 +47,13 @@ typedef enum {
   LAMP_ERR_UNSUPPORTED = 2,  /* head_dim not in {64,128,256}, or not an sm_103 device */
   LAMP_ERR_CUDA = 3,         /* a CUDA runtime / driver call failed */
   LAMP_ERR_TIMEOUT = 4,      /* a device-side wait hit its time limit (status word) */
-  LAMP_ERR_WORKSPACE = 5     /* caller workspace smaller than lamp_attn_workspace_bytes() */
+  LAMP_ERR_WORKSPACE = 5,    /* caller workspace smaller than lamp_attn_workspace_bytes() */
+  LAMP_ERR_TOO_LARGE = 6     /* lamp_attn_fwd_noalloc: the shapes need more scratch than
+                                LAMP_NOALLOC_SCRATCH_BYTES */
 } lamp_status;
+
+/* Size of the fixed device array behind lamp_attn_fwd_noalloc (32 MiB). */
+#define LAMP_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 typedef enum {
   LAMP_MASK_NONE = 0,    /* every key visible to every query */
@@ -137,6 +142,33 @@ int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out,
  * copies of q and k, an fp16 copy of v, bf16 copies of fp32 inputs, and
  * per-row norms).  0 on invalid shapes. */
 size_t lamp_attn_workspace_bytes(const lamp_shapes* shapes);
+
+/*
+ * lamp_attn_fwd_noalloc: the same forward pass as lamp_attn_fwd, for callers
+ * that must not allocate device memory during the call -- e.g. a plug-in of
+ * a host framework that owns all device memory through its own pooling
+ * allocator (raw cudaMalloc/cudaFree would bypass it, and cudaFree
+ * synchronises the device), or a latency-bound serving loop that must stay
+ * free of implicit synchronisation.  The paper has no counterpart: this is
+ * a memory-management variant only.
+ *
+ * Arguments, layouts and results are those of lamp_attn_fwd; the caller
+ * still passes inputs, outputs and (optionally) stats.  shapes->workspace
+ * and workspace_bytes are ignored: the scratch is a file-scope device array
+ * of LAMP_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds
+ * until process exit.  Shapes whose lamp_attn_workspace_bytes() exceeds it
+ * are rejected with LAMP_ERR_TOO_LARGE before anything is enqueued.  No
+ * cudaMalloc, cudaFree or other allocating call is made.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress with that device current); make that first call
+ * before any stream capture.  All calls share the array and it keeps the
+ * last call's contents (each call clears what must start at zero); calls
+ * whose work overlaps on the GPU race on it and must be serialised.
+ */
+int lamp_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out,
+                          float* lse, const lamp_shapes* shapes, int mask_kind,
+                          float delta, float tau, lamp_stats* stats);
 
 /* Static, human-readable text for a lamp_status value. */
 const char* lamp_strerror(int status);

@@ -125,6 +125,7 @@ const char* lamp_strerror(int status) {
     case LAMP_ERR_CUDA: return "CUDA runtime or driver error";
     case LAMP_ERR_TIMEOUT: return "a device-side wait exceeded its time limit";
     case LAMP_ERR_WORKSPACE: return "workspace smaller than lamp_attn_workspace_bytes()";
+    case LAMP_ERR_TOO_LARGE: return "shapes need more scratch than lamp_attn_fwd_noalloc's fixed array (LAMP_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status";
   }
 }

@@ -1,0 +1,65 @@
+// lamp_noalloc.cu -- lamp_attn_fwd_noalloc: the forward pass with its
+// scratch in a fixed, file-scope device array instead of caller- or
+// call-allocated workspace.
+//
+// Who needs it: callers that must not allocate device memory while they
+// run -- for example a plug-in inside a host framework that owns all device
+// memory through its own pooling allocator (a raw cudaMalloc/cudaFree would
+// bypass its accounting and cudaFree synchronises the device), or a
+// latency-bound serving loop that has to keep every call free of implicit
+// synchronisation.  Such callers pass only inputs and outputs.
+//
+// Cost: the array (LAMP_NOALLOC_SCRATCH_BYTES) lives on every GPU that
+// loads this library, until the process exits.  All calls share it and it
+// keeps the last call's contents; the pre-pass rewrites the 8/16-bit copies
+// and norms in full and every call clears the parts that must start at zero
+// (per-tile key norms, abort word) before its kernels run.  Two calls whose
+// work overlaps on the GPU (different streams, or different host threads
+// on one device) race on the array: serialise them.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/lamp_attn.h"
+
+namespace {
+
+__device__ __align__(256) static unsigned char g_noalloc_scratch[LAMP_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_ptr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of the array on the current device.  In host code the
+// array's name only stands in for the symbol; the address has to come from
+// cudaGetSymbolAddress with that device current (once per device).
+int scratch_on_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LAMP_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return LAMP_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return LAMP_OK;
+}
+
+}  // namespace
+
+extern "C" int lamp_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
+                                     const lamp_shapes* shapes, int mask_kind, float delta, float tau,
+                                     lamp_stats* stats) {
+  if (!shapes) return LAMP_ERR_INVALID_ARG;
+  const size_t need = lamp_attn_workspace_bytes(shapes);
+  if (need == 0) return LAMP_ERR_INVALID_ARG;
+  if (need > (size_t)LAMP_NOALLOC_SCRATCH_BYTES) return LAMP_ERR_TOO_LARGE;
+  void* scratch = nullptr;
+  const int st = scratch_on_current_device(&scratch);
+  if (st != LAMP_OK) return st;
+  lamp_shapes s = *shapes;
+  s.workspace = scratch;
+  s.workspace_bytes = (size_t)LAMP_NOALLOC_SCRATCH_BYTES;
+  return lamp_attn_fwd(q, k, v, out, lse, &s, mask_kind, delta, tau, stats);
+}

@@ -14,15 +14,17 @@ import torch
 
 from . import build as _build
 
-LAMP_OK, LAMP_ERR_INVALID_ARG, LAMP_ERR_UNSUPPORTED, LAMP_ERR_CUDA, LAMP_ERR_TIMEOUT, LAMP_ERR_WORKSPACE = range(6)
+(LAMP_OK, LAMP_ERR_INVALID_ARG, LAMP_ERR_UNSUPPORTED, LAMP_ERR_CUDA, LAMP_ERR_TIMEOUT, LAMP_ERR_WORKSPACE,
+ LAMP_ERR_TOO_LARGE) = range(7)
+NOALLOC_SCRATCH_BYTES = 32 << 20
 MASK = {"none": 0, "causal": 1, "sliding": 2}
 FORCE = {"off": 0, "all16": 1, "all8": 2}
 DT = {torch.bfloat16: 0, torch.float32: 1}
 NUM_COUNTERS = 16
 COUNTER_NAMES = ["tiles", "hist0", "hist1", "hist2p", "strips", "stage1", "flagged",
                  "s8_saturated", "fixups", "status", "recompute_steps"]
-EXPORTS = ["lamp_attn_fwd", "lamp_attn_workspace_bytes", "lamp_strerror", "lamp_version",
-           "lamp_selftest"]
+EXPORTS = ["lamp_attn_fwd", "lamp_attn_fwd_noalloc", "lamp_attn_workspace_bytes", "lamp_strerror",
+           "lamp_version", "lamp_selftest"]
 
 
 class LampShapes(ctypes.Structure):
@@ -68,6 +70,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.lamp_attn_fwd.argtypes = [ctypes.c_void_p] * 4 + [
         ctypes.c_void_p, ctypes.POINTER(LampShapes), ctypes.c_int, ctypes.c_float, ctypes.c_float,
         ctypes.POINTER(LampStats)]
+    lib.lamp_attn_fwd_noalloc.restype = ctypes.c_int
+    lib.lamp_attn_fwd_noalloc.argtypes = lib.lamp_attn_fwd.argtypes
     lib.lamp_attn_workspace_bytes.restype = ctypes.c_size_t
     lib.lamp_attn_workspace_bytes.argtypes = [ctypes.POINTER(LampShapes)]
     lib.lamp_strerror.restype = ctypes.c_char_p
