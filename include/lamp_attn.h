@@ -81,7 +81,9 @@ enum {
   LAMP_CNT_SAT = 7,         /* visible logits with |S8| = 448 */
   LAMP_CNT_FIXUPS = 8,      /* logits re-derived exactly (near an 8-bit rounding boundary) */
   LAMP_CNT_STATUS = 9,      /* device-side status (lamp_status), 0 = ok */
-  LAMP_CNT_RECOMP_STEPS = 10, /* 128x64 kernel steps that ran the 16-bit recompute MMA */
+  LAMP_CNT_RECOMP_STEPS = 10, /* 128x64 kernel steps whose 16-bit recompute was used */
+  LAMP_CNT_SPEC_WASTE = 11, /* 16-bit recompute MMAs issued ahead (the previous step
+                               needed one) whose step then needed none */
   LAMP_NUM_COUNTERS = 16
 };
 
@@ -173,8 +175,14 @@ int lamp_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out
 /* Static, human-readable text for a lamp_status value. */
 const char* lamp_strerror(int status);
 
-/* Library version string, e.g. "lamp-attn 0.1 sm_103a". */
+/* Library version string, e.g. "lamp-attn 0.2 sm_103a". */
 const char* lamp_version(void);
+
+/* The 8-bit exponential the kernels use, as a table (host memory, 256
+ * bytes): out[c] = E4M3 code of fl8(exp(x)) for the E4M3 code c of x (round
+ * to nearest even, saturating; 0 for the NaN codes).  Abstract of the paper:
+ * exponentials evaluated in 8-bit formats.  For diagnostics and tests. */
+void lamp_exp8_table(uint8_t out[256]);
 
 /*
  * lamp_selftest: device checks of the tensor-core building blocks used by

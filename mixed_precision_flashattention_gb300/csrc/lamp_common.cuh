@@ -12,8 +12,10 @@ namespace lamp {
 constexpr int kBM = 128;        // query rows per CTA (one TMEM lane per row)
 constexpr int kBN = 64;         // keys per step = one 64-key tile of the method
 constexpr int kStrip = 16;      // query rows per sub-block
-constexpr int kSoftmaxThreads = 128;
-constexpr int kThreads = 192;   // 4 softmax warps + TMA warp + MMA warp
+constexpr int kSoftmaxWarps = 8;    // two warps (column halves) per 32 query rows
+constexpr int kSoftmaxThreads = 256;
+constexpr int kThreads = 320;       // 8 softmax warps + TMA warp + MMA warp
+constexpr int kNC = 32;             // logits per softmax thread per step
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Kernel parameters (passed by value as a __grid_constant__).
@@ -33,6 +35,7 @@ struct FwdParams {
   float guard;         // relative bound on |y_tc - y| per unit sigma*|q|*|k|
   float tau_abs;       // flag iff |S8| >= tau_abs (derived from tau)
   uint32_t delta_code; // stage 1 iff P8 code >= delta_code
+  uint8_t exp8[256];   // code of fl8(exp(x)) for every E4M3 code x
   unsigned long long timeout_ns;  // a wait gives up after this long
   unsigned int* gabort;           // grid-wide abort word (workspace, zeroed per call)
 };
@@ -87,6 +90,43 @@ __device__ __forceinline__ float e4m3_rne_from_double(double y) {
     r = (float)(v > 448.0 ? 448.0 : v);
   }
   return y < 0.0 ? -r : r;
+}
+
+// Host: E4M3 code of the round-to-nearest-even, saturating conversion of a
+// double (written from the format definition; NaN -> 0x7F).
+inline uint8_t host_e4m3_encode(double x) {
+  if (x != x) return 0x7F;
+  const uint8_t sign = x < 0 ? 0x80 : 0x00;
+  double a = x < 0 ? -x : x;
+  if (a >= 448.0) return sign | 0x7E;
+  if (a == 0.0) return sign;
+  int e = 0;
+  (void)frexp(a, &e);        // a = f * 2^e, f in [0.5, 1)
+  int E = e - 1;             // floor(log2 a)
+  if (E < -6) E = -6;
+  const double n = nearbyint(ldexp(a, 3 - E));  // RNE at the spacing 2^(E-3)
+  int ni = (int)n;
+  if (E == -6 && ni < 8) return sign | (uint8_t)ni;   // subnormal
+  if (ni == 16) { ni = 8; ++E; }
+  if (E > 8 || (E == 8 && ni > 14)) return sign | 0x7E;
+  return sign | (uint8_t)(((E + 7) << 3) | (ni - 8));
+}
+
+inline double host_e4m3_decode(uint8_t c) {
+  const int e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return 0.0 / 0.0;
+  const double v = e ? ldexp(1.0 + m / 8.0, e - 7) : ldexp((double)m, -9);
+  return (c & 0x80) ? -v : v;
+}
+
+// exp8 table: code of fl8(exp(x)) for each E4M3 code x.  The double exp is
+// far closer than the smallest distance (2^-11 relative) of e^x to an E4M3
+// rounding boundary for the codes that matter, so this is correctly rounded.
+inline void host_exp8_table(uint8_t* t) {
+  for (int c = 0; c < 256; ++c) {
+    const double x = host_e4m3_decode((uint8_t)c);
+    t[c] = (x != x) ? 0 : host_e4m3_encode(exp(x));
+  }
 }
 
 // Smallest non-negative E4M3 magnitude whose half-spacing is >= tau

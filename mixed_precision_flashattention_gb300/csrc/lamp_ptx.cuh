@@ -4,6 +4,8 @@
 #pragma once
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_fp16.h>
+#include <cstring>
 
 namespace lamp {
 
@@ -189,6 +191,14 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float a, float b) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(a), "f"(b));
   return r;
+}
+// f16x2 -> two E4M3 codes (RNE, saturating): hi byte <- hi half.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(__half2 h) {
+  uint16_t r;
+  uint32_t u;
+  memcpy(&u, &h, 4);
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(u));
+  return (uint32_t)r;
 }
 // Two E4M3 codes -> f16x2 (exact).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t c) {

@@ -22,9 +22,9 @@ FORCE = {"off": 0, "all16": 1, "all8": 2}
 DT = {torch.bfloat16: 0, torch.float32: 1}
 NUM_COUNTERS = 16
 COUNTER_NAMES = ["tiles", "hist0", "hist1", "hist2p", "strips", "stage1", "flagged",
-                 "s8_saturated", "fixups", "status", "recompute_steps"]
+                 "s8_saturated", "fixups", "status", "recompute_steps", "spec_waste"]
 EXPORTS = ["lamp_attn_fwd", "lamp_attn_fwd_noalloc", "lamp_attn_workspace_bytes", "lamp_strerror",
-           "lamp_version", "lamp_selftest"]
+           "lamp_version", "lamp_exp8_table", "lamp_selftest"]
 
 
 class LampShapes(ctypes.Structure):
@@ -77,6 +77,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.lamp_strerror.restype = ctypes.c_char_p
     lib.lamp_strerror.argtypes = [ctypes.c_int]
     lib.lamp_version.restype = ctypes.c_char_p
+    lib.lamp_exp8_table.restype = None
+    lib.lamp_exp8_table.argtypes = [ctypes.c_void_p]
     lib.lamp_selftest.restype = ctypes.c_int
     lib.lamp_selftest.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_int, ctypes.c_void_p]
@@ -155,6 +157,13 @@ def new_stats(B, Hq, N, device="cuda"):
     T = (N + 63) // 64
     return (torch.zeros((B, Hq, T, T), dtype=torch.uint8, device=device),
             torch.zeros(NUM_COUNTERS, dtype=torch.int64, device=device))
+
+
+def exp8_table() -> bytes:
+    """The library's 8-bit exponential table (host; no GPU needed)."""
+    buf = (ctypes.c_uint8 * 256)()
+    load().lamp_exp8_table(ctypes.cast(buf, ctypes.c_void_p))
+    return bytes(buf)
 
 
 def selftest(which: int, a, b, d: int):

@@ -91,3 +91,30 @@ def test_no_device_is_an_error_not_a_fallback(lib):
         pytest.skip("a GPU is present")
     # valid arguments on a machine without an sm_103 GPU: error, no CPU path
     assert _call(lib, _shapes()) in (lamp.LAMP_ERR_CUDA, lamp.LAMP_ERR_UNSUPPORTED)
+
+
+def test_library_exp8_table_matches_oracle(lib):
+    """The kernels' 8-bit exponential (built by the library's own host code)
+    equals the oracle's fl8(exp(x)) on every E4M3 input code."""
+    import numpy as np
+    from oracle import formats as F
+    tab = np.frombuffer(lamp.exp8_table(), dtype=np.uint8)
+    for c in range(256):
+        x = F.E4M3_TABLE[c]
+        if np.isnan(x):
+            assert tab[c] == 0
+            continue
+        expect = F.e4m3_encode(F.exp8(x)) if x <= 88 else F.e4m3_encode(448.0)
+        assert tab[c] == expect, (hex(c), x, tab[c], expect)
+
+
+def test_fp16_difference_then_e4m3_is_exact():
+    """The kernel forms x8 = fl8(S8 - m) as fl8(fp16(S8 - m)): for every pair
+    of E4M3 values the double rounding equals the single rounding (fp16 has
+    11 >= 2*4+1 significant bits; small differences are exact in fp16)."""
+    import numpy as np
+    from oracle import formats as F
+    v = F.E4M3_TABLE[np.isfinite(F.E4M3_TABLE)]
+    s, m = np.meshgrid(v, v)
+    d16 = (s.astype(np.float16) - m.astype(np.float16)).astype(np.float64)  # RN to fp16
+    assert np.array_equal(F.e4m3_round(d16), F.e4m3_round(s - m))

@@ -124,3 +124,22 @@ def test_qwen3_8b_full_size_sampled():
     assert gc[0] == gc[1] + gc[2] + gc[3] == w.batch * w.heads_q * T * (T + 1) // 2
     assert gc[4] == 4 * gc[0] and gc[6] <= gc[5] <= gc[4]
     print("qwen3_8b counters", gc[:11].tolist())
+
+
+@pytest.mark.parametrize("tau,delta", [(2.0 ** -12, 2.0 ** -8), (0.0, 2.0 ** -8), (-1.0, 2.0 ** -8),
+                                       (32.0, 2.0 ** -8), (0.5, 0.0), (2.0 ** -12, 0.0), (0.5, 2.0),
+                                       (2.0 ** -5, 2.0 ** -8), (2.0 ** -3, 0.0115)])
+def test_threshold_edges(tau, delta):
+    """tau below the smallest half-spacing, tau <= 0 (every stage-1
+    sub-block flags), tau above the largest, delta = 0 (first stage off),
+    delta > 1 (nothing passes stage 1), a delta that is no E4M3 value."""
+    q, k, v = synth.gen_tiny(1, 200, 2, 1, 64, seed=61)
+    _compare(q, k, v, "fp32", tau=tau, delta=delta)
+
+
+@pytest.mark.parametrize("t", [1, 3, 5])
+def test_small_logits_negative_maxima(t):
+    """Logits of small magnitude: running maxima near or below zero, where
+    negative logits decide the flags."""
+    q, k, v = synth.gen_iid(1, 320, 2, 1, 128, seed=62, scale=0.35)
+    _compare(q, k, v, "bf16", tau=2.0 ** -t, mask="sliding", window=150)
