@@ -107,13 +107,11 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volati
                                            volatile unsigned int* gabort, unsigned long long timeout_ns,
                                            unsigned long long* counters) {
   const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0u) {
-      if (*abort) return false;
-      if (*gabort) { *abort = 1u; return false; }
-      if (globaltimer_ns() - t0 > timeout_ns) break;
-    }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;  // suspended, not spinning
+    if (*abort) return false;
+    if (*gabort) { *abort = 1u; return false; }
+    if (globaltimer_ns() - t0 > timeout_ns) break;
   }
   *abort = 1u;
   atomicExch((unsigned int*)gabort, 1u);
