@@ -110,7 +110,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
@@ -135,6 +135,32 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+KERNEL_SOURCES = ["mixed_precision_flashattention_gb300/csrc/lamp_fwd.cu",
+                  "mixed_precision_flashattention_gb300/csrc/lamp_common.cuh",
+                  "mixed_precision_flashattention_gb300/csrc/lamp_ptx.cuh"]
+
+
+def kernel_source_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu
+    capture, if it was taken on this workload with the current kernel source
+    (else None)."""
+    path = os.path.join(ROOT, "profiles", "lamp_fwd_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    if d.get("workload") != workload or d.get("source_sha") != kernel_source_sha():
+        return None
+    return float(d["dram_bytes_read"]) + float(d["dram_bytes_write"])
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -147,7 +173,7 @@ def _peaks():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="lamp", choices=["lamp", "reference"])
     ap.add_argument("--workload", default="qwen3_8b", choices=sorted(synth.WORKLOADS))
@@ -304,7 +330,7 @@ def main():
         "config": {**config, "l2": "flushed between steps (256 MB write), per-step CUDA events"},
         "fp8_peak_frac": flops / (ms * 1e-3) / 1e12 / fp8_peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": achieved / fp8_peak, "traffic": None,
+                     "frac": achieved / fp8_peak, "traffic": _traffic(w.name),
                      "kernel": "lamp_fwd_kernel", "peak_basis": f"2 x {peak_src} bf16 burst {bf16_peak} (dense FP8:BF16 = 2)",
                      "mixed_tc_time_frac": t_tc / (ms_main * 1e-3)},
         "ms_main_kernel": ms_main, "ms_prepass": statistics.mean(t_prep), "wall_s": t_wall,

@@ -190,7 +190,7 @@ void lamp_exp8_table(uint8_t out[256]);
  * same shared-memory layouts and instruction sequences:
  *   which 0: out[128 x 64]    = A . B^T, A [128 x d], B [64 x d] E4M3 codes (uint8)
  *   which 1: out[128 x 64]    = A . B^T, A [128 x d], B [64 x d] BF16
- *   which 2: out[128 x (d+16)] = P . [V | 1], P [128 x 64], V [64 x d] FP16
+ *   which 2: out[128 x d]      = P . V, P [128 x 64], V [64 x d] FP16 (V MN-major)
  * a, b: DEVICE, row-major as listed; out: DEVICE float32, row-major.
  * Returns LAMP_OK or an error code after synchronising `stream`.
  */

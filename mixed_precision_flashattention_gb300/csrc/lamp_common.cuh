@@ -162,7 +162,7 @@ inline uint32_t host_delta_code(float delta) {
 //   16-bit    [rows x D] BF16/FP16, K-major: D/64 atom columns of
 //             [rows x 128 B], 128-byte swizzle.
 //   V         [64 keys x D] FP16, MN-major: D/64 regions of [64 keys x 128 B]
-//             (64 values of d per key row), then one region of ones.
+//             (64 values of d per key row).
 template <int D>
 struct Mma {
   static constexpr int F8_ROW = (D == 64) ? 64 : 128;
@@ -190,20 +190,14 @@ struct Mma {
       mma_f16(tmem_d, ad, bd, idesc, kk > 0);
     }
   }
-  // O[128 x (D+16)] (+)= P[128 x 64] . [V | 1][64 x (D+16)]  (FP16)
+  // O[128 x D] (+)= P[128 x 64] . V[64 x D]  (FP16 operands, FP32 accumulation)
   static __device__ __forceinline__ void pv(uint32_t tmem_o, uint32_t pbase, uint32_t vbase, bool acc) {
-    constexpr int N1 = (D + 16 <= 256) ? D + 16 : 256;
-    constexpr uint32_t idesc1 = make_idesc(0, 0, 1, 128, N1);
-    constexpr uint32_t idesc2 = make_idesc(0, 0, 1, 128, 16);
+    constexpr uint32_t idesc_v = make_idesc(0, 0, 1, 128, D);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t ad = make_sdesc(pbase + kk * 32, 16, 1024, kLayoutSW128);
       const uint64_t bd = make_sdesc(vbase + kk * 16 * 128, 64 * 128, 1024, kLayoutSW128);
-      mma_f16(tmem_o, ad, bd, idesc1, acc || kk > 0);
-      if (D + 16 > 256) {
-        const uint64_t bd2 = make_sdesc(vbase + (D / 64) * 64 * 128 + kk * 16 * 128, 64 * 128, 1024, kLayoutSW128);
-        mma_f16(tmem_o + 256, ad, bd2, idesc2, acc || kk > 0);
-      }
+      mma_f16(tmem_o, ad, bd, idesc_v, acc || kk > 0);
     }
   }
 };

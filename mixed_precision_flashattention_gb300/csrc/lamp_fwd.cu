@@ -1,19 +1,24 @@
 // lamp_fwd.cu -- fused LampAttention forward kernel for sm_103a.
 //
-// One CTA computes 128 query rows of one (batch, query head) against the
-// visible 64-key tiles, in ascending key order (the running maximum of the
-// method is defined over that order).  Warp roles:
-//   warps 0-3  softmax: thread t owns query row t (TMEM lane t).  Per step:
-//              8-bit logits S8 (with an exactness guard), running max,
-//              x8 / P8 = fl8(exp(x8)), two-stage detector, sub-block flags,
-//              mask byte + histogram, FP16 P (P8, or P16 for flagged rows),
-//              O rescale in TMEM.
-//   warp 4     TMA producer: Q8/Q16 once, then K8/K16/V16 per step into a
-//              ring of stages.
-//   warp 5     TMEM owner and MMA issuer: S = Q8 K8^T (kind::f8f6f4),
-//              S16 = Q16 K16^T (kind::f16, only when some sub-block of the
-//              step is flagged), O += P V16 (kind::f16, V MN-major, plus a
-//              block of ones so that column d of O accumulates l = sum P).
+// One CTA computes NT query tiles of 128 rows (NT = 2 for d <= 128, 1 for
+// d = 256) of one (batch, query head) against their visible 64-key tiles,
+// in ascending key order (the running maximum of the method is defined
+// over that order).  The tiles share the K/V stages and ping-pong: while
+// the softmax warps of one tile work, the tensor core serves the other.
+// Warp roles:
+//   warps 8t..8t+7  softmax of tile t: two threads per query row (warps
+//              8t+w and 8t+4+w hold TMEM lanes 32w.. for key columns 0-31
+//              and 32-63 of each step).  Per step: 8-bit logits S8 (with an
+//              exactness guard), running max, the two-stage detector,
+//              sub-block flags, mask byte + histogram, FP16 P (P8 from a
+//              table of exact 8-bit exponentials, or P16 for flagged rows),
+//              O rescale in TMEM, the row sum l in registers.
+//   warp 8*NT  TMA producer: Q8/Q16 of every tile once, then K8/K16/V16
+//              per step into a ring of stages.
+//   warp 8*NT+1  TMEM owner and MMA issuer: S = Q8 K8^T (kind::f8f6f4),
+//              S16 = Q16 K16^T (kind::f16, into the same TMEM columns once
+//              S8 has been read, only when a sub-block of the step is
+//              flagged), O += P V16 (kind::f16, V MN-major).
 //
 // The method follows "LampAttention: Look-Ahead Mixed-Precision
 // FlashAttention for Dedicated Accelerators" (abstract: 8-bit key-query
@@ -33,64 +38,58 @@ namespace lamp {
 
 template <int D>
 struct Cfg {
-  static constexpr int NS = (D == 256) ? 1 : 2;             // K/V stages
-  static constexpr int Q8_ROWB = D;                          // bytes per Q8/K8 row
-  static constexpr int F8_SWZ_ROW = (D == 64) ? 64 : 128;    // swizzle row width
+  static constexpr int NT = (D == 256) ? 1 : 2;  // query tiles of 128 rows per CTA
+  static constexpr int NS = (D == 256) ? 1 : 2;  // K/V stages
+  static constexpr int SM_THREADS = 256;                // softmax threads per tile (2 per row)
+  static constexpr int THREADS = 32 * (8 * NT + 2);
+  static constexpr int PRODUCER_WARP = 8 * NT, MMA_WARP = 8 * NT + 1;
+  static constexpr int F8_SWZ_ROW = (D == 64) ? 64 : 128;  // swizzle row width of 8-bit tiles
   static constexpr int Q8_BYTES = kBM * D;
   static constexpr int Q16_BYTES = kBM * D * 2;
+  static constexpr int QT_BYTES = Q8_BYTES + Q16_BYTES;  // per query tile
   static constexpr int K8_BYTES = kBN * D;
   static constexpr int K16_BYTES = kBN * D * 2;
-  static constexpr int V_REGIONS = D / 64 + 1;              // + block of ones
-  static constexpr int V_BYTES = V_REGIONS * kBN * 128;
+  static constexpr int V_BYTES = (D / 64) * kBN * 128;
   static constexpr int STAGE_BYTES = K8_BYTES + K16_BYTES + V_BYTES;
   static constexpr int P_BYTES = kBM * kBN * 2;
-  static constexpr int OFF_Q8 = 0;
-  static constexpr int OFF_Q16 = OFF_Q8 + Q8_BYTES;
-  static constexpr int OFF_ST = OFF_Q16 + Q16_BYTES;
-  static constexpr int OFF_P = OFF_ST + NS * STAGE_BYTES;
-  static constexpr int OFF_MISC = OFF_P + P_BYTES;
-  static constexpr int MISC_BYTES = 3072;
-  // + alignment slack; at least 116 KB so that one CTA owns an SM (and all
-  // of its TMEM)
-  static constexpr int SMEM_USED = OFF_MISC + MISC_BYTES + 1024;
-  static constexpr int SMEM = SMEM_USED > 116 * 1024 ? SMEM_USED : 116 * 1024;
-  // TMEM columns (fp32): O (d values + 16 columns of l), S ring, S16.
-  static constexpr int O_COLS = D + 16;
-  static constexpr int S_COL0 = ((O_COLS + 31) / 32) * 32;
-  static constexpr int S16_COL = S_COL0 + 2 * kBN;
-  // two S16 slots let the MMA warp issue the 16-bit recompute of step j+1
-  // speculatively (when step j needed one); d = 256 has room for one
-  static constexpr int NSLOT16 = (S16_COL + 2 * kBN <= 512) ? 2 : 1;
-  static constexpr bool SPEC16 = NSLOT16 == 2 && NS >= 2;
+  static constexpr int OFF_Q = 0;  // tile t: Q8 at t*QT_BYTES, Q16 right after
+  static constexpr int OFF_ST = NT * QT_BYTES;
+  static constexpr int OFF_P = OFF_ST + NS * STAGE_BYTES;  // tile t at + t*P_BYTES
+  static constexpr int OFF_MISC = OFF_P + NT * P_BYTES;
+  static constexpr int MISC_BYTES = 5120;
+  static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
+  // TMEM columns per tile (fp32): O (d values) and two 64-column S buffers;
+  // step j uses buffer j % 2 for S8's accumulator, then for S16's, so the
+  // QK8 of step j+1 can run while the softmax works on step j.
+  static constexpr int O_COLS = D;
+  static constexpr int S_OFF = D;
+  static constexpr int TILE_COLS = S_OFF + 2 * kBN;
   static constexpr int TMEM_COLS = 512;
-  static_assert(S16_COL + NSLOT16 * kBN <= TMEM_COLS, "TMEM budget");
+  static_assert(NT * TILE_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-// misc area (byte offsets inside OFF_MISC)
+// misc area (byte offsets inside OFF_MISC); per-tile barriers at + 8 * t
 enum : int {
-  M_KV_FULL = 0,      // [2] x 8 B
-  M_KV_EMPTY = 16,    // [2]
+  M_KV_FULL = 0,      // [2 stages]
+  M_KV_EMPTY = 16,    // [2 stages]
   M_Q_FULL = 32,
-  M_S_FULL = 40,      // [2]
-  M_S_EMPTY = 56,     // [2]
-  M_REC_REQ = 72,     // [2] per step parity: the decision of step j is published
-  M_S16_FULL = 88,    // [2] per S16 slot
-  M_S16_EMPTY = 104,  // [2] per S16 slot
-  M_P_FULL = 120,
-  M_PV_DONE = 128,
+  M_S_FULL = 40,      // [2 tiles][2 buffers] QK8 result in TMEM (at + 16 t + 8 buf)
+  M_DEC = 72,         // [2 tiles] the softmax published its recompute decision
+  M_S16_FULL = 88,    // [2 tiles] QK16 result in TMEM
+  M_P_FULL = 104,     // [2 tiles] P written, O rescaled, the step's S buffer free
+  M_PV_DONE = 120,    // [2 tiles]
   M_DRAIN = 136,
   M_TMEM = 144,       // u32 TMEM base address
   M_ABORT = 148,      // u32 abort flag
-  M_REC = 152,        // u32 [2] recompute decision per step parity
-  M_SFLAG = 160,      // u32 [2][4] per-warp strip bits
-  M_XCH = 256,        // f32 [2][128] per-row values exchanged between the two column halves
-  M_EXP8 = 1280,      // u8 [256] exp8 table: code of fl8(exp(x)) per code of x
-  M_XB = 1536,        // u32 [2][128] per-row bits exchanged between the two column halves
+  M_REC = 152,        // u32 [2 tiles] recompute decision of the current step
+  M_SFLAG = 160,      // u32 [2 tiles][2 step parities][4 warps] strip bits
+  M_EXP8 = 256,       // u8 [256] exp8 table: code of fl8(exp(x)) per code of x
+  M_XCH = 512,        // f32 [2 tiles][2 halves][128 rows] values exchanged between a row's two threads
+  M_XB = 2560,        // u32 [2 tiles][2 halves][128 rows] bits exchanged between a row's two threads
 };
 
 struct Ctx {
-  uint32_t misc;                 // shared address of the misc area
   volatile uint32_t* abort;      // CTA abort flag (shared memory)
   volatile unsigned int* gabort; // grid abort word (global memory)
   unsigned long long timeout_ns;
@@ -102,13 +101,14 @@ constexpr unsigned long long kDrainNs = 200000000ull;  // 0.2 s for in-flight co
 // Bounded wait: gives up after cx.timeout_ns, or as soon as this CTA or any
 // other CTA has given up; on expiry it raises both abort flags and writes
 // LAMP_ERR_TIMEOUT into the status counter.  The first probe is inline; the
-// spinning part is out of line and takes its state by value.
+// waiting part is out of line, suspends in hardware and takes its state by
+// value.
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
                                            volatile unsigned int* gabort, unsigned long long timeout_ns,
                                            unsigned long long* counters) {
   const unsigned long long t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;  // suspended, not spinning
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort) return false;
     if (*gabort) { *abort = 1u; return false; }
     if (globaltimer_ns() - t0 > timeout_ns) break;
@@ -124,17 +124,17 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, uint32_t bar, uint32_t p
   return wait_bar_slow(bar, parity, cx.abort, cx.gabort, cx.timeout_ns, cx.counters);
 }
 
+// Warp-uniform variant: every lane waits; true only if all lanes succeeded.
+__device__ __forceinline__ bool wait_bar_warp(const Ctx& cx, uint32_t bar, uint32_t parity) {
+  const bool okl = wait_bar(cx, bar, parity);
+  return __all_sync(0xffffffffu, okl);
+}
+
 // Wait used only to let this CTA's own copies and MMAs land before exit.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity))
     if (globaltimer_ns() - t0 > kDrainNs) return;
-}
-
-// Warp-uniform variant: every lane waits; true only if all lanes succeeded.
-__device__ __forceinline__ bool wait_bar_warp(const Ctx& cx, uint32_t bar, uint32_t parity) {
-  const bool okl = wait_bar(cx, bar, parity);
-  return __all_sync(0xffffffffu, okl);
 }
 
 __device__ __forceinline__ __half2 as_half2(uint32_t u) {
@@ -154,22 +154,26 @@ __device__ __forceinline__ void row_range(const FwdParams& p, int R, int& lo, in
   lo = (p.mask_kind == 2) ? imax(0, R - p.window + 1) : 0;
 }
 
-// Key-tile range [j_lo, j_hi) of the CTA with first row q0.
+// Key-tile range [j_lo, j_hi) of the 128-row query tile starting at row q0
+// (empty when q0 >= N).
 __device__ __forceinline__ void tile_range(const FwdParams& p, int q0, int& j_lo, int& j_hi) {
-  int last = imin(q0 + kBM - 1, p.N - 1);
+  if (q0 >= p.N) { j_lo = 0; j_hi = 0; return; }
+  const int last = imin(q0 + kBM - 1, p.N - 1);
   if (p.mask_kind == 0) { j_lo = 0; j_hi = p.T; return; }
   j_hi = last / kBN + 1;
   j_lo = (p.mask_kind == 2) ? imax(0, q0 - p.window + 1) / kBN : 0;
 }
 
-// Exact A * 2^18 of (row r, key c): integer dot product of the E4M3
-// operands in shared memory, split across the warp (every lane gets the sum).
+// Exact A * 2^18 of (row r of the tile's Q8, key c of the stage's K8):
+// integer dot product of the E4M3 operands in shared memory, split across
+// the warp (every lane gets the sum).
 template <int D>
 __device__ long long exact_dot(const uint8_t* sQ8, const uint8_t* sK8, int r, int c, int lane) {
+  constexpr int RB = (Cfg<D>::F8_SWZ_ROW == 64) ? 64 : D;
   long long acc = 0;
   for (int t = lane; t < D; t += 32) {
-    uint32_t qa = sQ8[swz_offset(r, t, kBM, Cfg<D>::F8_SWZ_ROW == 64 ? 64 : D)];
-    uint32_t kb = sK8[swz_offset(c, t, kBN, Cfg<D>::F8_SWZ_ROW == 64 ? 64 : D)];
+    const uint32_t qa = sQ8[swz_offset(r, t, kBM, RB)];
+    const uint32_t kb = sK8[swz_offset(c, t, kBN, RB)];
     acc += (long long)e4m3_to_int512(qa) * (long long)e4m3_to_int512(kb);
   }
 #pragma unroll
@@ -177,16 +181,18 @@ __device__ long long exact_dot(const uint8_t* sQ8, const uint8_t* sK8, int r, in
   return acc;
 }
 
+}  // namespace lamp
+
+namespace lamp {
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   // align by pointer arithmetic on the __shared__ array so that every access
   // through `smem` stays a shared-memory access
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  uint8_t* sQ8 = smem + C::OFF_Q8;
-  uint8_t* sP = smem + C::OFF_P;
   uint8_t* misc = smem + C::OFF_MISC;
   const uint32_t mb = sbase + C::OFF_MISC;
   auto bar = [&](int off) { return mb + (uint32_t)off; };
@@ -197,85 +203,77 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
   const int bh = blockIdx.x % bh_count;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int g = h / (p.Hq / p.Hkv);
-  const int q0 = qb * kBM;
-  int j_lo, j_hi;
-  tile_range(p, q0, j_lo, j_hi);
-  const int nsteps = j_hi - j_lo;
+  const int q0 = qb * kBM * C::NT;  // first row of the CTA
+  // key-tile range of each query tile and of the CTA
+  int jlo[2], jhi[2];
+  tile_range(p, q0, jlo[0], jhi[0]);
+  jlo[1] = jhi[1] = 0;
+  if (C::NT == 2) tile_range(p, q0 + kBM, jlo[1], jhi[1]);
+  const int J0 = (C::NT == 2 && jhi[1] > jlo[1]) ? imin(jlo[0], jlo[1]) : jlo[0];
+  const int J1 = (C::NT == 2) ? imax(jhi[0], jhi[1]) : jhi[0];
 
   Ctx cx;
-  cx.misc = mb;
   cx.abort = (volatile uint32_t*)(misc + M_ABORT);
   cx.gabort = p.gabort;
   cx.timeout_ns = p.timeout_ns;
   cx.counters = p.counters;
 
   if (threadIdx.x == 0) {
+    for (int s = 0; s < 4; ++s) mbar_init(bar(M_S_FULL + 8 * s), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(M_KV_FULL + 8 * s), 1);
       mbar_init(bar(M_KV_EMPTY + 8 * s), 1);
-      mbar_init(bar(M_S_FULL + 8 * s), 1);
-      mbar_init(bar(M_S_EMPTY + 8 * s), kSoftmaxThreads);
-      mbar_init(bar(M_REC_REQ + 8 * s), 1);
+      mbar_init(bar(M_DEC + 8 * s), 1);
+      mbar_init(bar(M_S16_FULL + 8 * s), 1);
+      mbar_init(bar(M_P_FULL + 8 * s), C::SM_THREADS);
+      mbar_init(bar(M_PV_DONE + 8 * s), 1);
     }
     mbar_init(bar(M_Q_FULL), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(M_S16_FULL + 8 * s), 1);
-      mbar_init(bar(M_S16_EMPTY + 8 * s), kSoftmaxThreads);
-    }
-    mbar_init(bar(M_P_FULL), kSoftmaxThreads);
-    mbar_init(bar(M_PV_DONE), 1);
     mbar_init(bar(M_DRAIN), 1);
     *(volatile uint32_t*)(misc + M_ABORT) = 0u;
     fence_mbar_init();
   }
-  if (warp == 9) tmem_alloc(bar(M_TMEM), C::TMEM_COLS);
-  // the block of ones that turns column d.. of O into the running sum l
-  if (threadIdx.x < kSoftmaxThreads) {
-    const uint32_t one2 = 0x3C003C00u;  // two fp16 1.0
-    for (int s = 0; s < C::NS; ++s) {
-      uint32_t* ones = (uint32_t*)(smem + C::OFF_ST + s * C::STAGE_BYTES + C::K8_BYTES +
-                                   C::K16_BYTES + (C::V_REGIONS - 1) * kBN * 128);
-      for (int i = threadIdx.x; i < kBN * 128 / 4; i += kSoftmaxThreads) ones[i] = one2;
-    }
+  if (warp == C::MMA_WARP) tmem_alloc(bar(M_TMEM), C::TMEM_COLS);
+  // the exp8 table
+  if (threadIdx.x < kBM) {
     misc[M_EXP8 + threadIdx.x] = p.exp8[threadIdx.x];
-    fence_proxy_async_smem();
+    misc[M_EXP8 + kBM + threadIdx.x] = p.exp8[kBM + threadIdx.x];
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *(volatile uint32_t*)(misc + M_TMEM);
 
-  if (warp == 8) {
+  if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && nsteps > 0) {
+    if (lane == 0 && J1 > J0) {
       prefetch_tmap(&p.tmQ8);
       prefetch_tmap(&p.tmQ16);
       prefetch_tmap(&p.tmK8);
       prefetch_tmap(&p.tmK16);
       prefetch_tmap(&p.tmV);
-      mbar_expect_tx(bar(M_Q_FULL), C::Q8_BYTES + C::Q16_BYTES);
-      for (int c = 0; c < D / (C::F8_SWZ_ROW); ++c)
-        tma_load_4d(sbase + C::OFF_Q8 + c * kBM * 128, &p.tmQ8, bar(M_Q_FULL),
-                    c * C::F8_SWZ_ROW, q0, h, b);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_4d(sbase + C::OFF_Q16 + c * kBM * 128, &p.tmQ16, bar(M_Q_FULL), c * 64, q0, h,
-                    b);
+      mbar_expect_tx(bar(M_Q_FULL), C::NT * C::QT_BYTES);
+      for (int t = 0; t < C::NT; ++t) {
+        const uint32_t qd = sbase + C::OFF_Q + t * C::QT_BYTES;
+        for (int c = 0; c < D / C::F8_SWZ_ROW; ++c)
+          tma_load_4d(qd + c * kBM * 128, &p.tmQ8, bar(M_Q_FULL), c * C::F8_SWZ_ROW, q0 + t * kBM, h, b);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(qd + C::Q8_BYTES + c * kBM * 128, &p.tmQ16, bar(M_Q_FULL), c * 64, q0 + t * kBM, h, b);
+      }
       int uses0 = 0, uses1 = 0;
-      for (int jj = 0; jj < nsteps && !*cx.abort; ++jj) {
-        const int s = jj % C::NS, u = jj / C::NS;
+      for (int j = J0; j < J1 && !*cx.abort; ++j) {
+        const int s = (j - J0) % C::NS, u = (j - J0) / C::NS;
         if (u >= 1 && !wait_bar(cx, bar(M_KV_EMPTY + 8 * s), (u - 1) & 1)) break;
-        const int key0 = (j_lo + jj) * kBN;
+        const int key0 = j * kBN;
         const uint32_t st = sbase + C::OFF_ST + s * C::STAGE_BYTES;
-        mbar_expect_tx(bar(M_KV_FULL + 8 * s), C::K8_BYTES + C::K16_BYTES + (D / 64) * kBN * 128);
-        for (int c = 0; c < D / (C::F8_SWZ_ROW); ++c)
-          tma_load_4d(st + c * kBN * 128, &p.tmK8, bar(M_KV_FULL + 8 * s), c * C::F8_SWZ_ROW,
-                      key0, g, b);
+        const uint32_t fb = bar(M_KV_FULL + 8 * s);
+        mbar_expect_tx(fb, C::STAGE_BYTES);
+        for (int c = 0; c < D / C::F8_SWZ_ROW; ++c)
+          tma_load_4d(st + c * kBN * 128, &p.tmK8, fb, c * C::F8_SWZ_ROW, key0, g, b);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(st + C::K8_BYTES + c * kBN * 128, &p.tmK16, bar(M_KV_FULL + 8 * s), c * 64,
-                      key0, g, b);
+          tma_load_4d(st + C::K8_BYTES + c * kBN * 128, &p.tmK16, fb, c * 64, key0, g, b);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(st + C::K8_BYTES + C::K16_BYTES + c * kBN * 128, &p.tmV,
-                      bar(M_KV_FULL + 8 * s), c * 64, key0, g, b);
+          tma_load_4d(st + C::K8_BYTES + C::K16_BYTES + c * kBN * 128, &p.tmV, fb, c * 64, key0, g, b);
         if (s) uses1 = u + 1; else uses0 = u + 1;
       }
       if (*cx.abort) {  // let every load in flight land before the CTA exits
@@ -284,68 +282,87 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
         drain_wait(bar(M_Q_FULL), 0);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nsteps > 0) {
-      auto issue_qk8 = [&](int jj) {
-        const uint32_t st = sbase + C::OFF_ST + (jj % C::NS) * C::STAGE_BYTES;
-        Mma<D>::qk8(tmem + C::S_COL0 + (jj & 1) * kBN, sbase + C::OFF_Q8, st);
-        mma_commit(bar(M_S_FULL + 8 * (jj & 1)));
-      };
-      auto load_and_qk8 = [&](int jj) -> bool {
-        const int s = jj % C::NS, u = jj / C::NS;
-        if (!wait_bar(cx, bar(M_KV_FULL + 8 * s), u & 1)) return false;
-        if (jj >= 2 && !wait_bar(cx, bar(M_S_EMPTY + 8 * (jj & 1)), ((jj - 2) >> 1) & 1))
-          return false;
-        tc_fence_after();
-        issue_qk8(jj);
-        return true;
-      };
-      // 16-bit recompute bookkeeping per S16 slot (slot of step j = j % NSLOT16):
-      // a QK16 of step j is issued speculatively when step j-1 needed one
-      // (step 0: always), or on demand once step j's decision arrives.
-      // per slot: was its last QK16 read (wanted), reads (s16_empty arrivals) expected
-      bool wanted0 = false, wanted1 = false;
-      int reads0 = 0, reads1 = 0;
-      auto issue_qk16 = [&](int j) -> bool {
-        const int sl = j % C::NSLOT16;
-        const bool wl = sl ? wanted1 : wanted0;
-        const int rd = sl ? reads1 : reads0;
-        if (wl && !wait_bar(cx, bar(M_S16_EMPTY + 8 * sl), (rd - 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t stj = sbase + C::OFF_ST + (j % C::NS) * C::STAGE_BYTES;
-        Mma<D>::qk16(tmem + C::S16_COL + sl * kBN, sbase + C::OFF_Q16, stj + C::K8_BYTES);
-        mma_commit(bar(M_S16_FULL + 8 * sl));
-        if (sl) wanted1 = false; else wanted0 = false;
-        return true;
-      };
+    // Event driven: poll the tiles' barriers and issue whatever is ready --
+    // a tile's next QK8 once its previous P is in (the softmax is then done
+    // with the S buffer) and the K8 tile has landed, its QK16 when the
+    // softmax's decision asks for it, its P.V when P is in -- so the two
+    // tiles drift into alternation; tile 1 starts once tile 0 has published
+    // its first decision.  A stage is released once every tile that uses
+    // it has issued its P.V.
+    if (lane == 0 && J1 > J0) {
+      auto stage_of = [&](int j) { return (j - J0) % C::NS; };
+      int nst[2] = {0, 0}, qk8_i[2] = {0, 0}, dec_i[2] = {0, 0}, p_i[2] = {0, 0};
+      for (int t = 0; t < C::NT; ++t) nst[t] = jhi[t] - jlo[t];
+      int released = J0;
       bool ok = wait_bar(cx, bar(M_Q_FULL), 0);
-      bool spec = false;  // QK16 of the current step already issued
-      if (ok) ok = load_and_qk8(0);
-      if (ok && C::SPEC16) {
-        ok = issue_qk16(0);
-        spec = true;
-      }
-      for (int jj = 0; ok && jj < nsteps; ++jj) {
-        if (C::NS == 1 && jj > 0) ok = load_and_qk8(jj);
-        if (ok && C::NS >= 2 && jj + 1 < nsteps) ok = load_and_qk8(jj + 1);
-        if (!ok) break;
-        if (!wait_bar(cx, bar(M_REC_REQ + 8 * (jj & 1)), (jj >> 1) & 1)) break;
-        const bool want = *(volatile uint32_t*)(misc + M_REC + 4 * (jj & 1)) != 0u;
-        const int s = jj % C::NS;
-        const uint32_t st = sbase + C::OFF_ST + s * C::STAGE_BYTES;
-        if (want && !spec && !issue_qk16(jj)) break;
-        if (want) {
-          if (jj % C::NSLOT16) { wanted1 = true; ++reads1; } else { wanted0 = true; ++reads0; }
+      unsigned long long t_last = globaltimer_ns();
+      while (ok) {
+        bool done = true, progress = false;
+#pragma unroll
+        for (int t = 0; t < C::NT; ++t) {
+          if (p_i[t] >= nst[t]) continue;
+          done = false;
+          const uint32_t tm = tmem + t * C::TILE_COLS;
+          const uint32_t qbase = sbase + C::OFF_Q + t * C::QT_BYTES;
+          // S buffer (step % 2) is free once P of the step two back is in
+          if (qk8_i[t] < nst[t] && qk8_i[t] <= p_i[t] + 1 && (t == 0 || dec_i[0] > 0 || nst[0] == 0)) {
+            const int j = jlo[t] + qk8_i[t];
+            if (mbar_test_wait(bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1)) {
+              tc_fence_after();
+              Mma<D>::qk8(tm + C::S_OFF + (qk8_i[t] & 1) * kBN, qbase,
+                          sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES);
+              mma_commit(bar(M_S_FULL + 16 * t + 8 * (qk8_i[t] & 1)));
+              ++qk8_i[t];
+              progress = true;
+            }
+          }
+          if (dec_i[t] < qk8_i[t] && mbar_test_wait(bar(M_DEC + 8 * t), dec_i[t] & 1)) {
+            if (*(volatile uint32_t*)(misc + M_REC + 4 * t)) {
+              const int j = jlo[t] + dec_i[t];
+              tc_fence_after();
+              Mma<D>::qk16(tm + C::S_OFF + (dec_i[t] & 1) * kBN, qbase + C::Q8_BYTES,
+                           sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES + C::K8_BYTES);
+              mma_commit(bar(M_S16_FULL + 8 * t));
+            }
+            ++dec_i[t];
+            progress = true;
+          }
+          if (p_i[t] < dec_i[t] && mbar_test_wait(bar(M_P_FULL + 8 * t), p_i[t] & 1)) {
+            const int j = jlo[t] + p_i[t];
+            tc_fence_after();
+            Mma<D>::pv(tm, sbase + C::OFF_P + t * C::P_BYTES,
+                       sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES + C::K8_BYTES + C::K16_BYTES,
+                       p_i[t] > 0);
+            mma_commit(bar(M_PV_DONE + 8 * t));
+            ++p_i[t];
+            progress = true;
+            for (;;) {  // release the stages every tile is done with
+              bool used = false;
+              for (int u = 0; u < C::NT; ++u)
+                used |= released >= jlo[u] && released < jhi[u] && jlo[u] + p_i[u] <= released;
+              if (released >= J1 || used) break;
+              mma_commit(bar(M_KV_EMPTY + 8 * stage_of(released)));
+              ++released;
+            }
+          }
         }
-        spec = C::SPEC16 && want && jj + 1 < nsteps;
-        if (spec && !issue_qk16(jj + 1)) break;
-        // O += P V16 (and l += P 1)
-        if (!wait_bar(cx, bar(M_P_FULL), jj & 1)) break;
-        tc_fence_after();
-        Mma<D>::pv(tmem, sbase + C::OFF_P, st + C::K8_BYTES + C::K16_BYTES, jj > 0);
-        mma_commit(bar(M_PV_DONE));
-        mma_commit(bar(M_KV_EMPTY + 8 * s));
+        if (done) break;
+        if (progress) {
+          t_last = globaltimer_ns();
+        } else {
+          if (*cx.abort) break;
+          if (*cx.gabort) { *cx.abort = 1u; break; }
+          const unsigned long long now = globaltimer_ns();
+          if (now - t_last > cx.timeout_ns) {
+            *cx.abort = 1u;
+            atomicExch((unsigned int*)cx.gabort, 1u);
+            if (cx.counters) atomicExch(&cx.counters[9], 4ull);  // LAMP_ERR_TIMEOUT
+            break;
+          }
+          __nanosleep(32);
+        }
       }
       // make sure no MMA is still writing TMEM before it is released
       mma_commit(bar(M_DRAIN));
@@ -353,67 +370,73 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // Two threads per query row: warps w and w+4 own the same 32 rows
-    // (TMEM lanes 32*(w%4)..), w < 4 the key columns 0..31 of each step,
-    // w >= 4 the columns 32..63.  Every softmax thread runs every step up to
-    // the CTA-wide reduction of `fail`, so named barriers never miss a
-    // participant; waits are warp-uniform so the .sync.aligned TMEM accesses
-    // stay converged.
-    const int rw = warp & 3;              // row group
-    const int hf = warp >> 2;             // column half
-    const int t = rw * 32 + lane;         // query row within the CTA == TMEM lane
-    const int col0 = hf * kNC;
-    const int R = q0 + t;
-    const uint32_t lane_base = tmem + ((uint32_t)(rw * 32) << 16);
-    const uint32_t pair_bar = 2 + rw;     // named barrier of warps rw and rw + 4
-    float* xch = (float*)(misc + M_XCH);
-    uint32_t* xb = (uint32_t*)(misc + M_XB);
+    // Two threads per query row: warps 8tt+rw and 8tt+4+rw hold TMEM lanes
+    // 32rw.. of tile tt, the first for key columns 0..31 of each step, the
+    // second for 32..63.  Every softmax thread of a tile runs every step of
+    // the tile up to the tile-wide reduction of `fail`, so named barriers
+    // never miss a participant; waits are warp-uniform so the .sync.aligned
+    // TMEM accesses stay converged.
+    constexpr int NC = kNC;               // logits per thread per step
+    const int tt = warp >> 3;             // query tile
+    const int hf = (warp >> 2) & 1;       // column half
+    const int rw = warp & 3;              // 32-row group of the tile
+    const int t = rw * 32 + lane;         // row within the tile == TMEM lane
+    const int col0 = hf * NC;
+    const int R = q0 + tt * kBM + t;
+    const int jlo_t = jlo[tt], nsteps = jhi[tt] - jlo[tt];
+    const uint32_t tile_bar = 1 + tt;             // the tile's 256 softmax threads
+    const uint32_t pair_bar = 3 + 4 * tt + rw;    // the two warps of these 32 rows
+    const uint32_t lane_base = tmem + tt * C::TILE_COLS + ((uint32_t)(rw * 32) << 16);
+    const uint8_t* sQ8 = smem + C::OFF_Q + tt * C::QT_BYTES;
+    uint8_t* sP = smem + C::OFF_P + tt * C::P_BYTES;
     const uint8_t* tab = misc + M_EXP8;
+    float* xch = (float*)(misc + M_XCH) + tt * 2 * kBM;
+    uint32_t* xb = (uint32_t*)(misc + M_XB) + tt * 2 * kBM;
     int lo, hi;
     row_range(p, R, lo, hi);
     float m = -INFINITY;
+    float l = 0.0f;  // this half's running sum of the (rounded) P values fed to P.V
     float nq = 0.0f;
     if (R < p.N) nq = p.nq[((size_t)b * p.Hq + h) * p.N + R];
     unsigned long long c_tiles = 0, c_h0 = 0, c_h1 = 0, c_h2 = 0, c_strips = 0, c_st1 = 0,
                        c_fl = 0, c_sat = 0, c_fix = 0, c_rec = 0;
-    const int qtile = 2 * qb + (rw >> 1);  // 64-row query tile of this warp
-    int commits16_0 = 0, commits16_1 = 0;  // QK16 results committed per S16 slot (mirrors the MMA warp)
-    bool spec16 = C::SPEC16;    // QK16 of the current step issued speculatively
-    unsigned long long c_waste = 0;
+    const int qtile = (q0 + tt * kBM) / kBN + (rw >> 1);  // 64-row query tile of this warp
+    int nrec = 0;
     const float sig = p.sigma_f;
     const float2 sig2 = make_float2(sig, sig);
     const float T = p.tau_abs;
     const uint32_t dcode = p.delta_code;
     bool fail = !(nsteps > 0 && wait_bar_warp(cx, bar(M_Q_FULL), 0));
     bool done_ok = false;
+    const float* nkrow = p.nkmax + ((size_t)b * p.Hkv + g) * p.T;
+    float nk_next = nsteps > 0 ? nkrow[jlo_t] : 0.0f;
 
     for (int jj = 0; jj < nsteps; ++jj) {
-      const int jt = j_lo + jj;
+      const int jt = jlo_t + jj;
+      const float nk = nk_next;  // loaded one step ahead
+      if (jj + 1 < nsteps) nk_next = nkrow[jt + 1];
       const int k0 = jt * kBN;
       const int clo = imax(k0, lo), chi = imin(k0 + kBN - 1, hi);
       const bool rowvis = clo <= chi;
-      // visible columns of this thread's half (bit c = key k0 + col0 + c)
-      uint32_t vm = 0u;
+      uint32_t vm = 0u;  // visible columns of this half (bit c = key k0 + col0 + c)
       {
-        const int a = imax(clo - (k0 + col0), 0), z = imin(chi - (k0 + col0), kNC - 1);
+        const int a = imax(clo - (k0 + col0), 0), z = imin(chi - (k0 + col0), NC - 1);
         if (rowvis && a <= z) vm = (z == 31 ? 0xFFFFFFFFu : ((1u << (z + 1)) - 1u)) & ~((1u << a) - 1u);
       }
       const bool all_full = __all_sync(0xffffffffu, vm == 0xFFFFFFFFu);
-      const float nk = p.nkmax[((size_t)b * p.Hkv + g) * p.T + jt];
       const float G = p.guard * sig * nq * nk;
 
       // ---- S = Q8 K8^T (fp32, TMEM) -> 8-bit logits
-      uint32_t a32[kNC];
-      if (!fail) fail = !wait_bar_warp(cx, bar(M_S_FULL + 8 * (jj & 1)), (jj >> 1) & 1);
+      const uint32_t sbuf = lane_base + C::S_OFF + (jj & 1) * kBN + col0;  // this step's S buffer
+      uint32_t a32[NC];
+      if (!fail) fail = !wait_bar_warp(cx, bar(M_S_FULL + 16 * tt + 8 * (jj & 1)), (jj >> 1) & 1);
       if (!fail) {
         tc_fence_after();
-        tmem_ld32(lane_base + C::S_COL0 + (jj & 1) * kBN + col0, a32);
+        tmem_ld32(sbuf, a32);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(M_S_EMPTY + 8 * (jj & 1)));
       } else {
 #pragma unroll
-        for (int c = 0; c < kNC; ++c) a32[c] = 0u;
+        for (int c = 0; c < NC; ++c) a32[c] = 0u;
       }
       // S8 = fl8(A sigma) is certain unless y = A_tc sigma lies within G of an
       // E4M3 rounding boundary (the two roundings of y -+ G then differ).  Of
@@ -422,13 +445,13 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
       // this tile) is exact and <= the new max, and a logit whose largest
       // rounding is <= m - 6.75 rounds x8 to <= -7 (P8 = 0, below any
       // delta > 0) and is not the maximum.  With delta = 0 all count.
-      uint32_t s8h[kNC / 2];  // S8 pairs as f16x2 (exact)
-      uint32_t unc = 0u;      // logits to re-derive exactly
+      uint32_t s8h[NC / 2];  // S8 pairs as f16x2 (exact)
+      uint32_t unc = 0u;     // logits to re-derive exactly
       {
         const float2 gm = make_float2(-G, -G), gp = make_float2(G, G);
         const float thr = m - 6.75f;
 #pragma unroll
-        for (int g4 = 0; g4 < kNC / 8; ++g4) {  // 4 pairs at a time, one branch
+        for (int g4 = 0; g4 < NC / 8; ++g4) {  // 4 pairs at a time, one branch
           float2 yh[4];
           uint32_t d4 = 0u, d16[4];
 #pragma unroll
@@ -458,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
       unc &= vm;
       if (fail) unc = 0u;
       if (__any_sync(0xffffffffu, unc != 0u)) {
-        const uint8_t* sK8 = smem + C::OFF_ST + (jj % C::NS) * C::STAGE_BYTES;
+        const uint8_t* sK8 = smem + C::OFF_ST + ((jt - J0) % C::NS) * C::STAGE_BYTES;
         for (;;) {
           const unsigned who = __ballot_sync(0xffffffffu, unc != 0u);
           if (!who) break;
@@ -469,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
             const float v = e4m3_rne_from_double((double)acc * 0x1p-18 * p.sigma_d);
             const uint32_t hv = (uint32_t)__half_as_ushort(__float2half_rn(v));  // exact
 #pragma unroll
-            for (int i = 0; i < kNC / 2; ++i)
+            for (int i = 0; i < NC / 2; ++i)
               if (i == (cb >> 1))
                 s8h[i] = (cb & 1) ? ((s8h[i] & 0x0000FFFFu) | (hv << 16)) : ((s8h[i] & 0xFFFF0000u) | hv);
             unc &= unc - 1u;
@@ -480,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
       // hidden keys take -inf: they are never the max and x8 saturates to -448 (P8 = 0)
       if (!all_full) {
 #pragma unroll
-        for (int i = 0; i < kNC / 2; ++i) {
+        for (int i = 0; i < NC / 2; ++i) {
           const uint32_t keep = (((vm >> (2 * i)) & 1u) ? 0x0000FFFFu : 0u) | (((vm >> (2 * i + 1)) & 1u) ? 0xFFFF0000u : 0u);
           s8h[i] = (s8h[i] & keep) | (0xFC00FC00u & ~keep);
         }
@@ -491,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
       {
         __half2 mx = as_half2(s8h[0]);
 #pragma unroll
-        for (int i = 1; i < kNC / 2; ++i) mx = __hmax2(mx, as_half2(s8h[i]));
+        for (int i = 1; i < NC / 2; ++i) mx = __hmax2(mx, as_half2(s8h[i]));
         const float mine = fmaxf(__low2float(mx), __high2float(mx));
         xch[hf * kBM + t] = mine;
         bar_sync(pair_bar, 64);
@@ -515,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
         if (maybe_neg) {
           const __half2 mh = __float2half2_rn(m_new);
 #pragma unroll
-          for (int i = 0; i < kNC / 2; ++i) {
+          for (int i = 0; i < NC / 2; ++i) {
             const __half2 sv = as_half2(s8h[i]);
             const uint32_t x8 = cvt_e4m3x2_f16x2(__hsub2(sv, mh));
             if (((vm >> (2 * i)) & 1u) && __low2float(sv) <= -T && tab[x8 & 0xFFu] >= dcode) mine = 1u;
@@ -528,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
       }
       if (rowvis && sig * nq * nk * (1.0f + p.guard) >= 432.0f) {
 #pragma unroll
-        for (int i = 0; i < kNC / 2; ++i) {
+        for (int i = 0; i < NC / 2; ++i) {
           const __half2 sv = as_half2(s8h[i]);
           c_sat += (fabsf(__low2float(sv)) == 448.0f) + (fabsf(__high2float(sv)) == 448.0f);
         }
@@ -548,16 +571,23 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
         if (p.force == 2) sf[hh] = 0u;
       }
       const bool my_flag = sf[lane >> 4] != 0u;
+      uint8_t* sflag = misc + M_SFLAG + 32 * tt + 16 * (jj & 1);
       if (lane == 0 && hf == 0)
-        *(volatile uint32_t*)(misc + M_SFLAG + 16 * (jj & 1) + 4 * rw) =
+        *(volatile uint32_t*)(sflag + 4 * rw) =
             sf[0] | (sf[1] << 1) | (s1[0] << 2) | (s1[1] << 3) | (sv[0] << 4) | (sv[1] << 5);
-      const bool any = bar_red_or(1, kSoftmaxThreads, my_flag);
-      if (bar_red_or(1, kSoftmaxThreads, fail)) break;  // uniform exit
+      const bool any = bar_red_or(tile_bar, C::SM_THREADS, my_flag);
+      if (bar_red_or(tile_bar, C::SM_THREADS, fail)) break;  // uniform exit of the tile
 
+      if (t == 0 && hf == 0) {  // publish the decision; S8 has been read, the buffer may take S16
+        *(volatile uint32_t*)(misc + M_REC + 4 * tt) = any ? 1u : 0u;
+        tc_fence_before();
+        mbar_arrive(bar(M_DEC + 8 * tt));
+        if (any) ++c_rec;
+      }
       if (lane == 0 && hf == 0 && (rw & 1) == 0) {
-        // lane 0 of warps 0 and 2 owns the 64-row query tile of row groups (rw, rw+1)
-        const uint32_t w0 = *(volatile uint32_t*)(misc + M_SFLAG + 16 * (jj & 1) + 4 * rw);
-        const uint32_t w1 = *(volatile uint32_t*)(misc + M_SFLAG + 16 * (jj & 1) + 4 * (rw + 1));
+        // lane 0 of row groups 0 and 2 owns the 64-row query tile of groups (rw, rw+1)
+        const uint32_t w0 = *(volatile uint32_t*)(sflag + 4 * rw);
+        const uint32_t w1 = *(volatile uint32_t*)(sflag + 4 * (rw + 1));
         const uint32_t fl4 = (w0 & 3u) | ((w1 & 3u) << 2);
         const uint32_t st4 = ((w0 >> 2) & 3u) | (((w1 >> 2) & 3u) << 2);
         const uint32_t vs4 = ((w0 >> 4) & 3u) | (((w1 >> 4) & 3u) << 2);
@@ -572,20 +602,15 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
             p.mask[(((size_t)b * p.Hq + h) * p.T + qtile) * p.T + jt] = (uint8_t)(fl4 | (st4 << 4));
         }
       }
-      if (threadIdx.x == 0) {
-        *(volatile uint32_t*)(misc + M_REC + 4 * (jj & 1)) = any ? 1u : 0u;
-        mbar_arrive(bar(M_REC_REQ + 8 * (jj & 1)));
-        if (any) ++c_rec;
-      }
 
       // ---- x8 = fl8(S8 - m) (fp16 difference, then one E4M3 rounding: equal
       // to the single rounding for E4M3 operands), P8 from the exp8 table;
       // rows of flagged sub-blocks take P16 below instead
-      uint32_t pw[kNC / 2];
+      uint32_t pw[NC / 2];
       if (rowvis && !my_flag) {
         const __half2 mh = __float2half2_rn(m_new);
 #pragma unroll
-        for (int i = 0; i < kNC / 2; ++i) {
+        for (int i = 0; i < NC / 2; ++i) {
           const __half2 xh = __hsub2(as_half2(s8h[i]), mh);
           const uint32_t x8 = cvt_e4m3x2_f16x2(xh);
           const uint32_t pc = (uint32_t)tab[x8 & 0xFFu] | ((uint32_t)tab[x8 >> 8] << 8);
@@ -593,67 +618,67 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < kNC / 2; ++i) pw[i] = 0u;
+        for (int i = 0; i < NC / 2; ++i) pw[i] = 0u;
       }
 
       // ---- 16-bit recompute for the rows of flagged sub-blocks
-      {
-        const int sl = jj % C::NSLOT16;
-        if (spec16 || any) { if (sl) ++commits16_1; else ++commits16_0; }
-        const int ncommit = sl ? commits16_1 : commits16_0;
-        if (spec16 && !any) ++c_waste;
-        spec16 = C::SPEC16 && any && jj + 1 < nsteps;
-        if (any && !fail) fail = !wait_bar_warp(cx, bar(M_S16_FULL + 8 * sl), (ncommit - 1) & 1);
-        if (any && !fail) {
-          tc_fence_after();
-          uint32_t r16[kNC];
-          tmem_ld32(lane_base + C::S16_COL + sl * kBN + col0, r16);
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(bar(M_S16_EMPTY + 8 * sl));
-          if (my_flag && rowvis) {
-            const float sl2 = sig * kLog2e, ml = m_new * kLog2e;
+      if (any && !fail) fail = !wait_bar_warp(cx, bar(M_S16_FULL + 8 * tt), nrec & 1);
+      if (any && !fail) {
+        ++nrec;
+        tc_fence_after();
+        uint32_t r16[NC];
+        tmem_ld32(sbuf, r16);
+        tmem_wait_ld();
+        if (my_flag && rowvis) {
+          const float sl2 = sig * kLog2e, ml = m_new * kLog2e;
 #pragma unroll
-            for (int i = 0; i < kNC / 2; ++i) {
-              const float e0 = ex2_approx(fmaf(__uint_as_float(r16[2 * i]), sl2, -ml));
-              const float e1 = ex2_approx(fmaf(__uint_as_float(r16[2 * i + 1]), sl2, -ml));
-              pw[i] = cvt_f16x2_sat(e1, e0);
-            }
-            if (!all_full) {
+          for (int i = 0; i < NC / 2; ++i) {
+            const float e0 = ex2_approx(fmaf(__uint_as_float(r16[2 * i]), sl2, -ml));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(r16[2 * i + 1]), sl2, -ml));
+            pw[i] = cvt_f16x2_sat(e1, e0);
+          }
+          if (!all_full) {
 #pragma unroll
-              for (int i = 0; i < kNC / 2; ++i) {
-                if (!((vm >> (2 * i)) & 1u)) pw[i] &= 0xFFFF0000u;
-                if (!((vm >> (2 * i + 1)) & 1u)) pw[i] &= 0x0000FFFFu;
-              }
+            for (int i = 0; i < NC / 2; ++i) {
+              if (!((vm >> (2 * i)) & 1u)) pw[i] &= 0xFFFF0000u;
+              if (!((vm >> (2 * i + 1)) & 1u)) pw[i] &= 0x0000FFFFu;
             }
           }
         }
       }
 
       // ---- the previous P.V must be done before P and O are touched
-      if (jj > 0 && !fail) fail = !wait_bar_warp(cx, bar(M_PV_DONE), (jj - 1) & 1);
+      if (jj > 0 && !fail) fail = !wait_bar_warp(cx, bar(M_PV_DONE + 8 * tt), (jj - 1) & 1);
       if (!fail) {
         tc_fence_after();
         const float alpha =
             (m_new == m) ? 1.0f : (m == -INFINITY ? 0.0f : ex2_approx((m - m_new) * kLog2e));
         if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-          constexpr int NCH = C::O_COLS / 16, NCH0 = (NCH + 1) / 2;
-          const int cb = hf ? NCH0 : 0, ce = hf ? NCH : NCH0;
+          // this half rescales O columns [hf D/2, (hf+1) D/2)
 #pragma unroll 1
-          for (int ch = cb; ch < ce; ++ch) {
-            uint32_t o[16];
-            tmem_ld16(lane_base + ch * 16, o);
+          for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + c0, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; i += 2) {
+            for (int i = 0; i < 32; i += 2) {
               const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
                                           make_float2(alpha, alpha));
               o[i] = __float_as_uint(v.x);
               o[i + 1] = __float_as_uint(v.y);
             }
-            tmem_st16(lane_base + ch * 16, o);
+            tmem_st32(lane_base + c0, o);
           }
           tmem_wait_st();
+        }
+        {  // l = alpha l + sum of this half's P (exact fp16 values, fp32 sums)
+          float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+          for (int i = 0; i < NC / 2; ++i) {
+            ls[i & 1] = add_f32_f16lo(ls[i & 1], pw[i]);
+            ls[2 + (i & 1)] = add_f32_f16hi(ls[2 + (i & 1)], pw[i]);
+          }
+          l = fmaf(alpha, l, (ls[0] + ls[1]) + (ls[2] + ls[3]));
         }
         // P row half -> shared memory (K-major, 128-byte swizzle)
 #pragma unroll
@@ -663,24 +688,23 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(M_P_FULL));
+        mbar_arrive(bar(M_P_FULL + 8 * tt));
       }
       m = m_new;
       if (jj == nsteps - 1) done_ok = !fail;
     }
 
-    // ---- epilogue: out = O / l, LSE = m + ln l (each half writes d/2 columns)
-    if (done_ok) done_ok = wait_bar_warp(cx, bar(M_PV_DONE), (nsteps - 1) & 1);
+    // ---- epilogue: l of the row = sum of both halves; out = O / l, LSE = m + ln l
+    xch[hf * kBM + t] = l;
+    bar_sync(pair_bar, 64);
+    const float lrow = l + xch[(1 - hf) * kBM + t];
+    if (done_ok) done_ok = wait_bar_warp(cx, bar(M_PV_DONE + 8 * tt), (nsteps - 1) & 1);
     if (done_ok) {
       tc_fence_after();
-      uint32_t lw[16];
-      tmem_ld16(lane_base + D, lw);
-      tmem_wait_ld();
-      const float l = __uint_as_float(lw[0]);
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      const float inv = lrow > 0.0f ? 1.0f / lrow : 0.0f;
       const bool live = R < p.N;
       if (live && hf == 0 && p.lse)
-        p.lse[((size_t)b * p.Hq + h) * p.N + R] = l > 0.0f ? m + logf(l) : -INFINITY;
+        p.lse[((size_t)b * p.Hq + h) * p.N + R] = lrow > 0.0f ? m + logf(lrow) : -INFINITY;
       char* orow = (char*)p.out + ((size_t)b * p.o_stride[0] + (size_t)R * p.o_stride[1] +
                                    (size_t)h * p.o_stride[2]) * (p.out_f32 ? 4 : 2);
 #pragma unroll 1
@@ -722,30 +746,26 @@ __global__ void __launch_bounds__(kThreads, 1) lamp_fwd_kernel(const __grid_cons
       for (int o = 16; o > 0; o >>= 1) c_sat += __shfl_xor_sync(0xffffffffu, c_sat, o);
       if (lane == 0 && c_sat) atomicAdd(&p.counters[7], c_sat);
       if (lane == 0 && c_fix) atomicAdd(&p.counters[8], c_fix);
-      if (threadIdx.x == 0 && c_rec) atomicAdd(&p.counters[10], c_rec);
-      if (threadIdx.x == 0 && c_waste) atomicAdd(&p.counters[11], c_waste);
+      if (t == 0 && hf == 0 && c_rec) atomicAdd(&p.counters[10], c_rec);
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == C::MMA_WARP) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-}  // namespace lamp
-
 // ---------------------------------------------------------------- launcher
-namespace lamp {
-
 template <int D>
-static cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t st) {
-  const int smem = Cfg<D>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(lamp_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+static cudaError_t launch_fwd_d(FwdParams p, cudaStream_t st) {
+  using C = Cfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(lamp_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
+  p.nqb = (p.N + kBM * C::NT - 1) / (kBM * C::NT);
   const unsigned grid = (unsigned)p.nqb * (unsigned)p.B * (unsigned)p.Hq;
   if (grid == 0) return cudaSuccess;
-  lamp_fwd_kernel<D><<<grid, kThreads, smem, st>>>(p);
+  lamp_fwd_kernel<D><<<grid, C::THREADS, C::SMEM, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -3,7 +3,7 @@
 // layouts and TMEM read-back, run on caller-given data.
 //   which 0: S = A8 . B8^T, A8 [128 x D], B8 [64 x D] E4M3 codes, out [128 x 64]
 //   which 1: S = A . B^T,  A [128 x D], B [64 x D] BF16,          out [128 x 64]
-//   which 2: O = P . [V|1], P [128 x 64], V [64 x D] FP16,         out [128 x (D+16)]
+//   which 2: O = P . V,    P [128 x 64], V [64 x D] FP16,         out [128 x D]
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -20,7 +20,7 @@ __global__ void __launch_bounds__(128, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;                 // up to 128 x 512 B
-  uint8_t* sB = smem + 128 * 512;     // up to 64 x 512 B + ones
+  uint8_t* sB = smem + 128 * 512;     // up to 64 x 512 B
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t taddr;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -50,7 +50,6 @@ __global__ void __launch_bounds__(128, 1)
       const int key = i / D, d = i % D;
       *(uint16_t*)(sB + (d / 64) * 64 * 128 + swz_offset(key, 2 * (d % 64), 64, 128)) = v16[i];
     }
-    for (int i = tid; i < 64 * 64; i += 128) *(uint16_t*)(sB + (D / 64) * 64 * 128 + 2 * i) = 0x3C00;
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -68,7 +67,7 @@ __global__ void __launch_bounds__(128, 1)
   ok = __all_sync(0xffffffffu, ok);
   if (!ok && (tid & 31) == 0) atomicExch(status, 4u);
   tc_fence_after();
-  const int ncols = which == 2 ? D + 16 : 64;
+  const int ncols = which == 2 ? D : 64;
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
   for (int c0 = 0; c0 < ncols; c0 += 16) {
     uint32_t r[16];

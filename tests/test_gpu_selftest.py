@@ -67,6 +67,4 @@ def test_fp16_pv_mma_mn_major(lamp, d):
     v = torch.from_numpy(rng.standard_normal((64, d))).to(torch.float16)
     out = lamp.selftest(2, p.cuda(), v.cuda(), d).cpu().double()
     exact = p.double() @ v.double()
-    assert (out[:, :d] - exact).abs().max().item() <= 1e-3
-    lsum = p.double().sum(dim=1, keepdim=True).expand(128, 16)
-    assert (out[:, d:] - lsum).abs().max().item() <= 1e-3
+    assert (out - exact).abs().max().item() <= 1e-3
