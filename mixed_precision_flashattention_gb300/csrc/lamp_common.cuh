@@ -11,10 +11,6 @@ namespace lamp {
 
 constexpr int kBM = 128;        // query rows per CTA (one TMEM lane per row)
 constexpr int kBN = 64;         // keys per step = one 64-key tile of the method
-constexpr int kStrip = 16;      // query rows per sub-block
-constexpr int kSoftmaxWarps = 8;    // two warps (column halves) per 32 query rows
-constexpr int kSoftmaxThreads = 256;
-constexpr int kThreads = 320;       // 8 softmax warps + TMA warp + MMA warp
 constexpr int kNC = 32;             // logits per softmax thread per step
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -70,26 +66,28 @@ __device__ __forceinline__ uint32_t swz_offset(int r, int x, int rows, int row_b
   return (uint32_t)(col * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + chunk * 16 + (w & 15));
 }
 
-// E4M3 code -> exact integer value * 2^9 (so every finite code is an integer).
-__device__ __forceinline__ int e4m3_to_int512(uint32_t b) {
-  int e = (b >> 3) & 15, m = b & 7;
-  int v = e ? ((8 + m) << (e - 1)) : m;
-  return (b & 0x80) ? -v : v;
+// Exact product of two E4M3 codes, times 2^18 (an integer below 2^36): every
+// finite code is (significand <= 15) * 2^(shift - 9) with shift in 0..14.
+__device__ __forceinline__ long long e4m3_prod_2p18(uint32_t a, uint32_t b) {
+  const uint32_t ea = (a >> 3) & 15u, eb = (b >> 3) & 15u;
+  const uint32_t ma = ea ? ((a & 7u) | 8u) : (a & 7u);
+  const uint32_t mb = eb ? ((b & 7u) | 8u) : (b & 7u);
+  const uint32_t sh = (ea ? ea - 1u : 0u) + (eb ? eb - 1u : 0u);
+  const long long v = (long long)(ma * mb) << sh;
+  return ((a ^ b) & 0x80u) ? -v : v;
 }
 
-// Round a double to E4M3 (round to nearest even, saturating to +-448).
-// Used only on the rare exact path, so it is written for clarity.
-__device__ __forceinline__ float e4m3_rne_from_double(double y) {
-  double a = fabs(y);
-  float r = 0.0f;
-  if (a > 0.0) {
-    int e = ilogb(a);
-    int E = e < -6 ? -6 : e;
-    double n = rint(ldexp(a, 3 - E));  // multiples of the E4M3 spacing at a
-    double v = ldexp(n, E - 3);
-    r = (float)(v > 448.0 ? 448.0 : v);
-  }
-  return y < 0.0 ? -r : r;
+// E4M3 rounding (to nearest even, saturating to +-448) of a double, as the
+// f16 bit pattern of the result (exact: E4M3 values are f16 values).  The
+// double is first narrowed to float by rounding to odd (truncate, then set
+// the last bit if anything was dropped); with 24 >= 4 + 2 significand bits
+// the following single E4M3 rounding then equals the direct one (Boldo and
+// Melquiond, "Emulation of FMA and correctly rounded sums: proved algorithms
+// using rounding to odd", IEEE TC 2008).
+__device__ __forceinline__ uint32_t e4m3_f16_from_double(double y) {
+  float f = __double2float_rz(y);
+  if ((double)f != y) f = __uint_as_float(__float_as_uint(f) | 1u);
+  return e4m3x2_to_f16x2((uint16_t)(cvt_e4m3x2(0.0f, f) & 0xFFu)) & 0xFFFFu;
 }
 
 // Host: E4M3 code of the round-to-nearest-even, saturating conversion of a

@@ -100,10 +100,10 @@ constexpr unsigned long long kDrainNs = 200000000ull;  // 0.2 s for in-flight co
 
 // Bounded wait: gives up after cx.timeout_ns, or as soon as this CTA or any
 // other CTA has given up; on expiry it raises both abort flags and writes
-// LAMP_ERR_TIMEOUT into the status counter.  The first probe is inline; the
-// waiting part is out of line, suspends in hardware and takes its state by
-// value.
-__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+// LAMP_ERR_TIMEOUT into the status counter.  The waiting part suspends in
+// hardware; it is inlined (a real call would save live registers to local
+// memory around every wait).
+__device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
                                            volatile unsigned int* gabort, unsigned long long timeout_ns,
                                            unsigned long long* counters) {
   const unsigned long long t0 = globaltimer_ns();
@@ -164,21 +164,36 @@ __device__ __forceinline__ void tile_range(const FwdParams& p, int q0, int& j_lo
   j_lo = (p.mask_kind == 2) ? imax(0, q0 - p.window + 1) / kBN : 0;
 }
 
-// Exact A * 2^18 of (row r of the tile's Q8, key c of the stage's K8):
-// integer dot product of the E4M3 operands in shared memory, split across
-// the warp (every lane gets the sum).
+// Exact A * 2^18 of (row r of the tile's Q8, key c of the stage's K8): an
+// integer dot product of the E4M3 operands in shared memory, D/32 bytes per
+// lane (contiguous inside one 16-byte swizzle chunk).  The per-lane sums
+// (< 2^39) are split at bit 24 and both parts summed with one warp
+// reduction each, so every lane gets the exact total.
 template <int D>
-__device__ long long exact_dot(const uint8_t* sQ8, const uint8_t* sK8, int r, int c, int lane) {
+__device__ __forceinline__ long long exact_dot(const uint8_t* sQ8, const uint8_t* sK8, int r, int c,
+                                               int lane) {
   constexpr int RB = (Cfg<D>::F8_SWZ_ROW == 64) ? 64 : D;
-  long long acc = 0;
-  for (int t = lane; t < D; t += 32) {
-    const uint32_t qa = sQ8[swz_offset(r, t, kBM, RB)];
-    const uint32_t kb = sK8[swz_offset(c, t, kBN, RB)];
-    acc += (long long)e4m3_to_int512(qa) * (long long)e4m3_to_int512(kb);
+  constexpr int BPL = D / 32;
+  const int x = lane * BPL;
+  uint32_t q[2] = {0u, 0u}, k[2] = {0u, 0u};
+  if (BPL == 8) {
+    const uint2 a = *reinterpret_cast<const uint2*>(sQ8 + swz_offset(r, x, kBM, RB));
+    const uint2 bb = *reinterpret_cast<const uint2*>(sK8 + swz_offset(c, x, kBN, RB));
+    q[0] = a.x; q[1] = a.y; k[0] = bb.x; k[1] = bb.y;
+  } else if (BPL == 4) {
+    q[0] = *reinterpret_cast<const uint32_t*>(sQ8 + swz_offset(r, x, kBM, RB));
+    k[0] = *reinterpret_cast<const uint32_t*>(sK8 + swz_offset(c, x, kBN, RB));
+  } else {
+    q[0] = *reinterpret_cast<const uint16_t*>(sQ8 + swz_offset(r, x, kBM, RB));
+    k[0] = *reinterpret_cast<const uint16_t*>(sK8 + swz_offset(c, x, kBN, RB));
   }
+  long long acc = 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  return acc;
+  for (int i = 0; i < BPL; ++i)
+    acc += e4m3_prod_2p18((q[i >> 2] >> (8 * (i & 3))) & 0xFFu, (k[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+  const int hi = __reduce_add_sync(0xffffffffu, (int)(acc >> 24));
+  const unsigned lo = __reduce_add_sync(0xffffffffu, (unsigned)(acc & 0xFFFFFF));
+  return (long long)hi * 16777216ll + (long long)lo;
 }
 
 }  // namespace lamp
@@ -205,12 +220,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
   const int g = h / (p.Hq / p.Hkv);
   const int q0 = qb * kBM * C::NT;  // first row of the CTA
   // key-tile range of each query tile and of the CTA
-  int jlo[2], jhi[2];
-  tile_range(p, q0, jlo[0], jhi[0]);
-  jlo[1] = jhi[1] = 0;
-  if (C::NT == 2) tile_range(p, q0 + kBM, jlo[1], jhi[1]);
-  const int J0 = (C::NT == 2 && jhi[1] > jlo[1]) ? imin(jlo[0], jlo[1]) : jlo[0];
-  const int J1 = (C::NT == 2) ? imax(jhi[0], jhi[1]) : jhi[0];
+  int jlo0, jhi0, jlo1 = 0, jhi1 = 0;
+  tile_range(p, q0, jlo0, jhi0);
+  if (C::NT == 2) tile_range(p, q0 + kBM, jlo1, jhi1);
+  const int J0 = (C::NT == 2 && jhi1 > jlo1) ? imin(jlo0, jlo1) : jlo0;
+  const int J1 = (C::NT == 2) ? imax(jhi0, jhi1) : jhi0;
+  auto JLO = [&](int t) { return t ? jlo1 : jlo0; };
+  auto JHI = [&](int t) { return t ? jhi1 : jhi0; };
 
   Ctx cx;
   cx.abort = (volatile uint32_t*)(misc + M_ABORT);
@@ -294,7 +310,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     if (lane == 0 && J1 > J0) {
       auto stage_of = [&](int j) { return (j - J0) % C::NS; };
       int nst[2] = {0, 0}, qk8_i[2] = {0, 0}, dec_i[2] = {0, 0}, p_i[2] = {0, 0};
-      for (int t = 0; t < C::NT; ++t) nst[t] = jhi[t] - jlo[t];
+      for (int t = 0; t < C::NT; ++t) nst[t] = JHI(t) - JLO(t);
       int released = J0;
       bool ok = wait_bar(cx, bar(M_Q_FULL), 0);
       unsigned long long t_last = globaltimer_ns();
@@ -308,7 +324,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           const uint32_t qbase = sbase + C::OFF_Q + t * C::QT_BYTES;
           // S buffer (step % 2) is free once P of the step two back is in
           if (qk8_i[t] < nst[t] && qk8_i[t] <= p_i[t] + 1 && (t == 0 || dec_i[0] > 0 || nst[0] == 0)) {
-            const int j = jlo[t] + qk8_i[t];
+            const int j = JLO(t) + qk8_i[t];
             if (mbar_test_wait(bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1)) {
               tc_fence_after();
               Mma<D>::qk8(tm + C::S_OFF + (qk8_i[t] & 1) * kBN, qbase,
@@ -320,7 +336,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           }
           if (dec_i[t] < qk8_i[t] && mbar_test_wait(bar(M_DEC + 8 * t), dec_i[t] & 1)) {
             if (*(volatile uint32_t*)(misc + M_REC + 4 * t)) {
-              const int j = jlo[t] + dec_i[t];
+              const int j = JLO(t) + dec_i[t];
               tc_fence_after();
               Mma<D>::qk16(tm + C::S_OFF + (dec_i[t] & 1) * kBN, qbase + C::Q8_BYTES,
                            sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES + C::K8_BYTES);
@@ -330,7 +346,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
             progress = true;
           }
           if (p_i[t] < dec_i[t] && mbar_test_wait(bar(M_P_FULL + 8 * t), p_i[t] & 1)) {
-            const int j = jlo[t] + p_i[t];
+            const int j = JLO(t) + p_i[t];
             tc_fence_after();
             Mma<D>::pv(tm, sbase + C::OFF_P + t * C::P_BYTES,
                        sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES + C::K8_BYTES + C::K16_BYTES,
@@ -341,7 +357,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
             for (;;) {  // release the stages every tile is done with
               bool used = false;
               for (int u = 0; u < C::NT; ++u)
-                used |= released >= jlo[u] && released < jhi[u] && jlo[u] + p_i[u] <= released;
+                used |= released >= JLO(u) && released < JHI(u) && JLO(u) + p_i[u] <= released;
               if (released >= J1 || used) break;
               mma_commit(bar(M_KV_EMPTY + 8 * stage_of(released)));
               ++released;
@@ -373,9 +389,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     // Two threads per query row: warps 8tt+rw and 8tt+4+rw hold TMEM lanes
     // 32rw.. of tile tt, the first for key columns 0..31 of each step, the
     // second for 32..63.  Every softmax thread of a tile runs every step of
-    // the tile up to the tile-wide reduction of `fail`, so named barriers
-    // never miss a participant; waits are warp-uniform so the .sync.aligned
-    // TMEM accesses stay converged.
+    // the tile, also after a failed wait (its later waits and TMEM accesses
+    // are then skipped), so named barriers never miss a participant; waits
+    // are warp-uniform so the .sync.aligned TMEM accesses stay converged.
     constexpr int NC = kNC;               // logits per thread per step
     const int tt = warp >> 3;             // query tile
     const int hf = (warp >> 2) & 1;       // column half
@@ -383,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     const int t = rw * 32 + lane;         // row within the tile == TMEM lane
     const int col0 = hf * NC;
     const int R = q0 + tt * kBM + t;
-    const int jlo_t = jlo[tt], nsteps = jhi[tt] - jlo[tt];
+    const int jlo_t = JLO(tt), nsteps = JHI(tt) - JLO(tt);
     const uint32_t tile_bar = 1 + tt;             // the tile's 256 softmax threads
     const uint32_t pair_bar = 3 + 4 * tt + rw;    // the two warps of these 32 rows
     const uint32_t lane_base = tmem + tt * C::TILE_COLS + ((uint32_t)(rw * 32) << 16);
@@ -398,8 +414,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     float l = 0.0f;  // this half's running sum of the (rounded) P values fed to P.V
     float nq = 0.0f;
     if (R < p.N) nq = p.nq[((size_t)b * p.Hq + h) * p.N + R];
-    unsigned long long c_tiles = 0, c_h0 = 0, c_h1 = 0, c_h2 = 0, c_strips = 0, c_st1 = 0,
-                       c_fl = 0, c_sat = 0, c_fix = 0, c_rec = 0;
+    uint32_t c_h0 = 0, c_h1 = 0, c_h2 = 0, c_strips = 0, c_st1 = 0, c_fl = 0, c_sat = 0, c_fix = 0,
+             c_rec = 0;  // per-thread counts (a CTA sees at most 2^21 logits per thread slot)
     const int qtile = (q0 + tt * kBM) / kBN + (rw >> 1);  // 64-row query tile of this warp
     int nrec = 0;
     const float sig = p.sigma_f;
@@ -489,12 +505,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           const int cb = __shfl_sync(0xffffffffu, unc ? (__ffs(unc) - 1) : 0, src);
           const long long acc = exact_dot<D>(sQ8, sK8, rw * 32 + src, col0 + cb, lane);
           if (lane == src) {
-            const float v = e4m3_rne_from_double((double)acc * 0x1p-18 * p.sigma_d);
-            const uint32_t hv = (uint32_t)__half_as_ushort(__float2half_rn(v));  // exact
+            const uint32_t hv = e4m3_f16_from_double((double)acc * 0x1p-18 * p.sigma_d);
+            // replace half (cb & 1) of pair cb >> 1 (bit tests, no indexed access)
+            const uint32_t hit = 1u << cb;
 #pragma unroll
-            for (int i = 0; i < NC / 2; ++i)
-              if (i == (cb >> 1))
-                s8h[i] = (cb & 1) ? ((s8h[i] & 0x0000FFFFu) | (hv << 16)) : ((s8h[i] & 0xFFFF0000u) | hv);
+            for (int i = 0; i < NC / 2; ++i) {
+              const uint32_t keep = (((hit >> (2 * i)) & 1u) ? 0xFFFF0000u : 0xFFFFFFFFu) &
+                                    (((hit >> (2 * i + 1)) & 1u) ? 0x0000FFFFu : 0xFFFFFFFFu);
+              s8h[i] = (s8h[i] & keep) | ((hv * 0x00010001u) & ~keep);
+            }
             unc &= unc - 1u;
           }
           if (lane == 0) ++c_fix;
@@ -570,21 +589,22 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         if (p.force == 1) sf[hh] = sv[hh];
         if (p.force == 2) sf[hh] = 0u;
       }
-      const bool my_flag = sf[lane >> 4] != 0u;
+      const bool my_flag = ((lane >> 4) ? sf[1] : sf[0]) != 0u;
       uint8_t* sflag = misc + M_SFLAG + 32 * tt + 16 * (jj & 1);
       if (lane == 0 && hf == 0)
         *(volatile uint32_t*)(sflag + 4 * rw) =
             sf[0] | (sf[1] << 1) | (s1[0] << 2) | (s1[1] << 3) | (sv[0] << 4) | (sv[1] << 5);
+      // (after a failed wait a thread keeps stepping with its waits skipped,
+      // so every thread of the tile reaches every barrier)
       const bool any = bar_red_or(tile_bar, C::SM_THREADS, my_flag);
-      if (bar_red_or(tile_bar, C::SM_THREADS, fail)) break;  // uniform exit of the tile
 
-      if (t == 0 && hf == 0) {  // publish the decision; S8 has been read, the buffer may take S16
+      if (t == 0 && hf == 0 && !fail) {  // publish the decision; S8 has been read, the buffer may take S16
         *(volatile uint32_t*)(misc + M_REC + 4 * tt) = any ? 1u : 0u;
         tc_fence_before();
         mbar_arrive(bar(M_DEC + 8 * tt));
         if (any) ++c_rec;
       }
-      if (lane == 0 && hf == 0 && (rw & 1) == 0) {
+      if (lane == 0 && hf == 0 && (rw & 1) == 0 && !fail) {
         // lane 0 of row groups 0 and 2 owns the 64-row query tile of groups (rw, rw+1)
         const uint32_t w0 = *(volatile uint32_t*)(sflag + 4 * rw);
         const uint32_t w1 = *(volatile uint32_t*)(sflag + 4 * (rw + 1));
@@ -593,7 +613,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         const uint32_t vs4 = ((w0 >> 4) & 3u) | (((w1 >> 4) & 3u) << 2);
         if (vs4) {
           const int nf = __popc(fl4);
-          ++c_tiles;
           if (nf == 0) ++c_h0; else if (nf == 1) ++c_h1; else ++c_h2;
           c_strips += __popc(vs4);
           c_st1 += __popc(st4 & vs4);
@@ -619,6 +638,30 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       } else {
 #pragma unroll
         for (int i = 0; i < NC / 2; ++i) pw[i] = 0u;
+      }
+
+      // ---- the previous P.V must be done before O is rescaled and P is
+      // rewritten; the rescale overlaps this step's QK16 on the tensor core
+      if (jj > 0 && !fail) fail = !wait_bar_warp(cx, bar(M_PV_DONE + 8 * tt), (jj - 1) & 1);
+      const float alpha = (m_new == m) ? 1.0f : (m == -INFINITY ? 0.0f : ex2_approx((m - m_new) * kLog2e));
+      if (!fail && jj > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        tc_fence_after();
+        // this half rescales O columns [hf D/2, (hf+1) D/2)
+#pragma unroll 1
+        for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                        make_float2(alpha, alpha));
+            o[i] = __float_as_uint(v.x);
+            o[i + 1] = __float_as_uint(v.y);
+          }
+          tmem_st32(lane_base + c0, o);
+        }
+        tmem_wait_st();
       }
 
       // ---- 16-bit recompute for the rows of flagged sub-blocks
@@ -647,30 +690,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         }
       }
 
-      // ---- the previous P.V must be done before P and O are touched
-      if (jj > 0 && !fail) fail = !wait_bar_warp(cx, bar(M_PV_DONE + 8 * tt), (jj - 1) & 1);
       if (!fail) {
-        tc_fence_after();
-        const float alpha =
-            (m_new == m) ? 1.0f : (m == -INFINITY ? 0.0f : ex2_approx((m - m_new) * kLog2e));
-        if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-          // this half rescales O columns [hf D/2, (hf+1) D/2)
-#pragma unroll 1
-          for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + c0, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
-                                          make_float2(alpha, alpha));
-              o[i] = __float_as_uint(v.x);
-              o[i + 1] = __float_as_uint(v.y);
-            }
-            tmem_st32(lane_base + c0, o);
-          }
-          tmem_wait_st();
-        }
         {  // l = alpha l + sum of this half's P (exact fp16 values, fp32 sums)
           float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
@@ -734,19 +754,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       }
     }
     if (p.counters) {
+      typedef unsigned long long u64;
+      const uint32_t c_tiles = c_h0 + c_h1 + c_h2;
       if (lane == 0 && hf == 0 && (rw & 1) == 0 && c_tiles) {
-        atomicAdd(&p.counters[0], c_tiles);
-        atomicAdd(&p.counters[1], c_h0);
-        atomicAdd(&p.counters[2], c_h1);
-        atomicAdd(&p.counters[3], c_h2);
-        atomicAdd(&p.counters[4], c_strips);
-        atomicAdd(&p.counters[5], c_st1);
-        atomicAdd(&p.counters[6], c_fl);
+        atomicAdd(&p.counters[0], (u64)c_tiles);
+        atomicAdd(&p.counters[1], (u64)c_h0);
+        atomicAdd(&p.counters[2], (u64)c_h1);
+        atomicAdd(&p.counters[3], (u64)c_h2);
+        atomicAdd(&p.counters[4], (u64)c_strips);
+        atomicAdd(&p.counters[5], (u64)c_st1);
+        atomicAdd(&p.counters[6], (u64)c_fl);
       }
-      for (int o = 16; o > 0; o >>= 1) c_sat += __shfl_xor_sync(0xffffffffu, c_sat, o);
-      if (lane == 0 && c_sat) atomicAdd(&p.counters[7], c_sat);
-      if (lane == 0 && c_fix) atomicAdd(&p.counters[8], c_fix);
-      if (t == 0 && hf == 0 && c_rec) atomicAdd(&p.counters[10], c_rec);
+      c_sat = __reduce_add_sync(0xffffffffu, c_sat);
+      if (lane == 0 && c_sat) atomicAdd(&p.counters[7], (u64)c_sat);
+      if (lane == 0 && c_fix) atomicAdd(&p.counters[8], (u64)c_fix);
+      if (t == 0 && hf == 0 && c_rec) atomicAdd(&p.counters[10], (u64)c_rec);
     }
   }
 
