@@ -320,8 +320,9 @@ def main():
             kv_steps += last // 64 + 1 - max(0, qb * 128 - w.window + 1) // 64
     kv_steps *= B * Hq
     f_qk8 = kv_steps * 2.0 * 128 * 64 * d
-    f_pv = kv_steps * 2.0 * 128 * 64 * (d + 16)
-    f_rec = float(c[10]) * 2.0 * 128 * 64 * d
+    f_pv = kv_steps * 2.0 * 128 * 64 * d
+    f_rec = float(c[10] + c[11]) * 2.0 * 128 * 64 * d  # 16-bit products of every step, used or not
+    f_rec_used = float(c[10]) * 2.0 * 128 * 64 * d
     t_tc = (f_qk8 / (fp8_peak * 1e12) + (f_pv + f_rec) / (bf16_peak * 1e12))
     res = {
         "metric": METRIC, "value": flops / (ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "n_gpus": world,
@@ -337,7 +338,8 @@ def main():
         "stats": {n: int(c[i]) for i, n in enumerate(lamp.COUNTER_NAMES)},
         "subblock16_frac": float(c[6]) / max(1, c[4]),
         "tiles_0_1_2plus": [float(c[1]) / max(1, c[0]), float(c[2]) / max(1, c[0]), float(c[3]) / max(1, c[0])],
-        "tensor_flops_issued": {"qk_fp8": f_qk8, "pv_fp16": f_pv, "recompute_bf16": f_rec},
+        "tensor_flops_issued": {"qk_fp8": f_qk8, "pv_fp16": f_pv, "recompute_bf16": f_rec,
+                                "recompute_bf16_used": f_rec_used},
         "e2e": {"value": flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
         "gpu_launches": 2 * K,

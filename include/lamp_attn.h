@@ -82,8 +82,8 @@ enum {
   LAMP_CNT_FIXUPS = 8,      /* logits re-derived exactly (near an 8-bit rounding boundary) */
   LAMP_CNT_STATUS = 9,      /* device-side status (lamp_status), 0 = ok */
   LAMP_CNT_RECOMP_STEPS = 10, /* 128x64 kernel steps whose 16-bit recompute was used */
-  LAMP_CNT_SPEC_WASTE = 11, /* 16-bit recompute MMAs issued ahead (the previous step
-                               needed one) whose step then needed none */
+  LAMP_CNT_SPEC_WASTE = 11, /* 128x64 kernel steps whose 16-bit products, computed
+                               ahead of the decision, were not needed */
   LAMP_NUM_COUNTERS = 16
 };
 

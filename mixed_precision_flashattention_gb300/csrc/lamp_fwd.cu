@@ -58,12 +58,13 @@ struct Cfg {
   static constexpr int OFF_MISC = OFF_P + NT * P_BYTES;
   static constexpr int MISC_BYTES = 5120;
   static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
-  // TMEM columns per tile (fp32): O (d values) and two 64-column S buffers;
-  // step j uses buffer j % 2 for S8's accumulator, then for S16's, so the
-  // QK8 of step j+1 can run while the softmax works on step j.
+  // TMEM columns per tile (fp32): O (d values), the 64-column S8 buffer and
+  // the 64-column S16 buffer.  QK16 of a step is computed ahead, while the
+  // softmax still works on S8, so the recompute never waits for it.
   static constexpr int O_COLS = D;
-  static constexpr int S_OFF = D;
-  static constexpr int TILE_COLS = S_OFF + 2 * kBN;
+  static constexpr int S8_OFF = D;
+  static constexpr int S16_OFF = D + kBN;
+  static constexpr int TILE_COLS = D + 2 * kBN;
   static constexpr int TMEM_COLS = 512;
   static_assert(NT * TILE_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -74,15 +75,14 @@ enum : int {
   M_KV_FULL = 0,      // [2 stages]
   M_KV_EMPTY = 16,    // [2 stages]
   M_Q_FULL = 32,
-  M_S_FULL = 40,      // [2 tiles][2 buffers] QK8 result in TMEM (at + 16 t + 8 buf)
-  M_DEC = 72,         // [2 tiles] the softmax published its recompute decision
+  M_S_FULL = 40,      // [2 tiles] QK8 result in TMEM
+  M_DEC = 72,         // [2 tiles] the softmax has read S8 (the buffer is free)
   M_S16_FULL = 88,    // [2 tiles] QK16 result in TMEM
   M_P_FULL = 104,     // [2 tiles] P written, O rescaled, the step's S buffer free
   M_PV_DONE = 120,    // [2 tiles]
   M_DRAIN = 136,
   M_TMEM = 144,       // u32 TMEM base address
   M_ABORT = 148,      // u32 abort flag
-  M_REC = 152,        // u32 [2 tiles] recompute decision of the current step
   M_SFLAG = 160,      // u32 [2 tiles][2 step parities][4 warps] strip bits
   M_EXP8 = 256,       // u8 [256] exp8 table: code of fl8(exp(x)) per code of x
   M_XCH = 512,        // f32 [2 tiles][2 halves][128 rows] values exchanged between a row's two threads
@@ -235,8 +235,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
   cx.counters = p.counters;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 4; ++s) mbar_init(bar(M_S_FULL + 8 * s), 1);
     for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(M_S_FULL + 8 * s), 1);
       mbar_init(bar(M_KV_FULL + 8 * s), 1);
       mbar_init(bar(M_KV_EMPTY + 8 * s), 1);
       mbar_init(bar(M_DEC + 8 * s), 1);
@@ -300,16 +300,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     }
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    // Event driven: poll the tiles' barriers and issue whatever is ready --
-    // a tile's next QK8 once its previous P is in (the softmax is then done
-    // with the S buffer) and the K8 tile has landed, its QK16 when the
-    // softmax's decision asks for it, its P.V when P is in -- so the two
-    // tiles drift into alternation; tile 1 starts once tile 0 has published
-    // its first decision.  A stage is released once every tile that uses
-    // it has issued its P.V.
+    // Event driven: poll the tiles' barriers and issue whatever is ready.
+    // Per tile and step i: QK8(i) once the softmax has read S8(i-1) (DEC)
+    // and the K/V stage has landed; QK16(i) right behind it once the
+    // softmax has consumed S16(i-1) (P_FULL(i-1)) -- ahead of the decision,
+    // so a flagged step finds its 16-bit products ready; P.V(i) once P(i) is
+    // in.  The two tiles drift into alternation; tile 1 starts once tile 0
+    // has published its first decision.  A stage is released once every
+    // tile that uses it has issued its P.V.
     if (lane == 0 && J1 > J0) {
       auto stage_of = [&](int j) { return (j - J0) % C::NS; };
-      int nst[2] = {0, 0}, qk8_i[2] = {0, 0}, dec_i[2] = {0, 0}, p_i[2] = {0, 0};
+      int nst[2] = {0, 0}, qk8_i[2] = {0, 0}, qk16_i[2] = {0, 0}, dec_i[2] = {0, 0}, p_i[2] = {0, 0};
       for (int t = 0; t < C::NT; ++t) nst[t] = JHI(t) - JLO(t);
       int released = J0;
       bool ok = wait_bar(cx, bar(M_Q_FULL), 0);
@@ -322,30 +323,30 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           done = false;
           const uint32_t tm = tmem + t * C::TILE_COLS;
           const uint32_t qbase = sbase + C::OFF_Q + t * C::QT_BYTES;
-          // S buffer (step % 2) is free once P of the step two back is in
-          if (qk8_i[t] < nst[t] && qk8_i[t] <= p_i[t] + 1 && (t == 0 || dec_i[0] > 0 || nst[0] == 0)) {
+          if (qk8_i[t] < nst[t] && qk8_i[t] <= dec_i[t] && (t == 0 || dec_i[0] > 0 || nst[0] == 0)) {
             const int j = JLO(t) + qk8_i[t];
             if (mbar_test_wait(bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1)) {
               tc_fence_after();
-              Mma<D>::qk8(tm + C::S_OFF + (qk8_i[t] & 1) * kBN, qbase,
-                          sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES);
-              mma_commit(bar(M_S_FULL + 16 * t + 8 * (qk8_i[t] & 1)));
+              Mma<D>::qk8(tm + C::S8_OFF, qbase, sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES);
+              mma_commit(bar(M_S_FULL + 8 * t));
               ++qk8_i[t];
               progress = true;
             }
           }
+          if (qk16_i[t] < qk8_i[t] && qk16_i[t] <= p_i[t]) {
+            const int j = JLO(t) + qk16_i[t];
+            tc_fence_after();
+            Mma<D>::qk16(tm + C::S16_OFF, qbase + C::Q8_BYTES,
+                         sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES + C::K8_BYTES);
+            mma_commit(bar(M_S16_FULL + 8 * t));
+            ++qk16_i[t];
+            progress = true;
+          }
           if (dec_i[t] < qk8_i[t] && mbar_test_wait(bar(M_DEC + 8 * t), dec_i[t] & 1)) {
-            if (*(volatile uint32_t*)(misc + M_REC + 4 * t)) {
-              const int j = JLO(t) + dec_i[t];
-              tc_fence_after();
-              Mma<D>::qk16(tm + C::S_OFF + (dec_i[t] & 1) * kBN, qbase + C::Q8_BYTES,
-                           sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES + C::K8_BYTES);
-              mma_commit(bar(M_S16_FULL + 8 * t));
-            }
             ++dec_i[t];
             progress = true;
           }
-          if (p_i[t] < dec_i[t] && mbar_test_wait(bar(M_P_FULL + 8 * t), p_i[t] & 1)) {
+          if (p_i[t] < dec_i[t] && p_i[t] < qk16_i[t] && mbar_test_wait(bar(M_P_FULL + 8 * t), p_i[t] & 1)) {
             const int j = JLO(t) + p_i[t];
             tc_fence_after();
             Mma<D>::pv(tm, sbase + C::OFF_P + t * C::P_BYTES,
@@ -415,9 +416,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     float nq = 0.0f;
     if (R < p.N) nq = p.nq[((size_t)b * p.Hq + h) * p.N + R];
     uint32_t c_h0 = 0, c_h1 = 0, c_h2 = 0, c_strips = 0, c_st1 = 0, c_fl = 0, c_sat = 0, c_fix = 0,
-             c_rec = 0;  // per-thread counts (a CTA sees at most 2^21 logits per thread slot)
+             c_rec = 0, c_spec = 0;  // per-thread counts (a CTA sees at most 2^21 logits per thread slot)
     const int qtile = (q0 + tt * kBM) / kBN + (rw >> 1);  // 64-row query tile of this warp
-    int nrec = 0;
     const float sig = p.sigma_f;
     const float2 sig2 = make_float2(sig, sig);
     const float T = p.tau_abs;
@@ -443,12 +443,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       const float G = p.guard * sig * nq * nk;
 
       // ---- S = Q8 K8^T (fp32, TMEM) -> 8-bit logits
-      const uint32_t sbuf = lane_base + C::S_OFF + (jj & 1) * kBN + col0;  // this step's S buffer
       uint32_t a32[NC];
-      if (!fail) fail = !wait_bar_warp(cx, bar(M_S_FULL + 16 * tt + 8 * (jj & 1)), (jj >> 1) & 1);
+      if (!fail) fail = !wait_bar_warp(cx, bar(M_S_FULL + 8 * tt), jj & 1);
       if (!fail) {
         tc_fence_after();
-        tmem_ld32(sbuf, a32);
+        tmem_ld32(lane_base + C::S8_OFF + col0, a32);
         tmem_wait_ld();
       } else {
 #pragma unroll
@@ -596,13 +595,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
             sf[0] | (sf[1] << 1) | (s1[0] << 2) | (s1[1] << 3) | (sv[0] << 4) | (sv[1] << 5);
       // (after a failed wait a thread keeps stepping with its waits skipped,
       // so every thread of the tile reaches every barrier)
+      tc_fence_before();  // this thread's S8 reads before the buffer is handed back
       const bool any = bar_red_or(tile_bar, C::SM_THREADS, my_flag);
 
-      if (t == 0 && hf == 0 && !fail) {  // publish the decision; S8 has been read, the buffer may take S16
-        *(volatile uint32_t*)(misc + M_REC + 4 * tt) = any ? 1u : 0u;
-        tc_fence_before();
+      if (t == 0 && hf == 0 && !fail) {  // every S8 read is done: the buffer may take the next QK8
         mbar_arrive(bar(M_DEC + 8 * tt));
-        if (any) ++c_rec;
+        if (any) ++c_rec; else ++c_spec;
       }
       if (lane == 0 && hf == 0 && (rw & 1) == 0 && !fail) {
         // lane 0 of row groups 0 and 2 owns the 64-row query tile of groups (rw, rw+1)
@@ -665,12 +663,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       }
 
       // ---- 16-bit recompute for the rows of flagged sub-blocks
-      if (any && !fail) fail = !wait_bar_warp(cx, bar(M_S16_FULL + 8 * tt), nrec & 1);
+      // (the QK16 of every step is computed; a step without flags skips it)
+      if (any && !fail) fail = !wait_bar_warp(cx, bar(M_S16_FULL + 8 * tt), jj & 1);
       if (any && !fail) {
-        ++nrec;
         tc_fence_after();
         uint32_t r16[NC];
-        tmem_ld32(sbuf, r16);
+        tmem_ld32(lane_base + C::S16_OFF + col0, r16);
         tmem_wait_ld();
         if (my_flag && rowvis) {
           const float sl2 = sig * kLog2e, ml = m_new * kLog2e;
@@ -769,6 +767,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       if (lane == 0 && c_sat) atomicAdd(&p.counters[7], (u64)c_sat);
       if (lane == 0 && c_fix) atomicAdd(&p.counters[8], (u64)c_fix);
       if (t == 0 && hf == 0 && c_rec) atomicAdd(&p.counters[10], (u64)c_rec);
+      if (t == 0 && hf == 0 && c_spec) atomicAdd(&p.counters[11], (u64)c_spec);
     }
   }
 
