@@ -41,8 +41,8 @@ struct Cfg {
   static constexpr int NT = (D == 256) ? 1 : 2;  // query tiles of 128 rows per CTA
   static constexpr int NS = (D == 256) ? 1 : 2;  // K/V stages
   static constexpr int SM_THREADS = 256;                // softmax threads per tile (2 per row)
-  static constexpr int THREADS = 32 * (8 * NT + 2);
-  static constexpr int PRODUCER_WARP = 8 * NT, MMA_WARP = 8 * NT + 1;
+  static constexpr int THREADS = 32 * (8 * NT + 1 + NT);
+  static constexpr int PRODUCER_WARP = 8 * NT, MMA_WARP = 8 * NT + 1;  // + t: MMA warp of tile t
   static constexpr int F8_SWZ_ROW = (D == 64) ? 64 : 128;  // swizzle row width of 8-bit tiles
   static constexpr int Q8_BYTES = kBM * D;
   static constexpr int Q16_BYTES = kBM * D * 2;
@@ -67,22 +67,22 @@ struct Cfg {
   static constexpr int TILE_COLS = D + 2 * kBN;
   static constexpr int TMEM_COLS = 512;
   static_assert(NT * TILE_COLS <= TMEM_COLS, "TMEM budget");
-  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(SMEM + 1024 <= 227 * 1024, "shared memory budget (+ the static exp8 value table)");
 };
 
 // misc area (byte offsets inside OFF_MISC); per-tile barriers at + 8 * t
 enum : int {
   M_KV_FULL = 0,      // [2 stages]
-  M_KV_EMPTY = 16,    // [2 stages]
-  M_Q_FULL = 32,
-  M_S_FULL = 40,      // [2 tiles] QK8 result in TMEM
+  M_KV_EMPTY = 16,    // [2 stages][2 tiles] tile t is done with the stage (at + 16 s + 8 t)
+  M_Q_FULL = 48,
+  M_S_FULL = 56,      // [2 tiles] QK8 result in TMEM
   M_DEC = 72,         // [2 tiles] the softmax has read S8 (the buffer is free)
   M_S16_FULL = 88,    // [2 tiles] QK16 result in TMEM
-  M_P_FULL = 104,     // [2 tiles] P written, O rescaled, the step's S buffer free
+  M_P_FULL = 104,     // [2 tiles] P written, O rescaled, S16 read
   M_PV_DONE = 120,    // [2 tiles]
-  M_DRAIN = 136,
-  M_TMEM = 144,       // u32 TMEM base address
-  M_ABORT = 148,      // u32 abort flag
+  M_DRAIN = 136,      // [2 tiles]
+  M_TMEM = 152,       // u32 TMEM base address
+  M_ABORT = 156,      // u32 abort flag
   M_SFLAG = 160,      // u32 [2 tiles][2 step parities][4 warps] strip bits
   M_EXP8 = 256,       // u8 [256] exp8 table: code of fl8(exp(x)) per code of x
   M_XCH = 512,        // f32 [2 tiles][2 halves][128 rows] values exchanged between a row's two threads
@@ -106,12 +106,13 @@ constexpr unsigned long long kDrainNs = 200000000ull;  // 0.2 s for in-flight co
 __device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
                                            volatile unsigned int* gabort, unsigned long long timeout_ns,
                                            unsigned long long* counters) {
+  if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort) return false;
     if (*gabort) { *abort = 1u; return false; }
     if (globaltimer_ns() - t0 > timeout_ns) break;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
   }
   *abort = 1u;
   atomicExch((unsigned int*)gabort, 1u);
@@ -238,22 +239,27 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(M_S_FULL + 8 * s), 1);
       mbar_init(bar(M_KV_FULL + 8 * s), 1);
-      mbar_init(bar(M_KV_EMPTY + 8 * s), 1);
+      mbar_init(bar(M_KV_EMPTY + 16 * s), 1);
+      mbar_init(bar(M_KV_EMPTY + 16 * s + 8), 1);
       mbar_init(bar(M_DEC + 8 * s), 1);
       mbar_init(bar(M_S16_FULL + 8 * s), 1);
       mbar_init(bar(M_P_FULL + 8 * s), C::SM_THREADS);
       mbar_init(bar(M_PV_DONE + 8 * s), 1);
+      mbar_init(bar(M_DRAIN + 8 * s), 1);
     }
     mbar_init(bar(M_Q_FULL), 1);
-    mbar_init(bar(M_DRAIN), 1);
     *(volatile uint32_t*)(misc + M_ABORT) = 0u;
     fence_mbar_init();
   }
-  if (warp == C::MMA_WARP) tmem_alloc(bar(M_TMEM), C::TMEM_COLS);
-  // the exp8 table
-  if (threadIdx.x < kBM) {
-    misc[M_EXP8 + threadIdx.x] = p.exp8[threadIdx.x];
-    misc[M_EXP8 + kBM + threadIdx.x] = p.exp8[kBM + threadIdx.x];
+  if (warp == C::MMA_WARP) tmem_alloc(bar(M_TMEM), C::TMEM_COLS);  // the first MMA warp owns TMEM
+  // the exp8 table: codes (for the detector's comparisons with delta) and
+  // values as f16 in both halves of a word (P8 pairs are put together with
+  // one byte permute)
+  __shared__ uint32_t s_exp8v[256];
+  if (threadIdx.x < 256) {
+    const uint8_t code = p.exp8[threadIdx.x];
+    misc[M_EXP8 + threadIdx.x] = code;
+    s_exp8v[threadIdx.x] = (e4m3x2_to_f16x2((uint16_t)code) & 0xFFFFu) * 0x00010001u;
   }
   tc_fence_before();
   __syncthreads();
@@ -277,9 +283,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           tma_load_4d(qd + C::Q8_BYTES + c * kBM * 128, &p.tmQ16, bar(M_Q_FULL), c * 64, q0 + t * kBM, h, b);
       }
       int uses0 = 0, uses1 = 0;
+      uint32_t rel = 0u;  // releases waited for so far, one bit of parity per (tile, stage)
       for (int j = J0; j < J1 && !*cx.abort; ++j) {
         const int s = (j - J0) % C::NS, u = (j - J0) / C::NS;
-        if (u >= 1 && !wait_bar(cx, bar(M_KV_EMPTY + 8 * s), (u - 1) & 1)) break;
+        bool ok = true;
+        if (u >= 1) {  // the stage held key j - NS: wait until every tile that used it is done
+          const int jr = j - C::NS;
+#pragma unroll
+          for (int t = 0; t < C::NT; ++t) {
+            if (jr < JLO(t) || jr >= JHI(t)) continue;
+            const uint32_t bit = 1u << (2 * t + s);
+            ok = ok && wait_bar(cx, bar(M_KV_EMPTY + 16 * s + 8 * t), (rel & bit) ? 1u : 0u);
+            rel ^= bit;
+          }
+        }
+        if (!ok) break;
         const int key0 = j * kBN;
         const uint32_t st = sbase + C::OFF_ST + s * C::STAGE_BYTES;
         const uint32_t fb = bar(M_KV_FULL + 8 * s);
@@ -298,92 +316,62 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         drain_wait(bar(M_Q_FULL), 0);
       }
     }
-  } else if (warp == C::MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
-    // Event driven: poll the tiles' barriers and issue whatever is ready.
-    // Per tile and step i: QK8(i) once the softmax has read S8(i-1) (DEC)
-    // and the K/V stage has landed; QK16(i) right behind it once the
-    // softmax has consumed S16(i-1) (P_FULL(i-1)) -- ahead of the decision,
-    // so a flagged step finds its 16-bit products ready; P.V(i) once P(i) is
-    // in.  The two tiles drift into alternation; tile 1 starts once tile 0
-    // has published its first decision.  A stage is released once every
-    // tile that uses it has issued its P.V.
-    if (lane == 0 && J1 > J0) {
+  } else if (warp >= C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuers
+    // One warp per query tile, in a fixed order with blocking waits:
+    //   QK8(0) QK16(0) | DEC(i-1): QK8(i) | P(i-1): P.V(i-1) QK16(i) | ...
+    // QK8(i) goes into the S8 buffer once the softmax has read S8(i-1);
+    // QK16(i) into the S16 buffer once the softmax has consumed S16(i-1)
+    // (signalled with P(i-1)), ahead of the decision of step i, so a flagged
+    // step finds its 16-bit products ready.  After each P.V the tile hands
+    // the key's K/V stage back to the producer.
+    const int t = warp - C::MMA_WARP;
+    const int jlo = JLO(t), n = JHI(t) - JLO(t);
+    if (lane == 0 && n > 0) {
       auto stage_of = [&](int j) { return (j - J0) % C::NS; };
-      int nst[2] = {0, 0}, qk8_i[2] = {0, 0}, qk16_i[2] = {0, 0}, dec_i[2] = {0, 0}, p_i[2] = {0, 0};
-      for (int t = 0; t < C::NT; ++t) nst[t] = JHI(t) - JLO(t);
-      int released = J0;
+      auto kv = [&](int j) { return sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES; };
+      const uint32_t tm = tmem + t * C::TILE_COLS;
+      const uint32_t qbase = sbase + C::OFF_Q + t * C::QT_BYTES;
+      auto pv = [&](int i) {
+        Mma<D>::pv(tm, sbase + C::OFF_P + t * C::P_BYTES, kv(jlo + i) + C::K8_BYTES + C::K16_BYTES, i > 0);
+        mma_commit(bar(M_PV_DONE + 8 * t));
+        mma_commit(bar(M_KV_EMPTY + 16 * stage_of(jlo + i) + 8 * t));
+      };
       bool ok = wait_bar(cx, bar(M_Q_FULL), 0);
-      unsigned long long t_last = globaltimer_ns();
-      while (ok) {
-        bool done = true, progress = false;
-#pragma unroll
-        for (int t = 0; t < C::NT; ++t) {
-          if (p_i[t] >= nst[t]) continue;
-          done = false;
-          const uint32_t tm = tmem + t * C::TILE_COLS;
-          const uint32_t qbase = sbase + C::OFF_Q + t * C::QT_BYTES;
-          if (qk8_i[t] < nst[t] && qk8_i[t] <= dec_i[t] && (t == 0 || dec_i[0] > 0 || nst[0] == 0)) {
-            const int j = JLO(t) + qk8_i[t];
-            if (mbar_test_wait(bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1)) {
-              tc_fence_after();
-              Mma<D>::qk8(tm + C::S8_OFF, qbase, sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES);
-              mma_commit(bar(M_S_FULL + 8 * t));
-              ++qk8_i[t];
-              progress = true;
-            }
-          }
-          if (qk16_i[t] < qk8_i[t] && qk16_i[t] <= p_i[t]) {
-            const int j = JLO(t) + qk16_i[t];
-            tc_fence_after();
-            Mma<D>::qk16(tm + C::S16_OFF, qbase + C::Q8_BYTES,
-                         sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES + C::K8_BYTES);
-            mma_commit(bar(M_S16_FULL + 8 * t));
-            ++qk16_i[t];
-            progress = true;
-          }
-          if (dec_i[t] < qk8_i[t] && mbar_test_wait(bar(M_DEC + 8 * t), dec_i[t] & 1)) {
-            ++dec_i[t];
-            progress = true;
-          }
-          if (p_i[t] < dec_i[t] && p_i[t] < qk16_i[t] && mbar_test_wait(bar(M_P_FULL + 8 * t), p_i[t] & 1)) {
-            const int j = JLO(t) + p_i[t];
-            tc_fence_after();
-            Mma<D>::pv(tm, sbase + C::OFF_P + t * C::P_BYTES,
-                       sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES + C::K8_BYTES + C::K16_BYTES,
-                       p_i[t] > 0);
-            mma_commit(bar(M_PV_DONE + 8 * t));
-            ++p_i[t];
-            progress = true;
-            for (;;) {  // release the stages every tile is done with
-              bool used = false;
-              for (int u = 0; u < C::NT; ++u)
-                used |= released >= JLO(u) && released < JHI(u) && JLO(u) + p_i[u] <= released;
-              if (released >= J1 || used) break;
-              mma_commit(bar(M_KV_EMPTY + 8 * stage_of(released)));
-              ++released;
-            }
-          }
+      // with a single K/V stage, key i can only land after P.V(i-1) has
+      // released the stage, so P.V(i-1) goes first
+      constexpr bool kPvFirst = C::NS == 1;
+      for (int i = 0; ok && i < n; ++i) {
+        const int j = jlo + i;
+        if (i > 0) ok = wait_bar(cx, bar(M_DEC + 8 * t), (i - 1) & 1);
+        if (kPvFirst && ok && i > 0) {
+          ok = wait_bar(cx, bar(M_P_FULL + 8 * t), (i - 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          pv(i - 1);
         }
-        if (done) break;
-        if (progress) {
-          t_last = globaltimer_ns();
-        } else {
-          if (*cx.abort) break;
-          if (*cx.gabort) { *cx.abort = 1u; break; }
-          const unsigned long long now = globaltimer_ns();
-          if (now - t_last > cx.timeout_ns) {
-            *cx.abort = 1u;
-            atomicExch((unsigned int*)cx.gabort, 1u);
-            if (cx.counters) atomicExch(&cx.counters[9], 4ull);  // LAMP_ERR_TIMEOUT
-            break;
-          }
-          __nanosleep(32);
+        if (ok) ok = wait_bar(cx, bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        Mma<D>::qk8(tm + C::S8_OFF, qbase, kv(j));
+        mma_commit(bar(M_S_FULL + 8 * t));
+        if (!kPvFirst && i > 0) {
+          ok = wait_bar(cx, bar(M_P_FULL + 8 * t), (i - 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          pv(i - 1);
         }
+        Mma<D>::qk16(tm + C::S16_OFF, qbase + C::Q8_BYTES, kv(j) + C::K8_BYTES);
+        mma_commit(bar(M_S16_FULL + 8 * t));
       }
-      // make sure no MMA is still writing TMEM before it is released
-      mma_commit(bar(M_DRAIN));
-      drain_wait(bar(M_DRAIN), 0);
+      if (ok) ok = wait_bar(cx, bar(M_P_FULL + 8 * t), (n - 1) & 1);
+      if (ok) {
+        tc_fence_after();
+        pv(n - 1);
+      }
+      // make sure no MMA of this warp still writes TMEM before it is released
+      mma_commit(bar(M_DRAIN + 8 * t));
+      drain_wait(bar(M_DRAIN + 8 * t), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -411,10 +399,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     uint32_t* xb = (uint32_t*)(misc + M_XB) + tt * 2 * kBM;
     int lo, hi;
     row_range(p, R, lo, hi);
+    // key tiles the row sees whole: [jf0, jf1] (empty for a row past the end)
+    const int jf0 = (lo + kBN - 1) / kBN, jf1 = (hi + 1) / kBN - 1;
     float m = -INFINITY;
     float l = 0.0f;  // this half's running sum of the (rounded) P values fed to P.V
     float nq = 0.0f;
     if (R < p.N) nq = p.nq[((size_t)b * p.Hq + h) * p.N + R];
+    const float gq = p.guard * p.sigma_f * nq, satq = p.sigma_f * nq * (1.0f + p.guard);
     uint32_t c_h0 = 0, c_h1 = 0, c_h2 = 0, c_strips = 0, c_st1 = 0, c_fl = 0, c_sat = 0, c_fix = 0,
              c_rec = 0, c_spec = 0;  // per-thread counts (a CTA sees at most 2^21 logits per thread slot)
     const int qtile = (q0 + tt * kBM) / kBN + (rw >> 1);  // 64-row query tile of this warp
@@ -431,16 +422,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       const int jt = jlo_t + jj;
       const float nk = nk_next;  // loaded one step ahead
       if (jj + 1 < nsteps) nk_next = nkrow[jt + 1];
-      const int k0 = jt * kBN;
-      const int clo = imax(k0, lo), chi = imin(k0 + kBN - 1, hi);
-      const bool rowvis = clo <= chi;
-      uint32_t vm = 0u;  // visible columns of this half (bit c = key k0 + col0 + c)
-      {
+      bool rowvis = true;
+      uint32_t vm = 0xFFFFFFFFu;  // visible columns of this half (bit c = key k0 + col0 + c)
+      if (jt < jf0 || jt > jf1) {  // the row does not see the whole tile
+        const int k0 = jt * kBN;
+        const int clo = imax(k0, lo), chi = imin(k0 + kBN - 1, hi);
+        rowvis = clo <= chi;
         const int a = imax(clo - (k0 + col0), 0), z = imin(chi - (k0 + col0), NC - 1);
-        if (rowvis && a <= z) vm = (z == 31 ? 0xFFFFFFFFu : ((1u << (z + 1)) - 1u)) & ~((1u << a) - 1u);
+        vm = (rowvis && a <= z) ? ((z == 31 ? 0xFFFFFFFFu : ((1u << (z + 1)) - 1u)) & ~((1u << a) - 1u)) : 0u;
       }
       const bool all_full = __all_sync(0xffffffffu, vm == 0xFFFFFFFFu);
-      const float G = p.guard * sig * nq * nk;
+      const float G = gq * nk;            // bound on |A_tc sigma - A sigma| for this row and tile
+      const bool satp = satq * nk >= 400.0f;  // can a logit of this tile reach the 8-bit limit?
 
       // ---- S = Q8 K8^T (fp32, TMEM) -> 8-bit logits
       uint32_t a32[NC];
@@ -453,49 +446,65 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
 #pragma unroll
         for (int c = 0; c < NC; ++c) a32[c] = 0u;
       }
-      // S8 = fl8(A sigma) is certain unless y = A_tc sigma lies within G of an
-      // E4M3 rounding boundary (the two roundings of y -+ G then differ).  Of
+      // S8 = fl8(y), y = A_tc sigma, is certain unless y lies within G of an
+      // E4M3 rounding boundary (the roundings of y -+ G then differ).  Of
       // those, only logits that can change m, P8, the detector or the
       // saturation count need the exact value: m (the running max before
       // this tile) is exact and <= the new max, and a logit whose largest
-      // rounding is <= m - 6.75 rounds x8 to <= -7 (P8 = 0, below any
-      // delta > 0) and is not the maximum.  With delta = 0 all count.
+      // possible value fl8(y + G) is <= m - 6.75 rounds x8 to <= -7 (P8 = 0,
+      // below any delta > 0) and is not the maximum.  With delta = 0, or when
+      // the tile can reach the 8-bit limit, all count.  A group of 8 logits
+      // is screened first by its largest S8: its exact values are at most
+      // S8 + |S8|/4 + 2G + 2^-8, so below m - 6.75 nothing in it counts.
       uint32_t s8h[NC / 2];  // S8 pairs as f16x2 (exact)
+      uint32_t gmx[NC / 8];  // per group of 8: max of the pairs (f16x2)
       uint32_t unc = 0u;     // logits to re-derive exactly
       {
+        const float thr = (dcode == 0u || satp) ? -INFINITY : m - 6.75f;
+        const float c = thr - 2.0f * G - 0x1p-8f;
+        const __half2 sthr = __half2half2(__float2half_rd(c >= 0.0f ? 0.79f * c : 1.34f * c));
+        const __half2 lthr = __half2half2(__float2half_rd(thr));
         const float2 gm = make_float2(-G, -G), gp = make_float2(G, G);
-        const float thr = m - 6.75f;
 #pragma unroll
-        for (int g4 = 0; g4 < NC / 8; ++g4) {  // 4 pairs at a time, one branch
-          float2 yh[4];
-          uint32_t d4 = 0u, d16[4];
+        for (int g4 = 0; g4 < NC / 8; ++g4) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int i = 4 * g4 + k;
-            const float2 av = make_float2(__uint_as_float(a32[2 * i]), __uint_as_float(a32[2 * i + 1]));
-            const float2 yl = __ffma2_rn(av, sig2, gm);
-            yh[k] = __ffma2_rn(av, sig2, gp);
-            const uint16_t cl = cvt_e4m3x2(yl.y, yl.x), ch = cvt_e4m3x2(yh[k].y, yh[k].x);
-            s8h[i] = e4m3x2_to_f16x2(cl);
-            d16[k] = (uint32_t)(cl ^ ch);
-            d4 |= d16[k];
+            const float2 y = __fmul2_rn(make_float2(__uint_as_float(a32[2 * i]), __uint_as_float(a32[2 * i + 1])), sig2);
+            s8h[i] = e4m3x2_to_f16x2(cvt_e4m3x2(y.y, y.x));
           }
-          if (d4 != 0u) {
+          const __half2 mg = __hmax2(__hmax2(as_half2(s8h[4 * g4]), as_half2(s8h[4 * g4 + 1])),
+                                     __hmax2(as_half2(s8h[4 * g4 + 2]), as_half2(s8h[4 * g4 + 3])));
+          gmx[g4] = *reinterpret_cast<const uint32_t*>(&mg);
+          if (__any_sync(0xffffffffu, __hgt2_mask(mg, sthr) != 0u)) {  // rare: screen the group
+            uint32_t d4 = 0u, d16[4], hh[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int i = 4 * g4 + k;
-              const float h0 = yh[k].x, h1 = yh[k].y;
-              const bool r0 = dcode == 0u || h0 + 0.125f * fabsf(h0) + 0x1p-8f > thr || fabsf(h0) >= 400.0f;
-              const bool r1 = dcode == 0u || h1 + 0.125f * fabsf(h1) + 0x1p-8f > thr || fabsf(h1) >= 400.0f;
-              if ((d16[k] & 0xFFu) && r0) unc |= 1u << (2 * i);
-              if ((d16[k] >> 8) && r1) unc |= 1u << (2 * i + 1);
+              const float2 av = make_float2(__uint_as_float(a32[2 * i]), __uint_as_float(a32[2 * i + 1]));
+              const float2 yl = __ffma2_rn(av, sig2, gm), yh = __ffma2_rn(av, sig2, gp);
+              const uint16_t cl = cvt_e4m3x2(yl.y, yl.x), ch = cvt_e4m3x2(yh.y, yh.x);
+              d16[k] = (uint32_t)(cl ^ ch);
+              d4 |= d16[k];
+              hh[k] = e4m3x2_to_f16x2(ch);
+            }
+            if (d4 != 0u) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int i = 4 * g4 + k;
+                const uint32_t rel = __hgt2_mask(as_half2(hh[k]), lthr);
+                if ((d16[k] & 0xFFu) && (rel & 0xFFFFu)) unc |= 1u << (2 * i);
+                if ((d16[k] >> 8) && (rel >> 16)) unc |= 1u << (2 * i + 1);
+              }
             }
           }
         }
       }
       unc &= vm;
       if (fail) unc = 0u;
+      bool gmx_ok = all_full;  // group maxima still describe s8h (no fix-up, no hidden key)
       if (__any_sync(0xffffffffu, unc != 0u)) {
+        if (unc) gmx_ok = false;
         const uint8_t* sK8 = smem + C::OFF_ST + ((jt - J0) % C::NS) * C::STAGE_BYTES;
         for (;;) {
           const unsigned who = __ballot_sync(0xffffffffu, unc != 0u);
@@ -530,9 +539,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       // ---- tile max over both halves, running max
       float m_tile;
       {
-        __half2 mx = as_half2(s8h[0]);
+        __half2 mx;
+        if (gmx_ok) {
+          mx = __hmax2(__hmax2(as_half2(gmx[0]), as_half2(gmx[1])), __hmax2(as_half2(gmx[2]), as_half2(gmx[3])));
+        } else {
+          mx = as_half2(s8h[0]);
 #pragma unroll
-        for (int i = 1; i < NC / 2; ++i) mx = __hmax2(mx, as_half2(s8h[i]));
+          for (int i = 1; i < NC / 2; ++i) mx = __hmax2(mx, as_half2(s8h[i]));
+        }
         const float mine = fmaxf(__low2float(mx), __high2float(mx));
         xch[hf * kBM + t] = mine;
         bar_sync(pair_bar, 64);
@@ -567,7 +581,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         bar_sync(pair_bar, 64);
         if (maybe_neg) flg = (mine | xb[(1 - hf) * kBM + t]) != 0u;
       }
-      if (rowvis && sig * nq * nk * (1.0f + p.guard) >= 432.0f) {
+      if (rowvis && satp) {
 #pragma unroll
         for (int i = 0; i < NC / 2; ++i) {
           const __half2 sv = as_half2(s8h[i]);
@@ -576,23 +590,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       }
 
       // ---- sub-block bits: lanes 0-15 and 16-31 of a warp are two sub-blocks
-      const unsigned bv = __ballot_sync(0xffffffffu, rowvis);
-      const unsigned b1 = __ballot_sync(0xffffffffu, st1);
-      const unsigned bf = __ballot_sync(0xffffffffu, flg);
-      uint32_t sv[2], s1[2], sf[2];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        sv[hh] = ((bv >> (16 * hh)) & 0xFFFFu) != 0u;
-        s1[hh] = ((b1 >> (16 * hh)) & 0xFFFFu) != 0u;
-        sf[hh] = ((bf >> (16 * hh)) & 0xFFFFu) != 0u;
-        if (p.force == 1) sf[hh] = sv[hh];
-        if (p.force == 2) sf[hh] = 0u;
-      }
-      const bool my_flag = ((lane >> 4) ? sf[1] : sf[0]) != 0u;
+      unsigned bf = __ballot_sync(0xffffffffu, flg);
+      unsigned bv = 0u;
+      if (p.force != 0 || hf == 0) bv = __ballot_sync(0xffffffffu, rowvis);
+      if (p.force == 1) bf = bv;
+      if (p.force == 2) bf = 0u;
+      const bool my_flag = ((lane >> 4) ? (bf >> 16) : (bf & 0xFFFFu)) != 0u;
       uint8_t* sflag = misc + M_SFLAG + 32 * tt + 16 * (jj & 1);
-      if (lane == 0 && hf == 0)
-        *(volatile uint32_t*)(sflag + 4 * rw) =
-            sf[0] | (sf[1] << 1) | (s1[0] << 2) | (s1[1] << 3) | (sv[0] << 4) | (sv[1] << 5);
+      if (hf == 0) {  // the owner of the 64-row query tile needs the sub-block bits
+        const unsigned b1 = __ballot_sync(0xffffffffu, st1);
+        if (lane == 0)
+          *(volatile uint32_t*)(sflag + 4 * rw) =
+              ((bf & 0xFFFFu) != 0u) | (((bf >> 16) != 0u) << 1) | (((b1 & 0xFFFFu) != 0u) << 2) |
+              (((b1 >> 16) != 0u) << 3) | (((bv & 0xFFFFu) != 0u) << 4) | (((bv >> 16) != 0u) << 5);
+      }
       // (after a failed wait a thread keeps stepping with its waits skipped,
       // so every thread of the tile reaches every barrier)
       tc_fence_before();  // this thread's S8 reads before the buffer is handed back
@@ -630,8 +641,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         for (int i = 0; i < NC / 2; ++i) {
           const __half2 xh = __hsub2(as_half2(s8h[i]), mh);
           const uint32_t x8 = cvt_e4m3x2_f16x2(xh);
-          const uint32_t pc = (uint32_t)tab[x8 & 0xFFu] | ((uint32_t)tab[x8 >> 8] << 8);
-          pw[i] = e4m3x2_to_f16x2((uint16_t)pc);
+          pw[i] = __byte_perm(s_exp8v[x8 & 0xFFu], s_exp8v[x8 >> 8], 0x7610);
         }
       } else {
 #pragma unroll
