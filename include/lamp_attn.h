@@ -191,6 +191,10 @@ void lamp_exp8_table(uint8_t out[256]);
  *   which 0: out[128 x 64]    = A . B^T, A [128 x d], B [64 x d] E4M3 codes (uint8)
  *   which 1: out[128 x 64]    = A . B^T, A [128 x d], B [64 x d] BF16
  *   which 2: out[128 x d]      = P . V, P [128 x 64], V [64 x d] FP16 (V MN-major)
+ *   which 3: out[i] = the 8-bit logit the exact re-derivation produces for
+ *            the dot product a[i] * 2^-18 (a: int64[d]) and the scale b[0]
+ *            (b: double[1]): E4M3 rounding of the float64 product, as a
+ *            float; d = count, 1..65536.
  * a, b: DEVICE, row-major as listed; out: DEVICE float32, row-major.
  * Returns LAMP_OK or an error code after synchronising `stream`.
  */

@@ -244,6 +244,12 @@ int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out, float*
   fp.out_f32 = s.out_dtype == LAMP_DT_FP32;
   fp.sigma_f = (float)sigma_d;
   fp.sigma_d = sigma_d;
+  {
+    int e = 0;
+    const double f = std::frexp(sigma_d, &e);  // sigma_d = f * 2^e, f in [0.5, 1)
+    fp.sig_m = (unsigned long long)std::ldexp(f, 53);
+    fp.sig_e = e - 53;
+  }
   fp.guard = kGuard;
   fp.tau_abs = host_tau_abs(tau);
   fp.delta_code = host_delta_code(delta);

@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
 #pragma unroll
         for (int c = 0; c < NC; ++c) a32[c] = 0u;
       }
-      // S8 = fl8(y), y = A_tc sigma, is certain unless y lies within G of an
+      // S8 = fl8(A sigma) is certain unless y = A_tc sigma lies within G of an
       // E4M3 rounding boundary (the roundings of y -+ G then differ).  Of
       // those, only logits that can change m, P8, the detector or the
       // saturation count need the exact value: m (the running max before
@@ -454,48 +454,42 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       // possible value fl8(y + G) is <= m - 6.75 rounds x8 to <= -7 (P8 = 0,
       // below any delta > 0) and is not the maximum.  With delta = 0, or when
       // the tile can reach the 8-bit limit, all count.  A group of 8 logits
-      // is screened first by its largest S8: its exact values are at most
-      // S8 + |S8|/4 + 2G + 2^-8, so below m - 6.75 nothing in it counts.
+      // is looked at only if one of them is uncertain and its largest S8 is
+      // close enough to m: the exact values are at most S8 + |S8|/4 + 3G +
+      // 2^-8 (S8 the lower rounding), so below m - 6.75 nothing in it counts.
       uint32_t s8h[NC / 2];  // S8 pairs as f16x2 (exact)
       uint32_t gmx[NC / 8];  // per group of 8: max of the pairs (f16x2)
       uint32_t unc = 0u;     // logits to re-derive exactly
       {
         const float thr = (dcode == 0u || satp) ? -INFINITY : m - 6.75f;
-        const float c = thr - 2.0f * G - 0x1p-8f;
-        const __half2 sthr = __half2half2(__float2half_rd(c >= 0.0f ? 0.79f * c : 1.34f * c));
         const __half2 lthr = __half2half2(__float2half_rd(thr));
+        const float c = thr - 3.0f * G - 0x1p-8f;
+        const __half2 sthr = __half2half2(__float2half_rd(c >= 0.0f ? 0.79f * c : 1.34f * c));
         const float2 gm = make_float2(-G, -G), gp = make_float2(G, G);
 #pragma unroll
-        for (int g4 = 0; g4 < NC / 8; ++g4) {
+        for (int g4 = 0; g4 < NC / 8; ++g4) {  // 4 pairs at a time, one branch
+          uint32_t d4 = 0u, d16[4], ch4[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int i = 4 * g4 + k;
-            const float2 y = __fmul2_rn(make_float2(__uint_as_float(a32[2 * i]), __uint_as_float(a32[2 * i + 1])), sig2);
-            s8h[i] = e4m3x2_to_f16x2(cvt_e4m3x2(y.y, y.x));
+            const float2 av = make_float2(__uint_as_float(a32[2 * i]), __uint_as_float(a32[2 * i + 1]));
+            const float2 yl = __ffma2_rn(av, sig2, gm), yh = __ffma2_rn(av, sig2, gp);
+            const uint16_t cl = cvt_e4m3x2(yl.y, yl.x), ch = cvt_e4m3x2(yh.y, yh.x);
+            s8h[i] = e4m3x2_to_f16x2(cl);
+            d16[k] = (uint32_t)(cl ^ ch);
+            d4 |= d16[k];
+            ch4[k] = ch;
           }
           const __half2 mg = __hmax2(__hmax2(as_half2(s8h[4 * g4]), as_half2(s8h[4 * g4 + 1])),
                                      __hmax2(as_half2(s8h[4 * g4 + 2]), as_half2(s8h[4 * g4 + 3])));
           gmx[g4] = *reinterpret_cast<const uint32_t*>(&mg);
-          if (__any_sync(0xffffffffu, __hgt2_mask(mg, sthr) != 0u)) {  // rare: screen the group
-            uint32_t d4 = 0u, d16[4], hh[4];
+          if (d4 != 0u && __hgt2_mask(mg, sthr) != 0u) {  // rare: a logit near a boundary, maybe relevant
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int i = 4 * g4 + k;
-              const float2 av = make_float2(__uint_as_float(a32[2 * i]), __uint_as_float(a32[2 * i + 1]));
-              const float2 yl = __ffma2_rn(av, sig2, gm), yh = __ffma2_rn(av, sig2, gp);
-              const uint16_t cl = cvt_e4m3x2(yl.y, yl.x), ch = cvt_e4m3x2(yh.y, yh.x);
-              d16[k] = (uint32_t)(cl ^ ch);
-              d4 |= d16[k];
-              hh[k] = e4m3x2_to_f16x2(ch);
-            }
-            if (d4 != 0u) {
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int i = 4 * g4 + k;
-                const uint32_t rel = __hgt2_mask(as_half2(hh[k]), lthr);
-                if ((d16[k] & 0xFFu) && (rel & 0xFFFFu)) unc |= 1u << (2 * i);
-                if ((d16[k] >> 8) && (rel >> 16)) unc |= 1u << (2 * i + 1);
-              }
+              const uint32_t rel = __hgt2_mask(as_half2(e4m3x2_to_f16x2((uint16_t)ch4[k])), lthr);
+              if ((d16[k] & 0xFFu) && (rel & 0xFFFFu)) unc |= 1u << (2 * i);
+              if ((d16[k] >> 8) && (rel >> 16)) unc |= 1u << (2 * i + 1);
             }
           }
         }
@@ -513,7 +507,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           const int cb = __shfl_sync(0xffffffffu, unc ? (__ffs(unc) - 1) : 0, src);
           const long long acc = exact_dot<D>(sQ8, sK8, rw * 32 + src, col0 + cb, lane);
           if (lane == src) {
-            const uint32_t hv = e4m3_f16_from_double((double)acc * 0x1p-18 * p.sigma_d);
+            const uint32_t hv = e4m3_f16_of_scaled(acc, p.sig_m, p.sig_e);
             // replace half (cb & 1) of pair cb >> 1 (bit tests, no indexed access)
             const uint32_t hit = 1u << cb;
 #pragma unroll

@@ -82,6 +82,16 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+__global__ void lamp_round_selftest_kernel(const long long* acc, const double* sigma, float* out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  int e = 0;
+  const double f = frexp(*sigma, &e);
+  const unsigned long long m = (unsigned long long)ldexp(f, 53);
+  const uint32_t h = e4m3_f16_of_scaled(acc[i], m, e - 53);
+  out[i] = __half2float(__ushort_as_half((unsigned short)h));
+}
+
 template <int D>
 static cudaError_t run_selftest(int which, const void* a, const void* b, float* out, unsigned int* status,
                                 cudaStream_t st) {
@@ -95,8 +105,8 @@ static cudaError_t run_selftest(int which, const void* a, const void* b, float* 
 }  // namespace lamp
 
 extern "C" int lamp_selftest(int which, const void* a, const void* b, float* out, int d, void* stream) {
-  if (!a || !b || !out || which < 0 || which > 2) return LAMP_ERR_INVALID_ARG;
-  if (d != 64 && d != 128 && d != 256) return LAMP_ERR_UNSUPPORTED;
+  if (!a || !b || !out || which < 0 || which > 3) return LAMP_ERR_INVALID_ARG;
+  if (which == 3 ? (d < 1 || d > 65536) : (d != 64 && d != 128 && d != 256)) return LAMP_ERR_UNSUPPORTED;
   int dev = 0, maj = 0, min = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LAMP_ERR_CUDA;
   cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev);
@@ -106,9 +116,15 @@ extern "C" int lamp_selftest(int which, const void* a, const void* b, float* out
   unsigned int* status = nullptr;
   if (cudaMallocAsync((void**)&status, sizeof(unsigned int), st) != cudaSuccess) return LAMP_ERR_CUDA;
   cudaMemsetAsync(status, 0, sizeof(unsigned int), st);
-  cudaError_t e = d == 64    ? lamp::run_selftest<64>(which, a, b, out, status, st)
+  cudaError_t e = cudaSuccess;
+  if (which == 3) {
+    lamp::lamp_round_selftest_kernel<<<(d + 255) / 256, 256, 0, st>>>((const long long*)a, (const double*)b, out, d);
+    e = cudaGetLastError();
+  } else {
+    e = d == 64    ? lamp::run_selftest<64>(which, a, b, out, status, st)
                   : d == 128 ? lamp::run_selftest<128>(which, a, b, out, status, st)
                              : lamp::run_selftest<256>(which, a, b, out, status, st);
+  }
   unsigned int hs = 0;
   if (e == cudaSuccess) e = cudaMemcpyAsync(&hs, status, sizeof(hs), cudaMemcpyDeviceToHost, st);
   cudaFreeAsync(status, st);

@@ -167,10 +167,13 @@ def exp8_table() -> bytes:
 
 
 def selftest(which: int, a, b, d: int):
-    """Run a tcgen05 building-block check; returns the float32 result."""
+    """Run a device building-block check; returns the float32 result
+    (which 3: the exact 8-bit re-derivation of a[i] * 2^-18 * b[0], d values)."""
     lib = load()
-    ncols = d if which == 2 else 64
-    out = torch.full((128, ncols), float("nan"), dtype=torch.float32, device=a.device)
+    if which == 3:
+        out = torch.full((d,), float("nan"), dtype=torch.float32, device=a.device)
+    else:
+        out = torch.full((128, d if which == 2 else 64), float("nan"), dtype=torch.float32, device=a.device)
     s = torch.cuda.current_stream(a.device)
     _check(lib.lamp_selftest(which, a.data_ptr(), b.data_ptr(), out.data_ptr(), d, s.cuda_stream))
     return out

@@ -68,3 +68,31 @@ def test_fp16_pv_mma_mn_major(lamp, d):
     out = lamp.selftest(2, p.cuda(), v.cuda(), d).cpu().double()
     exact = p.double() @ v.double()
     assert (out - exact).abs().max().item() <= 1e-3
+
+
+@pytest.mark.parametrize("scale", [128 ** -0.5, 256 ** -0.5, 0.125, 0.0721])
+def test_exact_rederivation_rounding(lamp, scale):
+    """The integer re-derivation of an uncertain 8-bit logit equals the
+    E4M3 rounding of the float64 product A * sigma (A exact)."""
+    rng = np.random.default_rng(7)
+    n = 65536
+    # exact dot products * 2^18: magnitudes across the whole E4M3 range of
+    # the logit, zero, and values right at E4M3 midpoints of the product
+    mag = np.exp(rng.uniform(np.log(1.0), np.log(2.0 ** 42), n))
+    acc = (np.round(mag) * rng.choice([-1, 1], n)).astype(np.int64)
+    acc[:16] = [0, 1, -1, 2, 3, 2**42, -(2**42), 5, 7, 11, 13, 2**20, 2**30, 2**35, 12345, -54321]
+    from oracle.reference_attn import e4m3_sorted_values
+    mids = e4m3_sorted_values()
+    mids = mids[mids > 0]
+    mid = (mids[1:] + mids[:-1]) / 2
+    near = np.round(mid / scale * 2.0 ** 18).astype(np.int64)
+    k = min(len(near), 4096)
+    acc[16:16 + k] = near[:k]
+    acc[16 + k:16 + 2 * k] = near[:k] + 1
+    acc[16 + 2 * k:16 + 3 * k] = -(near[:k] - 1)
+    a = torch.from_numpy(acc).cuda()
+    b = torch.tensor([scale], dtype=torch.float64).cuda()
+    got = lamp.selftest(3, a, b, n).cpu().numpy().astype(np.float64)
+    want = F.e4m3_round(acc.astype(np.float64) * 2.0 ** -18 * np.float64(scale))
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, (acc[bad[:5]], got[bad[:5]], want[bad[:5]])
