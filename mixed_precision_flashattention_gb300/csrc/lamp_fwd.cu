@@ -405,7 +405,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     float l = 0.0f;  // this half's running sum of the (rounded) P values fed to P.V
     float nq = 0.0f;
     if (R < p.N) nq = p.nq[((size_t)b * p.Hq + h) * p.N + R];
-    const float gq = p.guard * p.sigma_f * nq, satq = p.sigma_f * nq * (1.0f + p.guard);
+    // exactness guard: |A_tc - A| * sigma <= gq * (max ||k8|| + 2^-6)
+    const float gq = p.guard * p.sigma_f * (nq + 0x1p-6f), satq = p.sigma_f * nq * (1.0f + p.guard);
     uint32_t c_h0 = 0, c_h1 = 0, c_h2 = 0, c_strips = 0, c_st1 = 0, c_fl = 0, c_sat = 0, c_fix = 0,
              c_rec = 0, c_spec = 0;  // per-thread counts (a CTA sees at most 2^21 logits per thread slot)
     const int qtile = (q0 + tt * kBM) / kBN + (rw >> 1);  // 64-row query tile of this warp
@@ -432,7 +433,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         vm = (rowvis && a <= z) ? ((z == 31 ? 0xFFFFFFFFu : ((1u << (z + 1)) - 1u)) & ~((1u << a) - 1u)) : 0u;
       }
       const bool all_full = __all_sync(0xffffffffu, vm == 0xFFFFFFFFu);
-      const float G = gq * nk;            // bound on |A_tc sigma - A sigma| for this row and tile
+      const float G = gq * (nk + 0x1p-6f);  // bound on |A_tc sigma - A sigma| for this row and tile
       const bool satp = satq * nk >= 400.0f;  // can a logit of this tile reach the 8-bit limit?
 
       // ---- S = Q8 K8^T (fp32, TMEM) -> 8-bit logits
