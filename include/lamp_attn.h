@@ -172,6 +172,42 @@ int lamp_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out
                           float* lse, const lamp_shapes* shapes, int mask_kind,
                           float delta, float tau, lamp_stats* stats);
 
+/*
+ * lamp_attn_fwd_host: lamp_attn_fwd on HOST q, k, v, out and lse, for
+ * callers whose tensors live in host memory (page-locked memory lets the
+ * copies run asynchronously and at full link speed).  The paper has no
+ * counterpart: this is a data-movement variant only, and the results are
+ * bit-identical to lamp_attn_fwd on the same inputs.
+ *
+ * The batch -- and, while batch * groups < 4, the kv-head groups -- is cut
+ * into chunks; per chunk the inputs are copied to the device, the forward
+ * pass runs on shapes->stream and the outputs are copied back, on two
+ * internal copy streams and two device slots, so the copies of one chunk
+ * overlap the computation of its neighbours.
+ *   q, k, v, out  HOST, BSHD with the strides of `shapes` (elements); the
+ *                 head and head_dim dimensions must be dense
+ *                 (stride[2] == head_dim).
+ *   lse           HOST [B, Hq, N] fp32 or NULL.
+ *   stats         DEVICE buffers as for lamp_attn_fwd (mask written per
+ *                 chunk; counters summed over the chunks), or NULL.
+ *   dev_buffer    DEVICE scratch of lamp_attn_host_buffer_bytes() bytes,
+ *                 256-byte aligned, or NULL (allocated and freed
+ *                 stream-ordered on shapes->stream); shapes->workspace is
+ *                 not used.
+ * Synchronous: returns after out and lse hold the results (the status of
+ * the device side is in counters[LAMP_CNT_STATUS] when counters are given).
+ * Errors as lamp_attn_fwd; LAMP_ERR_WORKSPACE if dev_buffer is too small or
+ * misaligned.
+ */
+int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out,
+                       float* lse, const lamp_shapes* shapes, int mask_kind,
+                       float delta, float tau, lamp_stats* stats,
+                       void* dev_buffer, size_t dev_buffer_bytes);
+
+/* Device scratch lamp_attn_fwd_host needs for these shapes; 0 on invalid
+ * shapes. */
+size_t lamp_attn_host_buffer_bytes(const lamp_shapes* shapes);
+
 /* Static, human-readable text for a lamp_status value. */
 const char* lamp_strerror(int status);
 

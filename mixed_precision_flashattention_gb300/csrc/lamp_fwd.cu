@@ -630,17 +630,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       // to the single rounding for E4M3 operands), P8 from the exp8 table;
       // rows of flagged sub-blocks take P16 below instead
       uint32_t pw[NC / 2];
-      if (rowvis && !my_flag) {
+#pragma unroll
+      for (int i = 0; i < NC / 2; ++i) pw[i] = 0u;
+      const bool want_p8 = rowvis && !my_flag;
+      if (__any_sync(0xffffffffu, want_p8)) {  // warp-uniform: most warps have only flagged rows
         const __half2 mh = __float2half2_rn(m_new);
 #pragma unroll
         for (int i = 0; i < NC / 2; ++i) {
           const __half2 xh = __hsub2(as_half2(s8h[i]), mh);
           const uint32_t x8 = cvt_e4m3x2_f16x2(xh);
-          pw[i] = __byte_perm(s_exp8v[x8 & 0xFFu], s_exp8v[x8 >> 8], 0x7610);
+          const uint32_t v = __byte_perm(s_exp8v[x8 & 0xFFu], s_exp8v[x8 >> 8], 0x7610);
+          pw[i] = want_p8 ? v : 0u;
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < NC / 2; ++i) pw[i] = 0u;
       }
 
       // ---- the previous P.V must be done before O is rescaled and P is
@@ -677,11 +678,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         tmem_wait_ld();
         if (my_flag && rowvis) {
           const float sl2 = sig * kLog2e, ml = m_new * kLog2e;
+          const float2 sl22 = make_float2(sl2, sl2), ml2 = make_float2(-ml, -ml);
 #pragma unroll
           for (int i = 0; i < NC / 2; ++i) {
-            const float e0 = ex2_approx(fmaf(__uint_as_float(r16[2 * i]), sl2, -ml));
-            const float e1 = ex2_approx(fmaf(__uint_as_float(r16[2 * i + 1]), sl2, -ml));
-            pw[i] = cvt_f16x2_sat(e1, e0);
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(r16[2 * i]), __uint_as_float(r16[2 * i + 1])),
+                                        sl22, ml2);
+            pw[i] = cvt_f16x2_sat(ex2_approx(x.y), ex2_approx(x.x));
           }
           if (!all_full) {
 #pragma unroll
@@ -697,10 +699,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         {  // l = alpha l + sum of this half's P (exact fp16 values, fp32 sums)
           float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-          for (int i = 0; i < NC / 2; ++i) {
-            ls[i & 1] = add_f32_f16lo(ls[i & 1], pw[i]);
-            ls[2 + (i & 1)] = add_f32_f16hi(ls[2 + (i & 1)], pw[i]);
-          }
+          for (int i = 0; i < NC / 2; ++i) add_f32_f16x2(ls[2 * (i & 1)], ls[2 * (i & 1) + 1], pw[i]);
           l = fmaf(alpha, l, (ls[0] + ls[1]) + (ls[2] + ls[3]));
         }
         // P row half -> shared memory (K-major, 128-byte swizzle)

@@ -217,6 +217,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 // acc + (fp16 half of h selected by hi), in fp32
+// acc_lo += low half of h, acc_hi += high half of h (f16 values added to
+// float accumulators with one rounding each).
+__device__ __forceinline__ void add_f32_f16x2(float& acc_lo, float& acc_hi, uint32_t h) {
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi) : "r"(h));
+}
 __device__ __forceinline__ float add_f32_f16lo(float acc, uint32_t h) {
   float r;
   const uint16_t v = (uint16_t)(h & 0xFFFFu);

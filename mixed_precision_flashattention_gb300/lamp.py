@@ -24,7 +24,8 @@ NUM_COUNTERS = 16
 COUNTER_NAMES = ["tiles", "hist0", "hist1", "hist2p", "strips", "stage1", "flagged",
                  "s8_saturated", "fixups", "status", "recompute_steps", "spec_waste"]
 EXPORTS = ["lamp_attn_fwd", "lamp_attn_fwd_noalloc", "lamp_attn_workspace_bytes", "lamp_strerror",
-           "lamp_version", "lamp_exp8_table", "lamp_selftest"]
+           "lamp_version", "lamp_exp8_table", "lamp_selftest", "lamp_attn_fwd_host",
+           "lamp_attn_host_buffer_bytes"]
 
 
 class LampShapes(ctypes.Structure):
@@ -79,6 +80,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.lamp_version.restype = ctypes.c_char_p
     lib.lamp_exp8_table.restype = None
     lib.lamp_exp8_table.argtypes = [ctypes.c_void_p]
+    lib.lamp_attn_fwd_host.restype = ctypes.c_int
+    lib.lamp_attn_fwd_host.argtypes = lib.lamp_attn_fwd.argtypes + [ctypes.c_void_p, ctypes.c_size_t]
+    lib.lamp_attn_host_buffer_bytes.restype = ctypes.c_size_t
+    lib.lamp_attn_host_buffer_bytes.argtypes = [ctypes.POINTER(LampShapes)]
     lib.lamp_selftest.restype = ctypes.c_int
     lib.lamp_selftest.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_int, ctypes.c_void_p]
@@ -148,6 +153,63 @@ def lamp_attn_fwd(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -
     code = lib.lamp_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                              lse.data_ptr() if lse is not None else None, ctypes.byref(sh),
                              MASK[mask], float(delta), float(tau), ctypes.byref(stats))
+    _check(code)
+    return out, lse, mask_bytes, counters
+
+
+def host_buffer_bytes(q, k, v, out=None, **kw) -> int:
+    """Device scratch bytes of lamp_attn_fwd_host for these (host) tensors."""
+    out = q if out is None else out
+    return int(load().lamp_attn_host_buffer_bytes(ctypes.byref(_host_shapes(q, k, v, out, **kw))))
+
+
+def _host_shapes(q, k, v, out, *, window=0, scale=0.0, force="off", stream=None, device=None):
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    B, N, Hq, d = q.shape
+    sh = LampShapes()
+    sh.batch, sh.seqlen, sh.heads_q, sh.heads_kv, sh.head_dim = B, N, Hq, k.shape[2], d
+    for name, t in (("q_stride", q), ("k_stride", k), ("v_stride", v), ("o_stride", out)):
+        st = t.stride()
+        if st[3] != 1:
+            raise LampError(f"{name}: head_dim must be contiguous")
+        getattr(sh, name)[:] = [st[0], st[1], st[2]]
+    sh.window = int(window)
+    sh.softmax_scale = float(scale)
+    sh.in_dtype = DT[q.dtype]
+    sh.out_dtype = DT[out.dtype]
+    sh.force = FORCE[force]
+    sh.stream = s.cuda_stream
+    return sh
+
+
+def lamp_attn_fwd_host(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -8, tau=2.0 ** -1,
+                       force="off", out=None, out_dtype=None, lse=None, want_lse=True, mask_bytes=None,
+                       counters=None, dev_buffer=None, stream=None, device=None):
+    """Forward pass on HOST tensors (CPU, page-locked for full speed): the
+    copies to and from the GPU are pipelined against the computation inside
+    the library.  Returns (out, lse, mask_bytes, counters) with out / lse on
+    the host; mask_bytes / counters are CUDA tensors (optional).  Returns
+    after the results are in host memory."""
+    lib = load()
+    if q.is_cuda or k.is_cuda or v.is_cuda:
+        raise LampError("lamp_attn_fwd_host takes host (CPU) tensors")
+    if q.dtype != k.dtype or q.dtype != v.dtype or q.dtype not in DT:
+        raise LampError("q, k, v must share a dtype in {bfloat16, float32}")
+    B, N, Hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, N, Hq, d), dtype=out_dtype or q.dtype).pin_memory()
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32).pin_memory()
+    sh = _host_shapes(q, k, v, out, window=window, scale=scale, force=force, stream=stream, device=device)
+    stats = LampStats()
+    stats.mask = mask_bytes.data_ptr() if mask_bytes is not None else None
+    stats.counters = counters.data_ptr() if counters is not None else None
+    buf_ptr, buf_bytes = (dev_buffer.data_ptr(), dev_buffer.numel() * dev_buffer.element_size()) \
+        if dev_buffer is not None else (None, 0)
+    code = lib.lamp_attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr() if lse is not None else None, ctypes.byref(sh),
+                                  MASK[mask], float(delta), float(tau), ctypes.byref(stats), buf_ptr, buf_bytes)
     _check(code)
     return out, lse, mask_bytes, counters
 
