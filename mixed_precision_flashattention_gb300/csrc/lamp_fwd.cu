@@ -456,16 +456,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       // below any delta > 0) and is not the maximum.  With delta = 0, or when
       // the tile can reach the 8-bit limit, all count.  A group of 8 logits
       // is looked at only if one of them is uncertain and its largest S8 is
-      // close enough to m: the exact values are at most S8 + |S8|/4 + 3G +
-      // 2^-8 (S8 the lower rounding), so below m - 6.75 nothing in it counts.
+      // close enough to m: with S8 the lower rounding, y - G is at most S8
+      // plus half a gap (<= |S8|/16 + 2^-10), and one more rounding of
+      // y + G adds at most |.|/16 + 2^-10, so the exact values are at most
+      // S8 + 0.13 |S8| + 2.2 G + 2^-8: below m - 6.75 nothing in it counts.
       uint32_t s8h[NC / 2];  // S8 pairs as f16x2 (exact)
       uint32_t gmx[NC / 8];  // per group of 8: max of the pairs (f16x2)
       uint32_t unc = 0u;     // logits to re-derive exactly
       {
         const float thr = (dcode == 0u || satp) ? -INFINITY : m - 6.75f;
         const __half2 lthr = __half2half2(__float2half_rd(thr));
-        const float c = thr - 3.0f * G - 0x1p-8f;
-        const __half2 sthr = __half2half2(__float2half_rd(c >= 0.0f ? 0.79f * c : 1.34f * c));
+        const float c = thr - 2.2f * G - 0x1p-8f;  // S8 + 0.13 |S8| > c  <=>  S8 > c / 1.13 or c / 0.87
+        const __half2 sthr = __half2half2(__float2half_rd(c >= 0.0f ? 0.884f * c : 1.15f * c));
         const float2 gm = make_float2(-G, -G), gp = make_float2(G, G);
 #pragma unroll
         for (int g4 = 0; g4 < NC / 8; ++g4) {  // 4 pairs at a time, one branch
@@ -509,13 +511,19 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           const long long acc = exact_dot<D>(sQ8, sK8, rw * 32 + src, col0 + cb, lane);
           if (lane == src) {
             const uint32_t hv = e4m3_f16_of_scaled(acc, p.sig_m, p.sig_e);
-            // replace half (cb & 1) of pair cb >> 1 (bit tests, no indexed access)
-            const uint32_t hit = 1u << cb;
-#pragma unroll
-            for (int i = 0; i < NC / 2; ++i) {
-              const uint32_t keep = (((hit >> (2 * i)) & 1u) ? 0xFFFF0000u : 0xFFFFFFFFu) &
-                                    (((hit >> (2 * i + 1)) & 1u) ? 0x0000FFFFu : 0xFFFFFFFFu);
-              s8h[i] = (s8h[i] & keep) | ((hv * 0x00010001u) & ~keep);
+            // replace half (cb & 1) of pair cb >> 1: a switch with constant
+            // indices keeps s8h in registers
+            static_assert(NC == 32, "the switch below lists 16 pairs");
+            const uint32_t keep = (cb & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+            const uint32_t put = (hv * 0x00010001u) & ~keep;
+            switch (cb >> 1) {
+#define LAMP_FIX_CASE(i) case i: s8h[i] = (s8h[i] & keep) | put; break;
+              LAMP_FIX_CASE(0) LAMP_FIX_CASE(1) LAMP_FIX_CASE(2) LAMP_FIX_CASE(3)
+              LAMP_FIX_CASE(4) LAMP_FIX_CASE(5) LAMP_FIX_CASE(6) LAMP_FIX_CASE(7)
+              LAMP_FIX_CASE(8) LAMP_FIX_CASE(9) LAMP_FIX_CASE(10) LAMP_FIX_CASE(11)
+              LAMP_FIX_CASE(12) LAMP_FIX_CASE(13) LAMP_FIX_CASE(14) LAMP_FIX_CASE(15)
+#undef LAMP_FIX_CASE
+              default: break;
             }
             unc &= unc - 1u;
           }
