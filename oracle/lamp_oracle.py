@@ -247,3 +247,97 @@ def flops(n, d, B, Hq, mask, window=0):
     else:
         pairs = int(np.minimum(rows + 1, window).sum())
     return 4.0 * d * B * Hq * pairs
+
+
+# ---------------------------------------------------------------- tau sweep
+# Figures 1-3 and 8 sweep tau at fixed delta.  The running max (R3), the 8-bit
+# exponentials (R4) and stage 1 (R6) do not depend on tau, and a sub-block is
+# flagged at tau iff its stage-1 entries reach half-ulp8(S8) >= tau.  So one
+# pass can record, per sub-block, the largest half-ulp8 among its stage-1
+# entries; the flag for any tau follows from it.  Record of a tile (uint32):
+# bits 0-3 visible sub-blocks, bits 4-7 stage 1, bits 8+4s..11+4s the code of
+# sub-block s: log2 of that largest half-ulp + 11 (1..15), 0 if none.
+
+def _sweep_block(q_rows, k_h, rows, n, sigma, mask, window, delta):
+    nI = q_rows.shape[0]
+    T = (n + TILE - 1) // TILE
+    A = e4m3_round(q_rows) @ e4m3_round(k_h).T  # R2
+    S8 = e4m3_round(A * sigma)
+    m = np.full((nI, TILE), -np.inf)
+    rec = np.zeros((nI, T), dtype=np.int64)
+    for j in range(T):
+        c0, c1 = j * TILE, min((j + 1) * TILE, n)
+        cols = np.arange(c0, c0 + TILE)
+        vis = visibility(rows, cols, n, mask, window)
+        if not vis.any():
+            continue
+        s8 = np.full((nI, TILE, TILE), 0.0)
+        s8[:, :, : c1 - c0] = S8[:, :, c0:c1]
+        m_new = np.maximum(m, np.where(vis, s8, -np.inf).max(axis=-1))  # R3
+        with np.errstate(invalid="ignore"):
+            diff = np.where(vis, s8 - m_new[..., None], 0.0)
+        p8 = np.where(vis, exp8(e4m3_round(diff)), 0.0)  # R4
+        stage1_e = vis & (p8 >= delta)  # R6
+        hx = np.log2(half_ulp_e4m3(s8))  # -10 .. 4
+        code_e = np.where(stage1_e, hx + 11, 0).astype(np.int64)
+        shp = (nI, NSTRIP, STRIP, TILE)
+        svis = vis.reshape(shp).any(axis=(2, 3))
+        st1 = stage1_e.reshape(shp).any(axis=(2, 3))
+        code = code_e.reshape(shp).max(axis=(2, 3))
+        r = np.zeros(nI, dtype=np.int64)
+        for s in range(NSTRIP):
+            r |= svis[:, s].astype(np.int64) << s
+            r |= st1[:, s].astype(np.int64) << (4 + s)
+            r |= code[:, s] << (8 + 4 * s)
+        rec[:, j] = np.where(vis.any(axis=(1, 2)), r, 0)
+        m = m_new
+    return rec
+
+
+def tau_sweep_records(q, k, *, mask="causal", window=0, scale=None, delta=2.0 ** -8):
+    """Per-tile sweep records [B, Hq, T, T] (uint32, layout above) of the LAMP
+    emulation; q [B, N, Hq, d], k [B, N, Hkv, d] (values as given)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    B, n, Hq, d = q.shape
+    Hkv = k.shape[2]
+    sigma = (1.0 / np.sqrt(float(d))) if scale is None else float(scale)
+    T = (n + TILE - 1) // TILE
+    grp = Hq // Hkv
+    rec = np.zeros((B, Hq, T, T), dtype=np.uint32)
+    idx = np.arange(T)
+    rows = idx[:, None] * TILE + np.arange(TILE)[None, :]
+    ok = rows < n
+    for b in range(B):
+        for h in range(Hq):
+            q_rows = np.zeros((T, TILE, d))
+            q_rows[ok] = q[b, rows[ok], h, :]
+            rec[b, h] = _sweep_block(q_rows, k[b, :, h // grp, :], rows, n, sigma,
+                                     mask, window, delta).astype(np.uint32)
+    return rec
+
+
+def tau_code(tau):
+    """Smallest sub-block code that is flagged at tau (16: none)."""
+    if not tau > 2.0 ** -10:
+        return 1
+    c = int(np.ceil(np.log2(tau))) + 11
+    return min(c, 16)
+
+
+def sweep_histograms(rec, taus):
+    """[len(taus), 4] counts per tau: visited tiles, tiles with 0, 1 and 2+
+    flagged sub-blocks (the 0 / 1 / 2+ buckets of Tables 1-6)."""
+    rec = np.asarray(rec, dtype=np.int64).ravel()
+    visited = (rec & 0xF) != 0
+    out = np.zeros((len(taus), 4), dtype=np.int64)
+    for i, tau in enumerate(taus):
+        tc = tau_code(tau)
+        nfl = np.zeros(rec.shape, dtype=np.int64)
+        for s in range(NSTRIP):
+            st1 = (rec >> (4 + s)) & 1
+            code = (rec >> (8 + 4 * s)) & 0xF
+            nfl += ((st1 == 1) & (code >= tc)).astype(np.int64)
+        out[i] = [visited.sum(), (visited & (nfl == 0)).sum(), (visited & (nfl == 1)).sum(),
+                  (visited & (nfl >= 2)).sum()]
+    return out
