@@ -208,6 +208,34 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out,
  * shapes. */
 size_t lamp_attn_host_buffer_bytes(const lamp_shapes* shapes);
 
+/*
+ * lamp_attn_tau_sweep: the histograms of 16-bit sub-blocks per tile (the
+ * 0 / 1 / 2+ buckets of Tables 1-6) for up to 8 values of tau at once,
+ * from one pass -- the tau sweeps of Figures 1-3 and 8.  The running max,
+ * the 8-bit exponentials and the first stage do not depend on tau, and a
+ * sub-block is flagged at tau iff one of its stage-1 entries has
+ * half-ulp8(S8) >= tau, so the pass records per sub-block the largest such
+ * half-ulp; no 16-bit recompute, no P.V and no output are computed.  The
+ * histograms equal the counters LAMP_CNT_TILES / HIST0 / HIST1 / HIST2 of
+ * lamp_attn_fwd at each tau (force off).
+ *   q, k      DEVICE, as for lamp_attn_fwd (shapes: v_stride, o_stride and
+ *             out_dtype are not used).
+ *   taus      HOST float[ntau], 0 <= ntau <= 8.
+ *   records   DEVICE uint32 [B][Hq][T][T], T = ceil(seqlen/64), written in
+ *             full: bits 0-3 visible sub-blocks, 4-7 stage-1 sub-blocks,
+ *             8+4s..11+4s the code of sub-block s = log2(largest stage-1
+ *             half-ulp8) + 11 (1..15), 0 if none; 0 for tiles not visited.
+ *   hist      DEVICE uint64 [ntau][4]: visited tiles, tiles with 0, 1, 2+
+ *             flagged sub-blocks at taus[i] (zeroed, then written).
+ *   stats     optional; counters as for lamp_attn_fwd except the flag-based
+ *             ones (HIST0..2, FLAGGED, RECOMP_STEPS, SPEC_WASTE stay 0);
+ *             stats->mask is not written.
+ * Asynchronous on shapes->stream; errors as lamp_attn_fwd.
+ */
+int lamp_attn_tau_sweep(const void* q, const void* k, const lamp_shapes* shapes,
+                        int mask_kind, float delta, const float* taus, int ntau,
+                        uint32_t* records, uint64_t* hist, lamp_stats* stats);
+
 /* Static, human-readable text for a lamp_status value. */
 const char* lamp_strerror(int status);
 

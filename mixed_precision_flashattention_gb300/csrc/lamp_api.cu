@@ -14,7 +14,9 @@
 
 namespace lamp {
 cudaError_t launch_prep(const PrepParams& p, int d, cudaStream_t st);
-cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st);
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st, bool sweep);
+cudaError_t launch_sweep_hist(const uint32_t* rec, long long n, const SweepCodes& tcode, int ntau,
+                              unsigned long long* hist, cudaStream_t st);
 
 // Exactness guard of the 8-bit logits.  The FP8 tensor-core chain for a
 // head dimension d is d/32 instructions of K = 32; measured on GB300, each
@@ -148,9 +150,18 @@ size_t lamp_attn_workspace_bytes(const lamp_shapes* shapes) {
   return ws_layout(*shapes).total;
 }
 
-int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const lamp_shapes* shapes,
-                  int mask_kind, float delta, float tau, lamp_stats* stats) {
-  if (!q || !k || !v || !out || !shapes_ok(shapes)) return LAMP_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace lamp {
+namespace {
+
+// The forward pass (sweep = false) or the tau-sweep pass (sweep = true: no v,
+// no out / lse; `records` receives the tile records).
+int run_pass(const void* q, const void* k, const void* v, void* out, float* lse, const lamp_shapes* shapes,
+             int mask_kind, float delta, float tau, lamp_stats* stats, uint32_t* records, bool sweep) {
+  if (!q || !k || !shapes_ok(shapes)) return LAMP_ERR_INVALID_ARG;
+  if (!sweep && (!v || !out)) return LAMP_ERR_INVALID_ARG;
+  if (sweep && !records) return LAMP_ERR_INVALID_ARG;
   const lamp_shapes& s = *shapes;
   const int D = s.head_dim;
   if (D != 64 && D != 128 && D != 256) return LAMP_ERR_UNSUPPORTED;
@@ -160,12 +171,12 @@ int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out, float*
   const int es_in = s.in_dtype == LAMP_DT_FP32 ? 4 : 2;
   const int es_out = s.out_dtype == LAMP_DT_FP32 ? 4 : 2;
   const int64_t* strides[4] = {s.q_stride, s.k_stride, s.v_stride, s.o_stride};
-  for (int t = 0; t < 4; ++t)
+  for (int t = 0; t < (sweep ? 2 : 4); ++t)
     for (int i = 0; i < 3; ++i) {
       const int es = t == 3 ? es_out : es_in;
       if (strides[t][i] < D || (strides[t][i] * es) % 16) return LAMP_ERR_INVALID_ARG;
     }
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || ((uintptr_t)lse & 3u))
+  if (!aligned16(q) || !aligned16(k) || (!sweep && (!aligned16(v) || !aligned16(out))) || ((uintptr_t)lse & 3u))
     return LAMP_ERR_INVALID_ARG;
   int st = device_check();
   if (st != LAMP_OK) return st;
@@ -190,14 +201,16 @@ int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out, float*
   if (stats && stats->counters &&
       cudaMemsetAsync(stats->counters, 0, LAMP_NUM_COUNTERS * sizeof(uint64_t), stream) != cudaSuccess)
     return fail(LAMP_ERR_CUDA);
-  if (stats && stats->mask &&
+  if (!sweep && stats && stats->mask &&
       cudaMemsetAsync(stats->mask, 0, (size_t)B * Hq * T * T, stream) != cudaSuccess)
+    return fail(LAMP_ERR_CUDA);
+  if (sweep && cudaMemsetAsync(records, 0, (size_t)B * Hq * T * T * 4, stream) != cudaSuccess)
     return fail(LAMP_ERR_CUDA);
   // norms of the key tiles and the abort word are contiguous: one memset
   if (cudaMemsetAsync(ws + w.nk, 0, w.total - w.nk, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
 
   PrepParams pp{};
-  pp.q = q; pp.k = k; pp.v = v;
+  pp.q = q; pp.k = k; pp.v = sweep ? nullptr : v;  // the sweep needs no V
   for (int i = 0; i < 3; ++i) { pp.qs[i] = s.q_stride[i]; pp.ks[i] = s.k_stride[i]; pp.vs[i] = s.v_stride[i]; }
   pp.q8 = ws + w.q8; pp.k8 = ws + w.k8; pp.v16 = ws + w.v16;
   pp.q16 = s.in_dtype == LAMP_DT_FP32 ? (void*)(ws + w.q16) : nullptr;
@@ -219,8 +232,9 @@ int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out, float*
   bool ok = true;
   ok &= make_map(&fp.tmQ8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ws + w.q8, D, N, Hq, B, D, NDq, NDq * Hq, f8box, kBM, f8swz);
   ok &= make_map(&fp.tmK8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ws + w.k8, D, N, Hkv, B, D, NDk, NDk * Hkv, f8box, kBN, f8swz);
-  ok &= make_map(&fp.tmV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws + w.v16, D, N, Hkv, B, D, NDk, NDk * Hkv, 64, kBN,
-                 CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!sweep)
+    ok &= make_map(&fp.tmV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws + w.v16, D, N, Hkv, B, D, NDk, NDk * Hkv, 64, kBN,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
   if (s.in_dtype == LAMP_DT_FP32) {
     ok &= make_map(&fp.tmQ16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + w.q16, D, N, Hq, B, D, NDq, NDq * Hq, 64, kBM,
                    CU_TENSOR_MAP_SWIZZLE_128B);
@@ -237,7 +251,8 @@ int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out, float*
   const double sigma_d = s.softmax_scale > 0.0f ? (double)s.softmax_scale : 1.0 / std::sqrt((double)D);
   fp.out = out;
   fp.lse = lse;
-  fp.mask = stats ? stats->mask : nullptr;
+  fp.mask = (stats && !sweep) ? stats->mask : nullptr;
+  fp.records = records;
   fp.counters = stats ? (unsigned long long*)stats->counters : nullptr;
   fp.nq = (const float*)(ws + w.nq);
   fp.nkmax = (const float*)(ws + w.nk);
@@ -263,9 +278,38 @@ int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out, float*
   fp.timeout_ns = kTimeoutNs;
   if (const char* e = getenv("LAMP_WAIT_TIMEOUT_NS")) fp.timeout_ns = strtoull(e, nullptr, 10);
   fp.gabort = (unsigned int*)(ws + w.abort);
-  if (launch_fwd(fp, D, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
+  if (launch_fwd(fp, D, stream, sweep) != cudaSuccess) return fail(LAMP_ERR_CUDA);
   if (!mark(2)) return fail(LAMP_ERR_CUDA);
   if (own_ws && cudaFreeAsync(ws, stream) != cudaSuccess) return LAMP_ERR_CUDA;
+  return LAMP_OK;
+}
+
+}  // namespace
+}  // namespace lamp
+
+extern "C" {
+
+int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const lamp_shapes* shapes,
+                  int mask_kind, float delta, float tau, lamp_stats* stats) {
+  return run_pass(q, k, v, out, lse, shapes, mask_kind, delta, tau, stats, nullptr, false);
+}
+
+int lamp_attn_tau_sweep(const void* q, const void* k, const lamp_shapes* shapes, int mask_kind, float delta,
+                        const float* taus, int ntau, uint32_t* records, uint64_t* hist, lamp_stats* stats) {
+  if (ntau < 0 || ntau > kMaxSweepTaus || (ntau > 0 && (!taus || !hist))) return LAMP_ERR_INVALID_ARG;
+  SweepCodes tc{};
+  for (int i = 0; i < ntau; ++i) {
+    if (std::isnan(taus[i])) return LAMP_ERR_INVALID_ARG;
+    tc.v[i] = host_tau_code(taus[i]);
+  }
+  const int r = run_pass(q, k, nullptr, nullptr, nullptr, shapes, mask_kind, delta, 0.5f, stats, records, true);
+  if (r != LAMP_OK || ntau == 0) return r;
+  const lamp_shapes& s = *shapes;
+  cudaStream_t stream = (cudaStream_t)s.stream;
+  const long long T = (s.seqlen + kBN - 1) / kBN;
+  const long long n = (long long)s.batch * s.heads_q * T * T;
+  if (cudaMemsetAsync(hist, 0, (size_t)ntau * 4 * sizeof(uint64_t), stream) != cudaSuccess) return LAMP_ERR_CUDA;
+  if (launch_sweep_hist(records, n, tc, ntau, (unsigned long long*)hist, stream) != cudaSuccess) return LAMP_ERR_CUDA;
   return LAMP_OK;
 }
 

@@ -13,6 +13,10 @@ constexpr int kBM = 128;        // query rows per CTA (one TMEM lane per row)
 constexpr int kBN = 64;         // keys per step = one 64-key tile of the method
 constexpr int kNC = 32;             // logits per softmax thread per step
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxSweepTaus = 8;    // tau values per sweep call
+struct SweepCodes {
+  int v[kMaxSweepTaus];  // per tau: the smallest sub-block code flagged at it
+};
 
 // Kernel parameters (passed by value as a __grid_constant__).
 struct FwdParams {
@@ -21,6 +25,7 @@ struct FwdParams {
   float* lse;
   uint8_t* mask;
   unsigned long long* counters;
+  uint32_t* records;   // tau-sweep pass: [B, Hq, T, T] tile records
   const float* nq;     // [B, Hq, N]   ||fl8(q_r)||_2 (upper bound)
   const float* nkmax;  // [B, Hkv, T]  max over the tile of ||fl8(k_c)||_2
   long long o_stride[3];
@@ -173,6 +178,16 @@ inline float host_tau_abs(float tau) {
     if (half >= tau) return e == -6 ? 0x1p-9f : ldexpf(1.0f, e);
   }
   return __builtin_inff();
+}
+
+// tau-sweep records store, per sub-block, log2(largest stage-1 half-ulp8)
+// + 11 (1..15; half-ulps of E4M3 run from 2^-10 to 2^4); the sub-block is
+// flagged at tau iff its code is >= this (16: never).
+inline int host_tau_code(float tau) {
+  if (!(tau > 0x1p-10f)) return 1;
+  for (int c = 2; c <= 15; ++c)
+    if (ldexpf(1.0f, c - 11) >= tau) return c;
+  return 16;
 }
 
 // Code of the smallest non-negative E4M3 value >= delta (0xFF if none),

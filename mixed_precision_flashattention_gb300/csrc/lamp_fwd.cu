@@ -201,7 +201,12 @@ __device__ __forceinline__ long long exact_dot(const uint8_t* sQ8, const uint8_t
 
 namespace lamp {
 
-template <int D>
+// kSweep: the tau-sweep pass (Figures 1-3 and 8 sweep tau at fixed delta):
+// only the 8-bit logits, the running max and the detector run, and each
+// visited tile gets a record with, per sub-block, the largest half-ulp8 of
+// its stage-1 entries (the flag at any tau follows from it); no 16-bit
+// recompute, no P.V, no output.
+template <int D, bool kSweep>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -270,17 +275,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     // ------------------------------------------------------------ producer
     if (lane == 0 && J1 > J0) {
       prefetch_tmap(&p.tmQ8);
-      prefetch_tmap(&p.tmQ16);
       prefetch_tmap(&p.tmK8);
-      prefetch_tmap(&p.tmK16);
-      prefetch_tmap(&p.tmV);
-      mbar_expect_tx(bar(M_Q_FULL), C::NT * C::QT_BYTES);
+      if (!kSweep) {  // the sweep pass has no V map
+        prefetch_tmap(&p.tmQ16);
+        prefetch_tmap(&p.tmK16);
+        prefetch_tmap(&p.tmV);
+      }
+      mbar_expect_tx(bar(M_Q_FULL), C::NT * (kSweep ? C::Q8_BYTES : C::QT_BYTES));
       for (int t = 0; t < C::NT; ++t) {
         const uint32_t qd = sbase + C::OFF_Q + t * C::QT_BYTES;
         for (int c = 0; c < D / C::F8_SWZ_ROW; ++c)
           tma_load_4d(qd + c * kBM * 128, &p.tmQ8, bar(M_Q_FULL), c * C::F8_SWZ_ROW, q0 + t * kBM, h, b);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(qd + C::Q8_BYTES + c * kBM * 128, &p.tmQ16, bar(M_Q_FULL), c * 64, q0 + t * kBM, h, b);
+        if (!kSweep)
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(qd + C::Q8_BYTES + c * kBM * 128, &p.tmQ16, bar(M_Q_FULL), c * 64, q0 + t * kBM, h, b);
       }
       int uses0 = 0, uses1 = 0;
       uint32_t rel = 0u;  // releases waited for so far, one bit of parity per (tile, stage)
@@ -301,13 +309,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         const int key0 = j * kBN;
         const uint32_t st = sbase + C::OFF_ST + s * C::STAGE_BYTES;
         const uint32_t fb = bar(M_KV_FULL + 8 * s);
-        mbar_expect_tx(fb, C::STAGE_BYTES);
+        mbar_expect_tx(fb, kSweep ? C::K8_BYTES : C::STAGE_BYTES);
         for (int c = 0; c < D / C::F8_SWZ_ROW; ++c)
           tma_load_4d(st + c * kBN * 128, &p.tmK8, fb, c * C::F8_SWZ_ROW, key0, g, b);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(st + C::K8_BYTES + c * kBN * 128, &p.tmK16, fb, c * 64, key0, g, b);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(st + C::K8_BYTES + C::K16_BYTES + c * kBN * 128, &p.tmV, fb, c * 64, key0, g, b);
+        if (!kSweep) {
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(st + C::K8_BYTES + c * kBN * 128, &p.tmK16, fb, c * 64, key0, g, b);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(st + C::K8_BYTES + C::K16_BYTES + c * kBN * 128, &p.tmV, fb, c * 64, key0, g, b);
+        }
         if (s) uses1 = u + 1; else uses0 = u + 1;
       }
       if (*cx.abort) {  // let every load in flight land before the CTA exits
@@ -338,6 +348,27 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         mma_commit(bar(M_KV_EMPTY + 16 * stage_of(jlo + i) + 8 * t));
       };
       bool ok = wait_bar(cx, bar(M_Q_FULL), 0);
+      if (kSweep) {
+        // QK8 only.  A key's stage is handed back once the softmax has
+        // published the step (DEC): its exact re-derivations read K8 from
+        // the stage until then.
+        for (int i = 0; ok && i < n; ++i) {
+          const int j = jlo + i;
+          if (i > 0) {
+            ok = wait_bar(cx, bar(M_DEC + 8 * t), (i - 1) & 1);
+            if (!ok) break;
+            mbar_arrive(bar(M_KV_EMPTY + 16 * stage_of(j - 1) + 8 * t));
+          }
+          ok = wait_bar(cx, bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          Mma<D>::qk8(tm + C::S8_OFF, qbase, kv(j));
+          mma_commit(bar(M_S_FULL + 8 * t));
+        }
+        if (ok && wait_bar(cx, bar(M_DEC + 8 * t), (n - 1) & 1))
+          mbar_arrive(bar(M_KV_EMPTY + 16 * stage_of(jlo + n - 1) + 8 * t));
+        ok = false;  // nothing more to issue
+      }
       // with a single K/V stage, key i can only land after P.V(i-1) has
       // released the stage, so P.V(i-1) goes first
       constexpr bool kPvFirst = C::NS == 1;
@@ -566,7 +597,41 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         st1 = tab[cvt_e4m3x2(0.0f, m_tile - m_new) & 0xFFu] >= dcode;
         flg = st1 && (T <= 0.0f || m_tile >= T);
       }
-      const bool maybe_neg = rowvis && st1 && !flg && T > 0.0f &&
+      uint32_t scode = 0u;  // sweep pass: code of this row's largest stage-1 half-ulp8
+      if constexpr (kSweep) {
+        // the stage-1 entries are the visible S8 >= some threshold (P8 is
+        // monotone in S8): the largest |S8| among them is the tile maximum,
+        // or the smallest of them when it is negative
+        flg = false;
+        float A = fabsf(m_tile);
+        const bool scan = rowvis && st1 && (m_new <= 0.0f || tab[cvt_e4m3x2(0.0f, -m_new) & 0xFFu] >= dcode);
+        if (__any_sync(0xffffffffu, scan)) {  // same outcome in both halves
+          __half2 mn = __float2half2_rn(0.0f);
+          if (scan) {
+            const __half2 mh = __float2half2_rn(m_new);
+#pragma unroll
+            for (int i = 0; i < NC / 2; ++i) {
+              const __half2 sv = as_half2(s8h[i]);
+              const uint32_t x8 = cvt_e4m3x2_f16x2(__hsub2(sv, mh));
+              const bool q0 = ((vm >> (2 * i)) & 1u) && tab[x8 & 0xFFu] >= dcode;
+              const bool q1 = ((vm >> (2 * i + 1)) & 1u) && tab[x8 >> 8] >= dcode;
+              mn = __hmin2(mn, __halves2half2(q0 ? __low2half(sv) : __float2half(0.0f),
+                                              q1 ? __high2half(sv) : __float2half(0.0f)));
+            }
+          }
+          const float mine = fminf(__low2float(mn), __high2float(mn));
+          xb[hf * kBM + t] = __float_as_uint(mine);
+          bar_sync(pair_bar, 64);
+          if (scan) A = fmaxf(A, -fminf(mine, __uint_as_float(xb[(1 - hf) * kBM + t])));
+        }
+        if (rowvis && st1) {
+          const int e = (int)((__float_as_uint(A) >> 23) & 0xFFu) - 127;  // floor(log2 A), A >= 2^-6
+          scode = (uint32_t)((A < 0x1p-6f ? -10 : e - 4) + 11);           // half-ulp8 = 2^(code - 11)
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) scode = max(scode, __shfl_xor_sync(0xffffffffu, scode, o));
+      }
+      const bool maybe_neg = !kSweep && rowvis && st1 && !flg && T > 0.0f &&
                              tab[cvt_e4m3x2(0.0f, -T - m_new) & 0xFFu] >= dcode;
       if (__any_sync(0xffffffffu, maybe_neg)) {  // same outcome in both halves
         uint32_t mine = 0u;
@@ -602,10 +667,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       uint8_t* sflag = misc + M_SFLAG + 32 * tt + 16 * (jj & 1);
       if (hf == 0) {  // the owner of the 64-row query tile needs the sub-block bits
         const unsigned b1 = __ballot_sync(0xffffffffu, st1);
+        const uint32_t scode_hi = kSweep ? __shfl_sync(0xffffffffu, scode, 16) : 0u;  // second sub-block's code
         if (lane == 0)
           *(volatile uint32_t*)(sflag + 4 * rw) =
               ((bf & 0xFFFFu) != 0u) | (((bf >> 16) != 0u) << 1) | (((b1 & 0xFFFFu) != 0u) << 2) |
-              (((b1 >> 16) != 0u) << 3) | (((bv & 0xFFFFu) != 0u) << 4) | (((bv >> 16) != 0u) << 5);
+              (((b1 >> 16) != 0u) << 3) | (((bv & 0xFFFFu) != 0u) << 4) | (((bv >> 16) != 0u) << 5) |
+              (scode << 8) | (scode_hi << 12);
       }
       // (after a failed wait a thread keeps stepping with its waits skipped,
       // so every thread of the tile reaches every barrier)
@@ -625,15 +692,23 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         const uint32_t vs4 = ((w0 >> 4) & 3u) | (((w1 >> 4) & 3u) << 2);
         if (vs4) {
           const int nf = __popc(fl4);
-          if (nf == 0) ++c_h0; else if (nf == 1) ++c_h1; else ++c_h2;
           c_strips += __popc(vs4);
           c_st1 += __popc(st4 & vs4);
-          c_fl += nf;
-          if (p.mask && qtile < p.T)
-            p.mask[(((size_t)b * p.Hq + h) * p.T + qtile) * p.T + jt] = (uint8_t)(fl4 | (st4 << 4));
+          if constexpr (kSweep) {
+            ++c_h0;  // counts visited tiles only (no flags in this pass)
+            const uint32_t codes = ((w0 >> 8) & 0xFFu) | (((w1 >> 8) & 0xFFu) << 8);
+            if (qtile < p.T)
+              p.records[(((size_t)b * p.Hq + h) * p.T + qtile) * p.T + jt] = vs4 | (st4 << 4) | (codes << 8);
+          } else {
+            if (nf == 0) ++c_h0; else if (nf == 1) ++c_h1; else ++c_h2;
+            c_fl += nf;
+            if (p.mask && qtile < p.T)
+              p.mask[(((size_t)b * p.Hq + h) * p.T + qtile) * p.T + jt] = (uint8_t)(fl4 | (st4 << 4));
+          }
         }
       }
 
+      if constexpr (!kSweep) {
       // ---- x8 = fl8(S8 - m) (fp16 difference, then one E4M3 rounding: equal
       // to the single rounding for E4M3 operands), P8 from the exp8 table;
       // rows of flagged sub-blocks take P16 below instead
@@ -720,6 +795,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         tc_fence_before();
         mbar_arrive(bar(M_P_FULL + 8 * tt));
       }
+      }  // !kSweep
       m = m_new;
       if (jj == nsteps - 1) done_ok = !fail;
     }
@@ -728,6 +804,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     xch[hf * kBM + t] = l;
     bar_sync(pair_bar, 64);
     const float lrow = l + xch[(1 - hf) * kBM + t];
+    if (kSweep) done_ok = false;  // no output
     if (done_ok) done_ok = wait_bar_warp(cx, bar(M_PV_DONE + 8 * tt), (nsteps - 1) & 1);
     if (done_ok) {
       tc_fence_after();
@@ -768,18 +845,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       const uint32_t c_tiles = c_h0 + c_h1 + c_h2;
       if (lane == 0 && hf == 0 && (rw & 1) == 0 && c_tiles) {
         atomicAdd(&p.counters[0], (u64)c_tiles);
-        atomicAdd(&p.counters[1], (u64)c_h0);
-        atomicAdd(&p.counters[2], (u64)c_h1);
-        atomicAdd(&p.counters[3], (u64)c_h2);
+        if (!kSweep) {
+          atomicAdd(&p.counters[1], (u64)c_h0);
+          atomicAdd(&p.counters[2], (u64)c_h1);
+          atomicAdd(&p.counters[3], (u64)c_h2);
+          atomicAdd(&p.counters[6], (u64)c_fl);
+        }
         atomicAdd(&p.counters[4], (u64)c_strips);
         atomicAdd(&p.counters[5], (u64)c_st1);
-        atomicAdd(&p.counters[6], (u64)c_fl);
       }
       c_sat = __reduce_add_sync(0xffffffffu, c_sat);
       if (lane == 0 && c_sat) atomicAdd(&p.counters[7], (u64)c_sat);
       if (lane == 0 && c_fix) atomicAdd(&p.counters[8], (u64)c_fix);
-      if (t == 0 && hf == 0 && c_rec) atomicAdd(&p.counters[10], (u64)c_rec);
-      if (t == 0 && hf == 0 && c_spec) atomicAdd(&p.counters[11], (u64)c_spec);
+      if (!kSweep && t == 0 && hf == 0 && c_rec) atomicAdd(&p.counters[10], (u64)c_rec);
+      if (!kSweep && t == 0 && hf == 0 && c_spec) atomicAdd(&p.counters[11], (u64)c_spec);
     }
   }
 
@@ -790,25 +869,74 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
 }
 
 // ---------------------------------------------------------------- launcher
-template <int D>
+template <int D, bool kSweep>
 static cudaError_t launch_fwd_d(FwdParams p, cudaStream_t st) {
   using C = Cfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(lamp_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e =
+      cudaFuncSetAttribute(lamp_fwd_kernel<D, kSweep>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   p.nqb = (p.N + kBM * C::NT - 1) / (kBM * C::NT);
   const unsigned grid = (unsigned)p.nqb * (unsigned)p.B * (unsigned)p.Hq;
   if (grid == 0) return cudaSuccess;
-  lamp_fwd_kernel<D><<<grid, C::THREADS, C::SMEM, st>>>(p);
+  lamp_fwd_kernel<D, kSweep><<<grid, C::THREADS, C::SMEM, st>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st) {
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st, bool sweep) {
   switch (d) {
-    case 64: return launch_fwd_d<64>(p, st);
-    case 128: return launch_fwd_d<128>(p, st);
-    case 256: return launch_fwd_d<256>(p, st);
+    case 64: return sweep ? launch_fwd_d<64, true>(p, st) : launch_fwd_d<64, false>(p, st);
+    case 128: return sweep ? launch_fwd_d<128, true>(p, st) : launch_fwd_d<128, false>(p, st);
+    case 256: return sweep ? launch_fwd_d<256, true>(p, st) : launch_fwd_d<256, false>(p, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// Histograms of the sweep records for several tau (as sub-block codes):
+// hist[4 i .. 4 i + 3] += visited tiles, tiles with 0, 1, 2+ flagged
+// sub-blocks at tau i.
+__global__ void lamp_sweep_hist_kernel(const uint32_t* __restrict__ rec, long long n, const SweepCodes tcode,
+                                       int ntau, unsigned long long* hist) {
+  __shared__ unsigned long long acc[kMaxSweepTaus * 4];
+  for (int i = threadIdx.x; i < ntau * 4; i += blockDim.x) acc[i] = 0ull;
+  __syncthreads();
+  uint32_t tot = 0u, h0[kMaxSweepTaus], h1[kMaxSweepTaus], h2[kMaxSweepTaus];
+#pragma unroll
+  for (int t = 0; t < kMaxSweepTaus; ++t) h0[t] = h1[t] = h2[t] = 0u;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const uint32_t r = rec[i];
+    if (!(r & 0xFu)) continue;
+    ++tot;
+#pragma unroll
+    for (int t = 0; t < kMaxSweepTaus; ++t) {
+      const int tc = t < ntau ? tcode.v[t] : 16;
+      int nf = 0;
+#pragma unroll
+      for (int sb = 0; sb < 4; ++sb) nf += (((r >> (4 + sb)) & 1u) && (int)((r >> (8 + 4 * sb)) & 0xFu) >= tc) ? 1 : 0;
+      h0[t] += nf == 0;
+      h1[t] += nf == 1;
+      h2[t] += nf >= 2;
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kMaxSweepTaus; ++t) {
+    if (t >= ntau) break;
+    if (tot) atomicAdd(&acc[4 * t], (unsigned long long)tot);
+    if (h0[t]) atomicAdd(&acc[4 * t + 1], (unsigned long long)h0[t]);
+    if (h1[t]) atomicAdd(&acc[4 * t + 2], (unsigned long long)h1[t]);
+    if (h2[t]) atomicAdd(&acc[4 * t + 3], (unsigned long long)h2[t]);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < ntau * 4; i += blockDim.x)
+    if (acc[i]) atomicAdd(&hist[i], acc[i]);
+}
+
+cudaError_t launch_sweep_hist(const uint32_t* rec, long long n, const SweepCodes& tcode, int ntau,
+                              unsigned long long* hist, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 1216) blocks = 1216;  // 8 per SM
+  lamp_sweep_hist_kernel<<<(unsigned)blocks, 256, 0, st>>>(rec, n, tcode, ntau, hist);
+  return cudaGetLastError();
 }
 
 }  // namespace lamp

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(256) lamp_prep_kernel(const PrepParams p) {
       // non-negative floats order like their bit patterns
       atomicMax((int*)&p.nkmax[((size_t)b * p.Hkv + g) * p.T + n / kBN], __float_as_int(nk));
     }
-  } else if (row < nQ + 2 * nK) {
+  } else if (p.v && row < nQ + 2 * nK) {  // (no V rows in the sweep pass: the grid's last block may overhang)
     const long long r = row - nQ - nK;
     const int g = (int)(r % p.Hkv);
     const long long bn = r / p.Hkv;
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(256) lamp_prep_kernel(const PrepParams p) {
 
 template <int D>
 static cudaError_t launch_prep_d(const PrepParams& p, cudaStream_t st) {
-  const long long rows = (long long)p.B * p.N * (p.Hq + 2LL * p.Hkv);
+  const long long rows = (long long)p.B * p.N * (p.Hq + (p.v ? 2LL : 1LL) * p.Hkv);  // no V rows without v
   const long long blocks = (rows + 7) / 8;
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;

@@ -25,7 +25,7 @@ COUNTER_NAMES = ["tiles", "hist0", "hist1", "hist2p", "strips", "stage1", "flagg
                  "s8_saturated", "fixups", "status", "recompute_steps", "spec_waste"]
 EXPORTS = ["lamp_attn_fwd", "lamp_attn_fwd_noalloc", "lamp_attn_workspace_bytes", "lamp_strerror",
            "lamp_version", "lamp_exp8_table", "lamp_selftest", "lamp_attn_fwd_host",
-           "lamp_attn_host_buffer_bytes"]
+           "lamp_attn_host_buffer_bytes", "lamp_attn_tau_sweep"]
 
 
 class LampShapes(ctypes.Structure):
@@ -84,6 +84,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.lamp_attn_fwd_host.argtypes = lib.lamp_attn_fwd.argtypes + [ctypes.c_void_p, ctypes.c_size_t]
     lib.lamp_attn_host_buffer_bytes.restype = ctypes.c_size_t
     lib.lamp_attn_host_buffer_bytes.argtypes = [ctypes.POINTER(LampShapes)]
+    lib.lamp_attn_tau_sweep.restype = ctypes.c_int
+    lib.lamp_attn_tau_sweep.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(LampShapes), ctypes.c_int,
+                                        ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.POINTER(LampStats)]
     lib.lamp_selftest.restype = ctypes.c_int
     lib.lamp_selftest.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_int, ctypes.c_void_p]
@@ -212,6 +216,35 @@ def lamp_attn_fwd_host(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0
                                   MASK[mask], float(delta), float(tau), ctypes.byref(stats), buf_ptr, buf_bytes)
     _check(code)
     return out, lse, mask_bytes, counters
+
+
+def lamp_tau_sweep(q, k, taus, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -8, records=None,
+                   counters=None, stream=None):
+    """Histograms of 16-bit sub-blocks per tile for up to 8 tau values from
+    one pass.  q [B, N, Hq, d], k [B, N, Hkv, d] CUDA tensors.  Returns
+    (hist [ntau, 4] int64 CUDA tensor: visited tiles, tiles with 0 / 1 / 2+
+    flagged sub-blocks; records [B, Hq, T, T] int32 CUDA tensor of the tile
+    records).  Asynchronous on ``stream``."""
+    lib = load()
+    if not (q.is_cuda and k.is_cuda):
+        raise LampError("q, k must be CUDA tensors")
+    if q.dtype != k.dtype or q.dtype not in DT:
+        raise LampError("q, k must share a dtype in {bfloat16, float32}")
+    taus = [float(t) for t in taus]
+    B, N, Hq, d = q.shape
+    T = (N + 63) // 64
+    if records is None:
+        records = torch.empty((B, Hq, T, T), dtype=torch.int32, device=q.device)
+    hist = torch.zeros((max(1, len(taus)), 4), dtype=torch.int64, device=q.device)
+    sh = make_shapes(q, k, k, q, window=window, scale=scale, stream=stream)
+    stats = LampStats()
+    stats.mask = None
+    stats.counters = counters.data_ptr() if counters is not None else None
+    tarr = (ctypes.c_float * max(1, len(taus)))(*taus)
+    code = lib.lamp_attn_tau_sweep(q.data_ptr(), k.data_ptr(), ctypes.byref(sh), MASK[mask], float(delta),
+                                   tarr, len(taus), records.data_ptr(), hist.data_ptr(), ctypes.byref(stats))
+    _check(code)
+    return hist[:len(taus)], records
 
 
 def new_stats(B, Hq, N, device="cuda"):
