@@ -72,7 +72,7 @@ def cpu_sample_tasks(w, q, k, v, delta, tau, wall_budget_s, ncores, seed=0):
     t_long = _oracle_task(probe)  # seconds for the longest query tile
     rng = np.random.default_rng(seed)
     picks, est = {}, 0.0
-    while est < wall_budget_s * ncores and sum(len(x) for x in picks.values()) < 4096:
+    while est < wall_budget_s * ncores and sum(len(x) for x in picks.values()) < 8192:
         b, h, i = int(rng.integers(w.batch)), int(rng.integers(w.heads_q)), int(rng.integers(T))
         if i in picks.get((b, h), ()):
             continue
@@ -304,6 +304,23 @@ def main():
     h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
     d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
 
+    # the tau sweep of the pages' figures (tau = 2^0 .. 2^-5 at this delta)
+    # from one detector-only pass, against six forward passes
+    sweep_taus = [2.0 ** -i for i in range(6)]
+    srec = torch.empty((B, Hq, (N + 63) // 64, (N + 63) // 64), dtype=torch.int32, device=dev)
+    sw_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(8)]
+    for i in range(3 + len(sw_ev)):
+        flush.zero_()
+        if i >= 3:
+            sw_ev[i - 3][0].record()
+        sw_hist, _ = lamp.lamp_tau_sweep(qd, kd, sweep_taus, mask=w.mask, window=w.window, delta=args.delta,
+                                         records=srec)
+        if i >= 3:
+            sw_ev[i - 3][1].record()
+    torch.cuda.synchronize()
+    sweep_ms = statistics.median(a.elapsed_time(b) for a, b in sw_ev)
+    sw_hist = sw_hist.cpu().numpy()
+
     bf16_peak, bf16_sus, peak_src = _peaks()
     fp8_peak = 2.0 * bf16_peak  # nominal dense FP8 : BF16 ratio of the part
     achieved = flops / (ms_main * 1e-3) / 1e12
@@ -342,6 +359,9 @@ def main():
                                 "recompute_bf16_used": f_rec_used},
         "e2e": {"value": flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
+        "tau_sweep": {"taus": sweep_taus, "ms": sweep_ms, "forward_ms": ms, "speedup_vs_forward_per_tau":
+                      len(sweep_taus) * ms / sweep_ms,
+                      "tiles_0_1_2plus": [[float(x) / max(1, hrow[0]) for x in hrow[1:]] for hrow in sw_hist]},
         "gpu_launches": 2 * K,
         "clocks": clocks,
     }
