@@ -201,13 +201,16 @@ __device__ __forceinline__ long long exact_dot(const uint8_t* sQ8, const uint8_t
 
 namespace lamp {
 
-// kSweep: the tau-sweep pass (Figures 1-3 and 8 sweep tau at fixed delta):
-// only the 8-bit logits, the running max and the detector run, and each
-// visited tile gets a record with, per sub-block, the largest half-ulp8 of
-// its stage-1 entries (the flag at any tau follows from it); no 16-bit
-// recompute, no P.V, no output.
-template <int D, bool kSweep>
+// kMode 0: the forward pass (delta > 0); 1: the forward pass with the first
+// stage off (delta = 0); 2 (kSweep): the tau-sweep pass (Figures 1-3 and 8
+// sweep tau at fixed delta): only the 8-bit logits, the running max and the
+// detector run, and each visited tile gets a record with, per sub-block,
+// the largest half-ulp8 of its stage-1 entries (the flag at any tau follows
+// from it); no 16-bit recompute, no P.V, no output.
+template <int D, int kMode>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __grid_constant__ FwdParams p) {
+  constexpr bool kSweep = kMode == 2;
+  constexpr bool kNoStage1 = kMode == 1;
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   // align by pointer arithmetic on the __shared__ array so that every access
@@ -495,10 +498,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       uint32_t gmx[NC / 8];  // per group of 8: max of the pairs (f16x2)
       uint32_t unc = 0u;     // logits to re-derive exactly
       {
-        const float thr = (dcode == 0u || satp) ? -INFINITY : m - 6.75f;
+        // delta = 0 (first stage off): stage 1 holds for every visible entry,
+        // so besides the logits near m only those whose two roundings lie on
+        // both sides of +tau_abs or -tau_abs can move the flag (the tile-max
+        // test and the negative scan); the sweep pass needs the largest |S8|
+        // and keeps every uncertain logit
+        const bool tsplit = kNoStage1 && T > 0.0f;
+        const float thr = (satp || (kSweep && dcode == 0u)) ? -INFINITY : m - 6.75f;
         const __half2 lthr = __half2half2(__float2half_rd(thr));
         const float c = thr - 2.2f * G - 0x1p-8f;  // S8 + 0.13 |S8| > c  <=>  S8 > c / 1.13 or c / 0.87
-        const __half2 sthr = __half2half2(__float2half_rd(c >= 0.0f ? 0.884f * c : 1.15f * c));
+        const __half2 sthr =
+            __half2half2(__float2half_rd(kNoStage1 ? -INFINITY : (c >= 0.0f ? 0.884f * c : 1.15f * c)));
         const float2 gm = make_float2(-G, -G), gp = make_float2(G, G);
 #pragma unroll
         for (int g4 = 0; g4 < NC / 8; ++g4) {  // 4 pairs at a time, one branch
@@ -521,7 +531,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int i = 4 * g4 + k;
-              const uint32_t rel = __hgt2_mask(as_half2(e4m3x2_to_f16x2((uint16_t)ch4[k])), lthr);
+              const __half2 hh = as_half2(e4m3x2_to_f16x2((uint16_t)ch4[k]));
+              uint32_t rel = __hgt2_mask(hh, lthr);
+              if (tsplit) {  // T and -T are E4M3 values: exact in f16
+                const __half2 tpos = __half2half2(__float2half_rn(T)), tneg = __hneg2(tpos);
+                const __half2 hl = as_half2(s8h[i]);
+                rel |= (__hlt2_mask(hl, tpos) & __hge2_mask(hh, tpos)) | (__hle2_mask(hl, tneg) & __hgt2_mask(hh, tneg));
+              }
               if ((d16[k] & 0xFFu) && (rel & 0xFFFFu)) unc |= 1u << (2 * i);
               if ((d16[k] >> 8) && (rel >> 16)) unc |= 1u << (2 * i + 1);
             }
@@ -869,24 +885,30 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
 }
 
 // ---------------------------------------------------------------- launcher
-template <int D, bool kSweep>
+template <int D, int kMode>
 static cudaError_t launch_fwd_d(FwdParams p, cudaStream_t st) {
   using C = Cfg<D>;
   cudaError_t e =
-      cudaFuncSetAttribute(lamp_fwd_kernel<D, kSweep>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      cudaFuncSetAttribute(lamp_fwd_kernel<D, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   p.nqb = (p.N + kBM * C::NT - 1) / (kBM * C::NT);
   const unsigned grid = (unsigned)p.nqb * (unsigned)p.B * (unsigned)p.Hq;
   if (grid == 0) return cudaSuccess;
-  lamp_fwd_kernel<D, kSweep><<<grid, C::THREADS, C::SMEM, st>>>(p);
+  lamp_fwd_kernel<D, kMode><<<grid, C::THREADS, C::SMEM, st>>>(p);
   return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_fwd_mode(const FwdParams& p, cudaStream_t st, bool sweep) {
+  if (sweep) return launch_fwd_d<D, 2>(p, st);
+  return p.delta_code == 0u ? launch_fwd_d<D, 1>(p, st) : launch_fwd_d<D, 0>(p, st);
 }
 
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st, bool sweep) {
   switch (d) {
-    case 64: return sweep ? launch_fwd_d<64, true>(p, st) : launch_fwd_d<64, false>(p, st);
-    case 128: return sweep ? launch_fwd_d<128, true>(p, st) : launch_fwd_d<128, false>(p, st);
-    case 256: return sweep ? launch_fwd_d<256, true>(p, st) : launch_fwd_d<256, false>(p, st);
+    case 64: return launch_fwd_mode<64>(p, st, sweep);
+    case 128: return launch_fwd_mode<128>(p, st, sweep);
+    case 256: return launch_fwd_mode<256>(p, st, sweep);
     default: return cudaErrorInvalidValue;
   }
 }
