@@ -198,32 +198,9 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
 
   const int B = s.batch, N = s.seqlen, Hq = s.heads_q, Hkv = s.heads_kv;
   const int T = (N + kBN - 1) / kBN;
-  if (stats && stats->counters &&
-      cudaMemsetAsync(stats->counters, 0, LAMP_NUM_COUNTERS * sizeof(uint64_t), stream) != cudaSuccess)
-    return fail(LAMP_ERR_CUDA);
-  if (!sweep && stats && stats->mask &&
-      cudaMemsetAsync(stats->mask, 0, (size_t)B * Hq * T * T, stream) != cudaSuccess)
-    return fail(LAMP_ERR_CUDA);
-  if (sweep && cudaMemsetAsync(records, 0, (size_t)B * Hq * T * T * 4, stream) != cudaSuccess)
-    return fail(LAMP_ERR_CUDA);
-  // norms of the key tiles and the abort word are contiguous: one memset
-  if (cudaMemsetAsync(ws + w.nk, 0, w.total - w.nk, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
-
-  PrepParams pp{};
-  pp.q = q; pp.k = k; pp.v = sweep ? nullptr : v;  // the sweep needs no V
-  for (int i = 0; i < 3; ++i) { pp.qs[i] = s.q_stride[i]; pp.ks[i] = s.k_stride[i]; pp.vs[i] = s.v_stride[i]; }
-  pp.q8 = ws + w.q8; pp.k8 = ws + w.k8; pp.v16 = ws + w.v16;
-  pp.q16 = s.in_dtype == LAMP_DT_FP32 ? (void*)(ws + w.q16) : nullptr;
-  pp.k16 = s.in_dtype == LAMP_DT_FP32 ? (void*)(ws + w.k16) : nullptr;
-  pp.nq = (float*)(ws + w.nq); pp.nkmax = (float*)(ws + w.nk);
-  pp.B = B; pp.N = N; pp.Hq = Hq; pp.Hkv = Hkv; pp.T = T; pp.in_f32 = s.in_dtype == LAMP_DT_FP32;
-  auto mark = [&](int i) {
-    return !s.stage_events[i] || cudaEventRecord((cudaEvent_t)s.stage_events[i], stream) == cudaSuccess;
-  };
-  if (!mark(0)) return fail(LAMP_ERR_CUDA);
-  if (launch_prep(pp, D, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
-  if (!mark(1)) return fail(LAMP_ERR_CUDA);
-
+  // all host-side preparation (kernel parameters, tensor maps) comes before
+  // the first enqueue, so the stream runs the memsets and both kernels
+  // back to back
   FwdParams fp;
   memset(&fp, 0, sizeof(fp));
   const int f8box = D == 64 ? 64 : 128;
@@ -278,6 +255,32 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   fp.timeout_ns = kTimeoutNs;
   if (const char* e = getenv("LAMP_WAIT_TIMEOUT_NS")) fp.timeout_ns = strtoull(e, nullptr, 10);
   fp.gabort = (unsigned int*)(ws + w.abort);
+  if (stats && stats->counters &&
+      cudaMemsetAsync(stats->counters, 0, LAMP_NUM_COUNTERS * sizeof(uint64_t), stream) != cudaSuccess)
+    return fail(LAMP_ERR_CUDA);
+  if (!sweep && stats && stats->mask &&
+      cudaMemsetAsync(stats->mask, 0, (size_t)B * Hq * T * T, stream) != cudaSuccess)
+    return fail(LAMP_ERR_CUDA);
+  if (sweep && cudaMemsetAsync(records, 0, (size_t)B * Hq * T * T * 4, stream) != cudaSuccess)
+    return fail(LAMP_ERR_CUDA);
+  // norms of the key tiles and the abort word are contiguous: one memset
+  if (cudaMemsetAsync(ws + w.nk, 0, w.total - w.nk, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
+
+  PrepParams pp{};
+  pp.q = q; pp.k = k; pp.v = sweep ? nullptr : v;  // the sweep needs no V
+  for (int i = 0; i < 3; ++i) { pp.qs[i] = s.q_stride[i]; pp.ks[i] = s.k_stride[i]; pp.vs[i] = s.v_stride[i]; }
+  pp.q8 = ws + w.q8; pp.k8 = ws + w.k8; pp.v16 = ws + w.v16;
+  pp.q16 = s.in_dtype == LAMP_DT_FP32 ? (void*)(ws + w.q16) : nullptr;
+  pp.k16 = s.in_dtype == LAMP_DT_FP32 ? (void*)(ws + w.k16) : nullptr;
+  pp.nq = (float*)(ws + w.nq); pp.nkmax = (float*)(ws + w.nk);
+  pp.B = B; pp.N = N; pp.Hq = Hq; pp.Hkv = Hkv; pp.T = T; pp.in_f32 = s.in_dtype == LAMP_DT_FP32;
+  auto mark = [&](int i) {
+    return !s.stage_events[i] || cudaEventRecord((cudaEvent_t)s.stage_events[i], stream) == cudaSuccess;
+  };
+  if (!mark(0)) return fail(LAMP_ERR_CUDA);
+  if (launch_prep(pp, D, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
+  if (!mark(1)) return fail(LAMP_ERR_CUDA);
+
   if (launch_fwd(fp, D, stream, sweep) != cudaSuccess) return fail(LAMP_ERR_CUDA);
   if (!mark(2)) return fail(LAMP_ERR_CUDA);
   if (own_ws && cudaFreeAsync(ws, stream) != cudaSuccess) return LAMP_ERR_CUDA;
