@@ -295,7 +295,28 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       }
       int uses0 = 0, uses1 = 0;
       uint32_t rel = 0u;  // releases waited for so far, one bit of parity per (tile, stage)
-      for (int j = J0; j < J1 && !*cx.abort; ++j) {
+      if (C::NS == 1 && !kSweep) {
+        // one stage, filled in two parts with their own barriers: K8
+        // (KV_FULL / KV_EMPTY slot 0) and K16 + V (slot 1)
+        const uint32_t st = sbase + C::OFF_ST;
+        for (int j = J0; j < J1 && !*cx.abort; ++j) {
+          const int u = j - J0, key0 = j * kBN;
+          if (u >= 1 && !wait_bar(cx, bar(M_KV_EMPTY), (u - 1) & 1)) break;
+          mbar_expect_tx(bar(M_KV_FULL), C::K8_BYTES);
+          for (int c = 0; c < D / C::F8_SWZ_ROW; ++c)
+            tma_load_4d(st + c * kBN * 128, &p.tmK8, bar(M_KV_FULL), c * C::F8_SWZ_ROW, key0, g, b);
+          uses0 = u + 1;
+          if (u >= 1 && !wait_bar(cx, bar(M_KV_EMPTY + 16), (u - 1) & 1)) break;
+          const uint32_t fb = bar(M_KV_FULL + 8);
+          mbar_expect_tx(fb, C::K16_BYTES + C::V_BYTES);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(st + C::K8_BYTES + c * kBN * 128, &p.tmK16, fb, c * 64, key0, g, b);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(st + C::K8_BYTES + C::K16_BYTES + c * kBN * 128, &p.tmV, fb, c * 64, key0, g, b);
+          uses1 = u + 1;
+        }
+      }
+      for (int j = J0; j < J1 && !*cx.abort && !(C::NS == 1 && !kSweep); ++j) {
         const int s = (j - J0) % C::NS, u = (j - J0) / C::NS;
         bool ok = true;
         if (u >= 1) {  // the stage held key j - NS: wait until every tile that used it is done
@@ -372,24 +393,57 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           mbar_arrive(bar(M_KV_EMPTY + 16 * stage_of(jlo + n - 1) + 8 * t));
         ok = false;  // nothing more to issue
       }
-      // with a single K/V stage, key i can only land after P.V(i-1) has
-      // released the stage, so P.V(i-1) goes first
-      constexpr bool kPvFirst = C::NS == 1;
+      if (C::NS == 1 && !kSweep) {
+        // One K/V stage (d = 256, one query tile): its K8 part and its
+        // K16 + V part are filled and handed back separately -- K8 once the
+        // softmax has published the step (its re-derivations read K8 until
+        // then), K16 + V after the step's P.V -- so the next key's K8 lands
+        // while the softmax still works on this step.
+        static_assert(C::NS != 1 || C::NT == 1, "one stage only with one query tile");
+        for (int i = 0; ok && i < n; ++i) {
+          const int j = jlo + i;
+          const uint32_t ph = (uint32_t)(j - J0) & 1u;
+          if (i > 0) {
+            ok = wait_bar(cx, bar(M_DEC), (i - 1) & 1);
+            if (!ok) break;
+            mbar_arrive(bar(M_KV_EMPTY));  // K8 of key j - 1
+          }
+          ok = wait_bar(cx, bar(M_KV_FULL), ph);
+          if (!ok) break;
+          tc_fence_after();
+          Mma<D>::qk8(tm + C::S8_OFF, qbase, kv(j));
+          mma_commit(bar(M_S_FULL));
+          if (i > 0) {
+            ok = wait_bar(cx, bar(M_P_FULL), (i - 1) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            Mma<D>::pv(tm, sbase + C::OFF_P, kv(j - 1) + C::K8_BYTES + C::K16_BYTES, i - 1 > 0);
+            mma_commit(bar(M_PV_DONE));
+            mma_commit(bar(M_KV_EMPTY + 16));  // K16 + V of key j - 1
+          }
+          ok = wait_bar(cx, bar(M_KV_FULL + 8), ph);
+          if (!ok) break;
+          tc_fence_after();
+          Mma<D>::qk16(tm + C::S16_OFF, qbase + C::Q8_BYTES, kv(j) + C::K8_BYTES);
+          mma_commit(bar(M_S16_FULL));
+        }
+        if (ok) ok = wait_bar(cx, bar(M_P_FULL), (n - 1) & 1);
+        if (ok) {
+          tc_fence_after();
+          Mma<D>::pv(tm, sbase + C::OFF_P, kv(jlo + n - 1) + C::K8_BYTES + C::K16_BYTES, n - 1 > 0);
+          mma_commit(bar(M_PV_DONE));
+        }
+        ok = false;
+      }
       for (int i = 0; ok && i < n; ++i) {
         const int j = jlo + i;
         if (i > 0) ok = wait_bar(cx, bar(M_DEC + 8 * t), (i - 1) & 1);
-        if (kPvFirst && ok && i > 0) {
-          ok = wait_bar(cx, bar(M_P_FULL + 8 * t), (i - 1) & 1);
-          if (!ok) break;
-          tc_fence_after();
-          pv(i - 1);
-        }
         if (ok) ok = wait_bar(cx, bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1);
         if (!ok) break;
         tc_fence_after();
         Mma<D>::qk8(tm + C::S8_OFF, qbase, kv(j));
         mma_commit(bar(M_S_FULL + 8 * t));
-        if (!kPvFirst && i > 0) {
+        if (i > 0) {
           ok = wait_bar(cx, bar(M_P_FULL + 8 * t), (i - 1) & 1);
           if (!ok) break;
           tc_fence_after();

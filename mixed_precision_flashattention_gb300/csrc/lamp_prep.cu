@@ -64,7 +64,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // 16-byte accesses: a lane holds 8 consecutive elements of a row, D/8
-// lanes a row, 256/D rows per warp instruction; each warp has its 8 rows'
+// lanes a row, 256/D rows per warp instruction; each warp has all its rows'
 // loads in flight before it converts any of them.  Rows are taken in the
 // inputs' (b, n, h) order, so the warps of a block read one contiguous
 // stretch of the tensor.
@@ -86,6 +86,11 @@ __device__ __forceinline__ void load8(const void* base, long long off, float (&x
     }
   }
 }
+
+// rows per warp of the pre-pass (all loads in flight together; d = 256 rows
+// are twice as long)
+template <int D>
+constexpr int kPrepRowsPerWarp = D <= 128 ? 8 : 2;
 
 // Row index -> (batch, position, head) for `heads` heads, in 32-bit
 // arithmetic when the row count allows it (64-bit division is slow).
@@ -109,12 +114,13 @@ template <int D, bool F32, bool W64>
 __global__ void __launch_bounds__(256) lamp_prep_kernel(const PrepParams p) {
   constexpr int LPR = D / 8;          // lanes per row
   constexpr int RPI = 32 / LPR;       // rows per warp instruction
-  constexpr int NI = 8 / RPI;         // instructions for the warp's 8 rows
+  constexpr int RPW = kPrepRowsPerWarp<D>;  // rows per warp
+  constexpr int NI = RPW / RPI;       // instructions for the warp's rows
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, col = (lane % LPR) * 8;
   const long long nQ = (long long)p.B * p.N * p.Hq, nK = (long long)p.B * p.N * p.Hkv;
   const long long nrows = nQ + (p.v ? 2 : 1) * nK;
-  const long long row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * 8;
+  const long long row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * RPW;
   float x[NI][8];
   long long rows[NI];
   int rb[NI], rn[NI], rh[NI];  // (batch, position, head) of each row
@@ -194,7 +200,8 @@ __global__ void __launch_bounds__(256) lamp_prep_kernel(const PrepParams p) {
 template <int D>
 static cudaError_t launch_prep_d(const PrepParams& p, cudaStream_t st) {
   const long long rows = (long long)p.B * p.N * (p.Hq + (p.v ? 2LL : 1LL) * p.Hkv);  // no V rows without v
-  const long long blocks = (rows + 63) / 64;  // 8 warps x 8 rows
+  const long long per_block = 8LL * kPrepRowsPerWarp<D>;  // 8 warps
+  const long long blocks = (rows + per_block - 1) / per_block;
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   const bool w64 = rows + 64 >= (1LL << 31);
