@@ -57,6 +57,9 @@ struct PrepParams {
   float* nq;                      // [B, Hq, N]
   float* nkmax;                   // [B, Hkv, T] (zeroed before the launch)
   int B, N, Hq, Hkv, T, in_f32;
+  // division by Hq, Hkv and N as multiply and shift (set by the launcher)
+  uint32_t mul_hq, mul_hkv, mul_n;
+  int shr_hq, shr_hkv, shr_n;
 };
 
 // Byte offset of byte `x` (0 <= x < row_bytes) of row `r` in a K-major

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "lamp_common.cuh"
 
@@ -26,54 +27,62 @@ namespace lamp {
 template <int D>
 constexpr int kPrepRows = D <= 128 ? 4 : 2;
 
-// Row index -> (batch, position, head) for `heads` heads, in 32-bit
-// arithmetic when the row count allows it (64-bit division is slow).
-template <bool W64>
-__device__ __forceinline__ void split_row(long long row, int heads, int N, int& b, int& n, int& h) {
-  if (W64) {
-    h = (int)(row % heads);
-    const long long bn = row / heads;
-    n = (int)(bn % N);
-    b = (int)(bn / N);
-  } else {
-    const uint32_t r = (uint32_t)row, bn = r / (uint32_t)heads;
-    h = (int)(r - bn * (uint32_t)heads);
-    const uint32_t bb = bn / (uint32_t)N;
-    n = (int)(bn - bb * (uint32_t)N);
-    b = (int)bb;
-  }
+// Division of n < 2^31 by a fixed d < 2^31 as (m n) >> s with
+// m = ceil(2^(31+l) / d), s = 31 + l, l = ceil(log2 d): the round-up
+// multiplier of Granlund and Montgomery, "Division by Invariant Integers
+// using Multiplication" (1994), Theorem 4.2 with N = 31.
+__device__ __forceinline__ uint32_t div_inv(uint32_t n, uint32_t m, int s) {
+  return (uint32_t)(((unsigned long long)m * n) >> s);
 }
 
-// One lane's share of one row: the raw 16 or 32 input bytes and where the
-// row goes.  kind: 0 q, 1 k, 2 v, -1 no row.
-template <bool F32>
+static void inv_divisor(int d, uint32_t& m, int& s) {
+  int l = 0;
+  while ((1LL << l) < d) ++l;
+  s = 31 + l;
+  m = (uint32_t)(((1ULL << s) + (unsigned long long)d - 1) / (unsigned long long)d);
+}
+
+// One lane's share of one row: the raw 16 or 32 input bytes, the kind of
+// row (0 q, 1 k, 2 v, -1 none), its output row (b, h, n) -> (b H + h) N + n
+// and, for k, its entry of the per-key-tile norm maximum.  In the 32-bit
+// variant every offset and index of the launch is below 2^31.
+template <bool F32, bool W64>
 struct PrepSlot {
+  using Off = std::conditional_t<W64, long long, uint32_t>;
   uint4 a, c;  // c only for fp32 input
-  int kind, b, n, h;
+  int kind;
+  Off orow, nki;
 };
 
 template <int D, bool F32, bool W64>
 __device__ __forceinline__ void prep_issue(const PrepParams& p, long long row, int col, long long nQ, long long nK,
-                                           long long nrows, PrepSlot<F32>& s) {
+                                           long long nrows, PrepSlot<F32, W64>& s) {
+  using Off = typename PrepSlot<F32, W64>::Off;
   s.kind = -1;
-  s.b = s.n = s.h = 0;
+  s.orow = s.nki = 0;
   if (row >= nrows) return;
-  const void* src;
-  long long off;
-  if (row < nQ) {
-    split_row<W64>(row, p.Hq, p.N, s.b, s.n, s.h);
-    s.kind = 0;
-    src = p.q;
-    off = s.b * p.qs[0] + s.n * p.qs[1] + s.h * p.qs[2];
+  const bool isq = row < nQ, isk = !isq && row < nQ + nK;
+  const long long r = isq ? row : (isk ? row - nQ : row - nQ - nK);
+  const int H = isq ? p.Hq : p.Hkv;
+  Off b, n, h;
+  if (W64) {
+    h = (Off)(r % H);
+    const long long bn = r / H;
+    n = (Off)(bn % p.N);
+    b = (Off)(bn / p.N);
   } else {
-    const bool isk = row < nQ + nK;
-    split_row<W64>(isk ? row - nQ : row - nQ - nK, p.Hkv, p.N, s.b, s.n, s.h);
-    s.kind = isk ? 1 : 2;
-    const long long* st = isk ? p.ks : p.vs;
-    src = isk ? p.k : p.v;
-    off = s.b * st[0] + s.n * st[1] + s.h * st[2];
+    const uint32_t ru = (uint32_t)r;
+    const uint32_t bn = div_inv(ru, isq ? p.mul_hq : p.mul_hkv, isq ? p.shr_hq : p.shr_hkv);
+    h = ru - bn * (uint32_t)H;
+    b = div_inv(bn, p.mul_n, p.shr_n);
+    n = bn - b * (uint32_t)p.N;
   }
-  off += col;
+  const long long* st = isq ? p.qs : (isk ? p.ks : p.vs);
+  const void* src = isq ? p.q : (isk ? p.k : p.v);
+  const Off off = b * (Off)st[0] + n * (Off)st[1] + h * (Off)st[2] + (Off)col;
+  s.kind = isq ? 0 : (isk ? 1 : 2);
+  s.orow = (b * (Off)H + h) * (Off)p.N + n;
+  s.nki = (b * (Off)p.Hkv + h) * (Off)p.T + n / kBN;
   if (F32) {
     const uint4* g = reinterpret_cast<const uint4*>((const float*)src + off);
     s.a = g[0];
@@ -83,8 +92,9 @@ __device__ __forceinline__ void prep_issue(const PrepParams& p, long long row, i
   }
 }
 
-template <int D, bool F32>
-__device__ __forceinline__ void prep_store(const PrepParams& p, int col, int lane, const PrepSlot<F32>& s) {
+template <int D, bool F32, bool W64>
+__device__ __forceinline__ void prep_store(const PrepParams& p, int col, int lane, const PrepSlot<F32, W64>& s) {
+  using Off = typename PrepSlot<F32, W64>::Off;
   constexpr int LPR = D / 8;
   float x[8];
   if (F32) {
@@ -104,7 +114,7 @@ __device__ __forceinline__ void prep_store(const PrepParams& p, int col, int lan
   const bool isq = s.kind == 0, isk = s.kind == 1;
   float ss = 0.0f;
   if (isq || isk) {
-    const size_t o = (((size_t)s.b * (isq ? p.Hq : p.Hkv) + s.h) * p.N + s.n) * D + col;
+    const Off o = s.orow * (Off)D + (Off)col;
     uint32_t c8[2];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -127,7 +137,7 @@ __device__ __forceinline__ void prep_store(const PrepParams& p, int col, int lan
       *reinterpret_cast<uint4*>((__nv_bfloat16*)(isq ? p.q16 : p.k16) + o) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   } else if (s.kind == 2) {  // v -> fp16
-    const size_t o = (((size_t)s.b * p.Hkv + s.h) * p.N + s.n) * D + col;
+    const Off o = s.orow * (Off)D + (Off)col;
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) w[i] = cvt_f16x2_sat(x[2 * i + 1], x[2 * i]);
@@ -139,9 +149,9 @@ __device__ __forceinline__ void prep_store(const PrepParams& p, int col, int lan
   if ((isq || isk) && (lane % LPR) == 0) {
     // upper bound of the norm: the float sum of squares is rounded up
     const float nrm = sqrtf(ss) * (1.0f + 0x1p-16f);
-    if (isq) p.nq[((size_t)s.b * p.Hq + s.h) * p.N + s.n] = nrm;
+    if (isq) p.nq[s.orow] = nrm;
     else  // non-negative floats order like their bit patterns
-      atomicMax((int*)&p.nkmax[((size_t)s.b * p.Hkv + s.h) * p.T + s.n / kBN], __float_as_int(nrm));
+      atomicMax((int*)&p.nkmax[s.nki], __float_as_int(nrm));
   }
 }
 
@@ -157,17 +167,17 @@ __global__ void __launch_bounds__(256) lamp_prep_kernel(const PrepParams p) {
   const long long ngroups = (nrows + kPrepRows<D> - 1) / kPrepRows<D>;
   const long long stride = (long long)gridDim.x * 8;
   long long g = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  PrepSlot<F32> cur[NI];
+  PrepSlot<F32, W64> cur[NI];
 #pragma unroll
   for (int it = 0; it < NI; ++it)
     prep_issue<D, F32, W64>(p, g * kPrepRows<D> + it * RPI + sub, col, nQ, nK, nrows, cur[it]);
   for (; g < ngroups; g += stride) {
-    PrepSlot<F32> nxt[NI];
+    PrepSlot<F32, W64> nxt[NI];
 #pragma unroll
     for (int it = 0; it < NI; ++it)
       prep_issue<D, F32, W64>(p, (g + stride) * kPrepRows<D> + it * RPI + sub, col, nQ, nK, nrows, nxt[it]);
 #pragma unroll
-    for (int it = 0; it < NI; ++it) prep_store<D, F32>(p, col, lane, cur[it]);
+    for (int it = 0; it < NI; ++it) prep_store<D, F32, W64>(p, col, lane, cur[it]);
 #pragma unroll
     for (int it = 0; it < NI; ++it) cur[it] = nxt[it];
   }
@@ -195,14 +205,29 @@ static cudaError_t launch_prep_t(const PrepParams& p, long long ngroups, cudaStr
   return cudaGetLastError();
 }
 
+// largest element offset b s0 + n s1 + h s2 + D of a tensor, or -1 if a
+// stride is negative
+static long long max_offset(const long long* st, int B, int N, int H, int D) {
+  if (st[0] < 0 || st[1] < 0 || st[2] < 0) return -1;
+  return (B - 1) * st[0] + (N - 1) * st[1] + (H - 1) * st[2] + D;
+}
+
 template <int D>
-static cudaError_t launch_prep_d(const PrepParams& p, cudaStream_t st) {
+static cudaError_t launch_prep_d(const PrepParams& p0, cudaStream_t st) {
+  PrepParams p = p0;
   const long long rows = (long long)p.B * p.N * (p.Hq + (p.v ? 2LL : 1LL) * p.Hkv);  // no V rows without v
   const long long ngroups = (rows + kPrepRows<D> - 1) / kPrepRows<D>;
   if (ngroups == 0) return cudaSuccess;
-  // 32-bit row arithmetic while every row index (and one stride past the
-  // last group) stays below 2^31
-  const bool w64 = rows + 64LL * 1024 * 1024 >= (1LL << 31);
+  inv_divisor(p.Hq, p.mul_hq, p.shr_hq);
+  inv_divisor(p.Hkv, p.mul_hkv, p.shr_hkv);
+  inv_divisor(p.N, p.mul_n, p.shr_n);
+  // 32-bit offsets when every row index, input offset and output offset of
+  // the launch stays below 2^31
+  const long long lim = (1LL << 31) - 1;
+  const long long oq = max_offset(p.qs, p.B, p.N, p.Hq, D), ok = max_offset(p.ks, p.B, p.N, p.Hkv, D),
+                  ov = p.v ? max_offset(p.vs, p.B, p.N, p.Hkv, D) : 0;
+  const bool w64 = rows >= lim || (long long)p.B * p.Hq * p.N * D >= lim || oq < 0 || oq >= lim || ok < 0 ||
+                   ok >= lim || ov < 0 || ov >= lim;
   if (p.in_f32)
     return w64 ? launch_prep_t<D, true, true>(p, ngroups, st) : launch_prep_t<D, true, false>(p, ngroups, st);
   return w64 ? launch_prep_t<D, false, true>(p, ngroups, st) : launch_prep_t<D, false, false>(p, ngroups, st);
