@@ -77,9 +77,13 @@ __device__ __forceinline__ void prep_issue(const PrepParams& p, long long row, i
     b = div_inv(bn, p.mul_n, p.shr_n);
     n = bn - b * (uint32_t)p.N;
   }
-  const long long* st = isq ? p.qs : (isk ? p.ks : p.vs);
+  // strides picked by value (a pointer into the parameters would make
+  // every row an indexed constant load)
+  const long long s0 = isq ? p.qs[0] : (isk ? p.ks[0] : p.vs[0]);
+  const long long s1 = isq ? p.qs[1] : (isk ? p.ks[1] : p.vs[1]);
+  const long long s2 = isq ? p.qs[2] : (isk ? p.ks[2] : p.vs[2]);
   const void* src = isq ? p.q : (isk ? p.k : p.v);
-  const Off off = b * (Off)st[0] + n * (Off)st[1] + h * (Off)st[2] + (Off)col;
+  const Off off = b * (Off)s0 + n * (Off)s1 + h * (Off)s2 + (Off)col;
   s.kind = isq ? 0 : (isk ? 1 : 2);
   s.orow = (b * (Off)H + h) * (Off)p.N + n;
   s.nki = (b * (Off)p.Hkv + h) * (Off)p.T + n / kBN;
@@ -167,19 +171,27 @@ __global__ void __launch_bounds__(256) lamp_prep_kernel(const PrepParams p) {
   const long long ngroups = (nrows + kPrepRows<D> - 1) / kPrepRows<D>;
   const long long stride = (long long)gridDim.x * 8;
   long long g = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  PrepSlot<F32, W64> cur[NI];
-#pragma unroll
-  for (int it = 0; it < NI; ++it)
-    prep_issue<D, F32, W64>(p, g * kPrepRows<D> + it * RPI + sub, col, nQ, nK, nrows, cur[it]);
-  for (; g < ngroups; g += stride) {
-    PrepSlot<F32, W64> nxt[NI];
+  // two sets of slots that take turns (the loop is unrolled by two so
+  // neither is copied into the other)
+  PrepSlot<F32, W64> sa[NI], sb[NI];
+  auto issue = [&](long long grp, PrepSlot<F32, W64>(&s)[NI]) {
 #pragma unroll
     for (int it = 0; it < NI; ++it)
-      prep_issue<D, F32, W64>(p, (g + stride) * kPrepRows<D> + it * RPI + sub, col, nQ, nK, nrows, nxt[it]);
+      prep_issue<D, F32, W64>(p, grp * kPrepRows<D> + it * RPI + sub, col, nQ, nK, nrows, s[it]);
+  };
+  auto store = [&](const PrepSlot<F32, W64>(&s)[NI]) {
 #pragma unroll
-    for (int it = 0; it < NI; ++it) prep_store<D, F32, W64>(p, col, lane, cur[it]);
-#pragma unroll
-    for (int it = 0; it < NI; ++it) cur[it] = nxt[it];
+    for (int it = 0; it < NI; ++it) prep_store<D, F32, W64>(p, col, lane, s[it]);
+  };
+  issue(g, sa);
+  while (g < ngroups) {
+    issue(g + stride, sb);
+    store(sa);
+    g += stride;
+    if (g >= ngroups) break;
+    issue(g + stride, sa);
+    store(sb);
+    g += stride;
   }
 }
 
