@@ -179,11 +179,14 @@ int lamp_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out
  * counterpart: this is a data-movement variant only, and the results are
  * bit-identical to lamp_attn_fwd on the same inputs.
  *
- * The batch -- and, while batch * groups < 4, the kv-head groups -- is cut
+ * The batch -- and, while batch * groups < 8, the kv-head groups -- is cut
  * into chunks; per chunk the inputs are copied to the device, the forward
- * pass runs on shapes->stream and the outputs are copied back, on two
- * internal copy streams and two device slots, so the copies of one chunk
- * overlap the computation of its neighbours.
+ * pass runs and the outputs are copied back, on two internal copy streams
+ * and two device slots, so the copies of one chunk overlap the computation
+ * of its neighbours.  Chunks compute alternately on shapes->stream and on
+ * an internal stream (joined back into shapes->stream before the call
+ * returns), so one chunk's kernels start on the SMs the previous chunk's
+ * tail leaves idle.
  *   q, k, v, out  HOST, BSHD with the strides of `shapes` (elements); the
  *                 head and head_dim dimensions must be dense
  *                 (stride[2] == head_dim).

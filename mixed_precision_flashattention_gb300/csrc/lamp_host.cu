@@ -1,8 +1,10 @@
 // lamp_host.cu -- lamp_attn_fwd on host buffers: the batch (and, for small
 // batches, the kv-head groups) is cut into chunks, and per chunk the
 // host->device copies, the forward pass and the device->host copies run on
-// three streams with two device slots, so the transfers of one chunk
-// overlap the computation of its neighbours.
+// their own streams with two device slots, so the transfers of one chunk
+// overlap the computation of its neighbours.  Consecutive chunks compute on
+// two streams (the caller's and an internal one), so the CTAs of the next
+// chunk fill the SMs that the tail of the current one leaves idle.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -25,13 +27,13 @@ struct Plan {
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// At least 4 chunks when possible: kv-head groups are split (a divisor of
-// heads_kv) until batch * groups reaches 4.
+// At least 8 chunks when possible: kv-head groups are split (a divisor of
+// heads_kv) until batch * groups reaches 8.
 bool make_plan(const lamp_shapes& s, Plan& p) {
   const int B = s.batch, Hq = s.heads_q, Hkv = s.heads_kv, N = s.seqlen, D = s.head_dim;
   if (B < 1 || N < 1 || Hkv < 1 || Hq < 1 || Hq % Hkv) return false;
   int nh = 1;
-  while (B * nh < 4 && nh < Hkv) {
+  while (B * nh < 8 && nh < Hkv) {
     int next = nh + 1;
     while (next <= Hkv && Hkv % next) ++next;
     if (next > Hkv) break;
@@ -87,9 +89,9 @@ __global__ void sum_counters_kernel(unsigned long long* dst, const unsigned long
   dst[i] = acc;
 }
 
-// Two copy streams per device, created once.
+// Two copy streams and a second compute stream per device, created once.
 struct CopyStreams {
-  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaStream_t h2d = nullptr, d2h = nullptr, comp = nullptr;
 };
 std::mutex g_streams_mu;
 CopyStreams g_streams[64];
@@ -100,6 +102,7 @@ bool copy_streams(int dev, CopyStreams& out) {
   CopyStreams& cs = g_streams[dev];
   if (!cs.h2d && cudaStreamCreateWithFlags(&cs.h2d, cudaStreamNonBlocking) != cudaSuccess) return false;
   if (!cs.d2h && cudaStreamCreateWithFlags(&cs.d2h, cudaStreamNonBlocking) != cudaSuccess) return false;
+  if (!cs.comp && cudaStreamCreateWithFlags(&cs.comp, cudaStreamNonBlocking) != cudaSuccess) return false;
   out = cs;
   return true;
 }
@@ -138,8 +141,8 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
 
   uint8_t* buf = (uint8_t*)dev_buffer;
   if (buf && (dev_buffer_bytes < p.total || ((uintptr_t)buf & 255u))) return LAMP_ERR_WORKSPACE;
-  cudaEvent_t ev[8] = {};  // per slot: inputs landed, computed, outputs read back; two joins
-  for (int i = 0; i < 8; ++i)
+  cudaEvent_t ev[9] = {};  // per slot: inputs landed, computed, outputs read back; three joins
+  for (int i = 0; i < 9; ++i)
     if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
       for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
       return LAMP_ERR_CUDA;
@@ -162,10 +165,13 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
   const int N = s.seqlen, Hq = s.heads_q, Hkv = s.heads_kv;
   const int T = (N + 63) / 64;
 
-  // the copy streams start after the work already queued on the compute stream
+  // the other streams start after the work already queued on the caller's
+  // stream; chunks on slot 0 compute there, chunks on slot 1 on cps.comp
   cuda_ok(cudaEventRecord(ev[6], sc));
   cuda_ok(cudaStreamWaitEvent(cps.h2d, ev[6], 0));
   cuda_ok(cudaStreamWaitEvent(cps.d2h, ev[6], 0));
+  cuda_ok(cudaStreamWaitEvent(cps.comp, ev[6], 0));
+  const cudaStream_t comp[2] = {sc, cps.comp};
   for (int c = 0; c < p.nchunks && rc == LAMP_OK; ++c) {
     const int b = c / p.nh, g0 = (c % p.nh) * p.hkv_c, h0 = g0 * (Hq / Hkv);
     const int slot = c & 1;
@@ -187,11 +193,12 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
                               N, cudaMemcpyHostToDevice, cps.h2d));
     cuda_ok(cudaEventRecord(e_in, cps.h2d));
     // compute: inputs landed, and the slot's previous outputs were read back
-    cuda_ok(cudaStreamWaitEvent(sc, e_in, 0));
-    if (c >= 2) cuda_ok(cudaStreamWaitEvent(sc, e_out, 0));
+    const cudaStream_t cst = comp[slot];
+    cuda_ok(cudaStreamWaitEvent(cst, e_in, 0));
+    if (c >= 2) cuda_ok(cudaStreamWaitEvent(cst, e_out, 0));
     if (rc != LAMP_OK) break;
     lamp_shapes cs = p.cs;
-    cs.stream = sc;
+    cs.stream = cst;
     cs.workspace = dws;
     cs.workspace_bytes = p.ws_bytes;
     lamp_stats st;
@@ -202,7 +209,7 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
       rc = r;
       break;
     }
-    cuda_ok(cudaEventRecord(e_done, sc));
+    cuda_ok(cudaEventRecord(e_done, cst));
     // outputs back to the host
     cuda_ok(cudaStreamWaitEvent(cps.d2h, e_done, 0));
     char* ho = (char*)out + ((size_t)b * s.o_stride[0] + (size_t)h0 * D) * eo;
@@ -213,11 +220,14 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
                               cps.d2h));
     cuda_ok(cudaEventRecord(e_out, cps.d2h));
   }
-  // join: the compute stream waits for the last read-back
+  // join: the caller's stream waits for the last read-back, the last copy
+  // in and the second compute stream
   cuda_ok(cudaEventRecord(ev[7], cps.d2h));
   cuda_ok(cudaStreamWaitEvent(sc, ev[7], 0));
   cuda_ok(cudaEventRecord(ev[6], cps.h2d));
   cuda_ok(cudaStreamWaitEvent(sc, ev[6], 0));
+  cuda_ok(cudaEventRecord(ev[8], cps.comp));
+  cuda_ok(cudaStreamWaitEvent(sc, ev[8], 0));
   if (rc == LAMP_OK && stats && stats->counters) {
     sum_counters_kernel<<<1, 32, 0, sc>>>((unsigned long long*)stats->counters, cnt, p.nchunks);
     cuda_ok(cudaGetLastError());
