@@ -95,7 +95,9 @@ def run_cpu_oracle(pool, tasks):
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock and throttle-reason samples (every 20 ms) with their
+    timestamps; only the samples inside the timed region are reported."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -103,16 +105,40 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.t0 = self.t1 = None
 
     def start(self):
+        """Start sampling; returns once the first sample is written (or after 5 s)."""
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        deadline = time.time() + 5.0
+        while time.time() < deadline and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
 
     def stop(self):
         if self.proc is None:
@@ -123,16 +149,24 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 9:
+            if len(parts) >= 10:
                 rows.append(parts)
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        inside = rows
+        if self.t0 is not None and self.t1 is not None:
+            stamped = [(self._when(r[0]), r) for r in rows]
+            inside = [r for t, r in stamped if t is not None and self.t0 <= t <= self.t1]
+            if not inside:  # region shorter than the sampling period: the samples around it
+                before = [r for t, r in stamped if t is not None and t <= self.t1]
+                after = [r for t, r in stamped if t is not None and t > self.t1]
+                inside = before[-1:] + after[:1]
+        sm = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in inside if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j].lower().startswith("active")})
+        reasons = sorted({names[j] for r in inside for j in range(4) if r[6 + j].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(inside)}
 
 
 KERNEL_SOURCES = ["mixed_precision_flashattention_gb300/csrc/lamp_fwd.cu",
@@ -265,10 +299,12 @@ def main():
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
+    clk.mark_start()
     for i in range(K):
         flush.zero_()
         step(ev[i])
     torch.cuda.synchronize()
+    clk.mark_end()
     t_wall = time.perf_counter() - t_wall
     clocks = clk.stop()
     t_step = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
