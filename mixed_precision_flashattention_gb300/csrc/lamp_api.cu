@@ -240,6 +240,9 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   fp.mask_kind = mask_kind;
   fp.force = s.force;
   fp.out_f32 = s.out_dtype == LAMP_DT_FP32;
+  // bf16 q: the fused kernel rounds its Q16 tile (the input values) to E4M3
+  // itself; fp32 q must be rounded from the fp32 values, by the pre-pass
+  fp.q8_in_cta = s.in_dtype == LAMP_DT_BF16 && !sweep;
   fp.sigma_f = (float)sigma_d;
   fp.sigma_d = sigma_d;
   {
@@ -268,6 +271,7 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
 
   PrepParams pp{};
   pp.q = q; pp.k = k; pp.v = sweep ? nullptr : v;  // the sweep needs no V
+  pp.skip_q = fp.q8_in_cta;
   for (int i = 0; i < 3; ++i) { pp.qs[i] = s.q_stride[i]; pp.ks[i] = s.k_stride[i]; pp.vs[i] = s.v_stride[i]; }
   pp.q8 = ws + w.q8; pp.k8 = ws + w.k8; pp.v16 = ws + w.v16;
   pp.q16 = s.in_dtype == LAMP_DT_FP32 ? (void*)(ws + w.q16) : nullptr;

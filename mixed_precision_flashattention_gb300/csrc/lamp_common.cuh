@@ -31,6 +31,7 @@ struct FwdParams {
   long long o_stride[3];
   int B, N, Hq, Hkv, T, nqb;
   int window, mask_kind, force, out_f32;
+  int q8_in_cta;        // bf16 q: Q8 = fl8(Q16 tile) in shared memory, row norms in the kernel
   float sigma_f;       // softmax scale rounded to float
   double sigma_d;      // softmax scale in double
   unsigned long long sig_m;  // sigma_d = sig_m * 2^sig_e, 2^52 <= sig_m < 2^53
@@ -57,6 +58,7 @@ struct PrepParams {
   float* nq;                      // [B, Hq, N]
   float* nkmax;                   // [B, Hkv, T] (zeroed before the launch)
   int B, N, Hq, Hkv, T, in_f32;
+  int skip_q;  // the fused kernel makes Q8 and the q norms itself
   // division by Hq, Hkv and N as multiply and shift (set by the launcher)
   uint32_t mul_hq, mul_hkv, mul_n;
   int shr_hq, shr_hkv, shr_n;

@@ -84,6 +84,7 @@ enum : int {
   M_TMEM = 152,       // u32 TMEM base address
   M_ABORT = 156,      // u32 abort flag
   M_SFLAG = 160,      // u32 [2 tiles][2 step parities][4 warps] strip bits
+  M_Q8_READY = 224,   // [2 tiles] Q8 made from the Q16 tile (bf16 q)
   M_EXP8 = 256,       // u8 [256] exp8 table: code of fl8(exp(x)) per code of x
   M_XCH = 512,        // f32 [2 tiles][2 halves][128 rows] values exchanged between a row's two threads
   M_XB = 2560,        // u32 [2 tiles][2 halves][128 rows] bits exchanged between a row's two threads
@@ -207,6 +208,39 @@ namespace lamp {
 // detector run, and each visited tile gets a record with, per sub-block,
 // the largest half-ulp8 of its stage-1 entries (the flag at any tau follows
 // from it); no 16-bit recompute, no P.V, no output.
+
+// bf16 q: a softmax thread rounds its half (hf) of row t of the Q16 tile to
+// E4M3 (the rounding the pre-pass applies to fp32 values; bf16 -> fp32 is
+// exact), writes the codes into the Q8 tile for the tensor core, arrives on
+// `rdy` and returns the sum of squares of their values.  Not inlined: kept
+// out of the step loop's code, which runs measurably slower otherwise.
+template <int D>
+__device__ __noinline__ float q8_from_q16(uint8_t* q8w, int t, int hf, uint32_t rdy) {
+  using C = Cfg<D>;
+  float ss = 0.0f;
+  const uint8_t* q16 = q8w + C::Q8_BYTES;
+#pragma unroll
+  for (int u = 0; u < D / 32; ++u) {
+    const int cb = hf * (D / 2) + 16 * u;  // first of the 16 columns
+    const uint4 w0 = *reinterpret_cast<const uint4*>(q16 + swz_offset(t, 2 * cb, kBM, 2 * D));
+    const uint4 w1 = *reinterpret_cast<const uint4*>(q16 + swz_offset(t, 2 * cb + 16, kBM, 2 * D));
+    const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint16_t c = cvt_e4m3x2(__uint_as_float(wd[i] & 0xFFFF0000u), __uint_as_float(wd[i] << 16));
+      const __half2 hv = as_half2(e4m3x2_to_f16x2(c));
+      const float a0 = __low2float(hv), a1 = __high2float(hv);
+      ss = fmaf(a0, a0, fmaf(a1, a1, ss));
+      if (i & 1) o[i >> 1] |= (uint32_t)c << 16; else o[i >> 1] = c;
+    }
+    *reinterpret_cast<uint4*>(q8w + swz_offset(t, cb, kBM, D)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  fence_proxy_async_smem();  // visible to the tensor core's reads
+  mbar_arrive(rdy);
+  return ss;
+}
+
 template <int D, int kMode>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __grid_constant__ FwdParams p) {
   constexpr bool kSweep = kMode == 2;
@@ -254,6 +288,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       mbar_init(bar(M_P_FULL + 8 * s), C::SM_THREADS);
       mbar_init(bar(M_PV_DONE + 8 * s), 1);
       mbar_init(bar(M_DRAIN + 8 * s), 1);
+      mbar_init(bar(M_Q8_READY + 8 * s), C::SM_THREADS);
     }
     mbar_init(bar(M_Q_FULL), 1);
     *(volatile uint32_t*)(misc + M_ABORT) = 0u;
@@ -284,10 +319,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         prefetch_tmap(&p.tmK16);
         prefetch_tmap(&p.tmV);
       }
-      mbar_expect_tx(bar(M_Q_FULL), C::NT * (kSweep ? C::Q8_BYTES : C::QT_BYTES));
+      // Q8 comes from the pre-pass, or (bf16 q) the softmax makes it from Q16
+      const bool load_q8 = kSweep || !p.q8_in_cta;
+      mbar_expect_tx(bar(M_Q_FULL),
+                     C::NT * ((load_q8 ? C::Q8_BYTES : 0) + (kSweep ? 0 : C::Q16_BYTES)));
       for (int t = 0; t < C::NT; ++t) {
         const uint32_t qd = sbase + C::OFF_Q + t * C::QT_BYTES;
-        for (int c = 0; c < D / C::F8_SWZ_ROW; ++c)
+        for (int c = 0; load_q8 && c < D / C::F8_SWZ_ROW; ++c)
           tma_load_4d(qd + c * kBM * 128, &p.tmQ8, bar(M_Q_FULL), c * C::F8_SWZ_ROW, q0 + t * kBM, h, b);
         if (!kSweep)
           for (int c = 0; c < D / 64; ++c)
@@ -372,6 +410,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         mma_commit(bar(M_KV_EMPTY + 16 * stage_of(jlo + i) + 8 * t));
       };
       bool ok = wait_bar(cx, bar(M_Q_FULL), 0);
+      if (ok && !kSweep && p.q8_in_cta) ok = wait_bar(cx, bar(M_Q8_READY + 8 * t), 0);
       if (kSweep) {
         // QK8 only.  A key's stage is handed back once the softmax has
         // published the step (DEC): its exact re-derivations read K8 from
@@ -491,8 +530,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     const int jf0 = (lo + kBN - 1) / kBN, jf1 = (hi + 1) / kBN - 1;
     float m = -INFINITY;
     float l = 0.0f;  // this half's running sum of the (rounded) P values fed to P.V
+    bool fail = !(nsteps > 0 && wait_bar_warp(cx, bar(M_Q_FULL), 0));
     float nq = 0.0f;
-    if (R < p.N) nq = p.nq[((size_t)b * p.Hq + h) * p.N + R];
+    if (!kSweep && p.q8_in_cta) {
+      // bf16 q: Q8 and this half's sum of squares from the Q16 tile; the
+      // row's two halves are added for ||fl8(q_r)||
+      float ss = 0.0f;
+      if (!fail) ss = q8_from_q16<D>(smem + C::OFF_Q + tt * C::QT_BYTES, t, hf, bar(M_Q8_READY + 8 * tt));
+      xb[hf * kBM + t] = __float_as_uint(ss);
+      bar_sync(pair_bar, 64);
+      // upper bound of the norm: the float sum of squares is rounded up
+      if (R < p.N) nq = sqrtf(__uint_as_float(xb[t]) + __uint_as_float(xb[kBM + t])) * (1.0f + 0x1p-16f);
+    } else if (R < p.N) {
+      nq = p.nq[((size_t)b * p.Hq + h) * p.N + R];
+    }
     // exactness guard: |A_tc - A| * sigma <= gq * (max ||k8|| + 2^-6)
     const float gq = p.guard * p.sigma_f * (nq + 0x1p-6f), satq = p.sigma_f * nq * (1.0f + p.guard);
     uint32_t c_h0 = 0, c_h1 = 0, c_h2 = 0, c_strips = 0, c_st1 = 0, c_fl = 0, c_sat = 0, c_fix = 0,
@@ -502,7 +553,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     const float2 sig2 = make_float2(sig, sig);
     const float T = p.tau_abs;
     const uint32_t dcode = p.delta_code;
-    bool fail = !(nsteps > 0 && wait_bar_warp(cx, bar(M_Q_FULL), 0));
     bool done_ok = false;
     const float* nkrow = p.nkmax + ((size_t)b * p.Hkv + g) * p.T;
     float nk_next = nsteps > 0 ? nkrow[jlo_t] : 0.0f;

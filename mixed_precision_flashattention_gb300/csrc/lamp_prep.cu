@@ -1,11 +1,12 @@
 // lamp_prep.cu -- input pre-pass of the LampAttention forward pass.
 //
 // Writes, into the workspace, the operand formats the fused kernel reads
-// with TMA: Q8 = fl8(q) and K8 = fl8(k) (E4M3, RNE, saturating, taken from
-// the input values directly), V16 = fp16(v) (RNE, saturating), BF16 copies
-// of fp32 q and k, the row norms ||Q8_r|| and the per-64-key-tile maximum
-// of ||K8_c|| (the bound that sizes the exactness guard of the 8-bit
-// logits).  HBM-bound.
+// with TMA: K8 = fl8(k) (E4M3, RNE, saturating, taken from the input values
+// directly), V16 = fp16(v) (RNE, saturating), BF16 copies of fp32 q and k,
+// the per-64-key-tile maximum of ||K8_c|| (the bound that sizes the
+// exactness guard of the 8-bit logits) and -- for fp32 q, and for the tau
+// sweep -- Q8 = fl8(q) with the row norms ||Q8_r||.  For bf16 q the fused
+// kernel rounds its own Q tile (skip_q).  HBM-bound.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(256) lamp_prep_kernel(const PrepParams p) {
   constexpr int NI = kPrepRows<D> / RPI;  // instructions per group
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, col = (lane % LPR) * 8;
-  const long long nQ = (long long)p.B * p.N * p.Hq, nK = (long long)p.B * p.N * p.Hkv;
+  const long long nQ = p.skip_q ? 0LL : (long long)p.B * p.N * p.Hq, nK = (long long)p.B * p.N * p.Hkv;
   const long long nrows = nQ + (p.v ? 2 : 1) * nK;
   const long long ngroups = (nrows + kPrepRows<D> - 1) / kPrepRows<D>;
   const long long stride = (long long)gridDim.x * 8;
@@ -227,7 +228,7 @@ static long long max_offset(const long long* st, int B, int N, int H, int D) {
 template <int D>
 static cudaError_t launch_prep_d(const PrepParams& p0, cudaStream_t st) {
   PrepParams p = p0;
-  const long long rows = (long long)p.B * p.N * (p.Hq + (p.v ? 2LL : 1LL) * p.Hkv);  // no V rows without v
+  const long long rows = (long long)p.B * p.N * ((p.skip_q ? 0LL : p.Hq) + (p.v ? 2LL : 1LL) * p.Hkv);  // no V rows without v
   const long long ngroups = (rows + kPrepRows<D> - 1) / kPrepRows<D>;
   if (ngroups == 0) return cudaSuccess;
   inv_divisor(p.Hq, p.mul_hq, p.shr_hq);
