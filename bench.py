@@ -71,12 +71,14 @@ def cpu_sample_tasks(w, q, k, v, delta, tau, wall_budget_s, ncores, seed=0):
              [(0, 0, T - 1)], w.mask, w.window, delta, tau)
     t_long = _oracle_task(probe)  # seconds for the longest query tile
     rng = np.random.default_rng(seed)
-    picks, est = {}, 0.0
-    while est < wall_budget_s * ncores and sum(len(x) for x in picks.values()) < 8192:
+    picks, est, n = {}, 0.0, 0
+    cap = min(8192, w.batch * w.heads_q * T)  # a small workload is sampled whole
+    while est < wall_budget_s * ncores and n < cap:
         b, h, i = int(rng.integers(w.batch)), int(rng.integers(w.heads_q)), int(rng.integers(T))
         if i in picks.get((b, h), ()):
             continue
         picks.setdefault((b, h), []).append(i)
+        n += 1
         est += t_long * _tile_flops(w, i) / _tile_flops(w, T - 1)
     tasks, flops = [], 0.0
     for (b, h), tiles in picks.items():
@@ -203,6 +205,22 @@ def _peaks():
     return 1900.0, 1700.0, "fallback"
 
 
+def reduce_over_ranks(ms: float, counters, world: int, device=None):
+    """Whole-job figures of a multi-rank run: the slowest rank's step time
+    and the counters summed over ranks (every rank holds its own shard).
+    One rank: returned unchanged."""
+    counters = np.asarray(counters, dtype=np.int64)
+    if world <= 1:
+        return float(ms), counters
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    c = torch.from_numpy(counters.copy()).to(device)
+    dist.all_reduce(c, op=dist.ReduceOp.SUM)
+    return float(t.item()), c.cpu().numpy()
+
+
 # ---------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -227,6 +245,8 @@ def main():
               "in_dtype": w.dtype, "tau": args.tau, "delta": args.delta,
               "generator": w.gen, "seed": args.seed}
 
+    if args.impl == "reference" and rank != 0:
+        return  # the oracle arm runs on rank 0 only
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     pool = None
     ncores = os.cpu_count() or 1
@@ -236,11 +256,12 @@ def main():
             os.environ[var] = "1"
         pool = mp.get_context("spawn").Pool(ncores)
 
-    q, k, v = synth.make(w, seed=args.seed)
+    # rank r holds its own shard of the job: the workload's shape with seed + r
+    q, k, v = synth.make(w, seed=args.seed + rank)
+    if world > 1:
+        config["shard"] = f"rank r of {world}: its own {w.batch} sequences (seed {args.seed} + r)"
 
     if args.impl == "reference":
-        if rank != 0:
-            return
         tasks, sflops = cpu_sample_tasks(w, q, k, v, args.delta, args.tau,
                                          args.cpu_seconds * 8 / max(1, args.steps + args.warmup), ncores)
         for _ in range(args.warmup):
@@ -310,12 +331,7 @@ def main():
     t_step = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
     t_prep = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     t_main = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    ms = statistics.mean(t_step)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
-    c = cnt.cpu().numpy()
+    ms, c = reduce_over_ranks(statistics.mean(t_step), cnt.cpu().numpy(), world, dev)
     ms_main = statistics.mean(t_main)
 
     # end to end through the public call on host buffers: pinned host in,
@@ -355,6 +371,7 @@ def main():
             sw_ev[i - 3][1].record()
     torch.cuda.synchronize()
     sweep_ms = statistics.median(a.elapsed_time(b) for a, b in sw_ev)
+    e2e_step, _ = reduce_over_ranks(statistics.mean(e2e_ms), [0], world, dev)  # slowest rank
     sw_hist = sw_hist.cpu().numpy()
 
     bf16_peak, bf16_sus, peak_src = _peaks()
@@ -393,12 +410,12 @@ def main():
         "tiles_0_1_2plus": [float(c[1]) / max(1, c[0]), float(c[2]) / max(1, c[0]), float(c[3]) / max(1, c[0])],
         "tensor_flops_issued": {"qk_fp8": f_qk8, "pv_fp16": f_pv, "recompute_bf16": f_rec,
                                 "recompute_bf16_used": f_rec_used},
-        "e2e": {"value": flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
+        "e2e": {"value": flops / (e2e_step * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world, "ms_per_step": e2e_step},
         "tau_sweep": {"taus": sweep_taus, "ms": sweep_ms, "forward_ms": ms, "speedup_vs_forward_per_tau":
                       len(sweep_taus) * ms / sweep_ms,
                       "tiles_0_1_2plus": [[float(x) / max(1, hrow[0]) for x in hrow[1:]] for hrow in sw_hist]},
-        "gpu_launches": 2 * K,
+        "gpu_launches": 2 * K * world,  # pre-pass + fused kernel per step and rank
         "clocks": clocks,
     }
     if want_cpu:
