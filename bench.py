@@ -262,8 +262,10 @@ def main():
         config["shard"] = f"rank r of {world}: its own {w.batch} sequences (seed {args.seed} + r)"
 
     if args.impl == "reference":
+        # about 4 x --cpu-seconds of estimated oracle time over the whole run
+        # (the pool's transfers roughly double the estimate)
         tasks, sflops = cpu_sample_tasks(w, q, k, v, args.delta, args.tau,
-                                         args.cpu_seconds * 8 / max(1, args.steps + args.warmup), ncores)
+                                         args.cpu_seconds * 4 / max(1, args.steps + args.warmup), ncores)
         for _ in range(args.warmup):
             run_cpu_oracle(pool, tasks)
         times = [run_cpu_oracle(pool, tasks) for _ in range(args.steps)]
