@@ -549,6 +549,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     uint32_t c_h0 = 0, c_h1 = 0, c_h2 = 0, c_strips = 0, c_st1 = 0, c_fl = 0, c_sat = 0, c_fix = 0,
              c_rec = 0, c_spec = 0;  // per-thread counts (a CTA sees at most 2^21 logits per thread slot)
     const int qtile = (q0 + tt * kBM) / kBN + (rw >> 1);  // 64-row query tile of this warp
+    // this query tile's row of the mask, or of the tau-sweep records
+    uint8_t* mrow = nullptr;
+    uint32_t* rrow = nullptr;
+    if (qtile < p.T) {
+      const size_t base = (((size_t)b * p.Hq + h) * p.T + qtile) * p.T;
+      if (!kSweep && p.mask) mrow = p.mask + base;
+      if (kSweep) rrow = p.records + base;
+    }
     const float sig = p.sigma_f;
     const float2 sig2 = make_float2(sig, sig);
     const float T = p.tau_abs;
@@ -805,8 +813,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       }
       if (lane == 0 && hf == 0 && (rw & 1) == 0 && !fail) {
         // lane 0 of row groups 0 and 2 owns the 64-row query tile of groups (rw, rw+1)
-        const uint32_t w0 = *(volatile uint32_t*)(sflag + 4 * rw);
-        const uint32_t w1 = *(volatile uint32_t*)(sflag + 4 * (rw + 1));
+        const unsigned long long ww = *(volatile unsigned long long*)(sflag + 4 * rw);  // rw even: 8-byte aligned
+        const uint32_t w0 = (uint32_t)ww, w1 = (uint32_t)(ww >> 32);
         const uint32_t fl4 = (w0 & 3u) | ((w1 & 3u) << 2);
         const uint32_t st4 = ((w0 >> 2) & 3u) | (((w1 >> 2) & 3u) << 2);
         const uint32_t vs4 = ((w0 >> 4) & 3u) | (((w1 >> 4) & 3u) << 2);
@@ -817,13 +825,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           if constexpr (kSweep) {
             ++c_h0;  // counts visited tiles only (no flags in this pass)
             const uint32_t codes = ((w0 >> 8) & 0xFFu) | (((w1 >> 8) & 0xFFu) << 8);
-            if (qtile < p.T)
-              p.records[(((size_t)b * p.Hq + h) * p.T + qtile) * p.T + jt] = vs4 | (st4 << 4) | (codes << 8);
+            if (rrow) rrow[jt] = vs4 | (st4 << 4) | (codes << 8);
           } else {
-            if (nf == 0) ++c_h0; else if (nf == 1) ++c_h1; else ++c_h2;
+            c_h0 += nf == 0;
+            c_h1 += nf == 1;
+            c_h2 += nf > 1;
             c_fl += nf;
-            if (p.mask && qtile < p.T)
-              p.mask[(((size_t)b * p.Hq + h) * p.T + qtile) * p.T + jt] = (uint8_t)(fl4 | (st4 << 4));
+            if (mrow) mrow[jt] = (uint8_t)(fl4 | (st4 << 4));
           }
         }
       }
