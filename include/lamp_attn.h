@@ -262,6 +262,9 @@ void lamp_exp8_table(uint8_t out[256]);
  *            the dot product a[i] * 2^-18 (a: int64[d]) and the scale b[0]
  *            (b: double[1]): E4M3 rounding of the float64 product, as a
  *            float; d = count, 1..65536.
+ *   which 4: out[i] = fl8(exp(x)) as the fused kernel computes it, for the
+ *            E4M3 code a[i] of x <= 0 (a: uint8[d]; b: any non-NULL device
+ *            pointer, unused); d = count, 1..65536.
  * a, b: DEVICE, row-major as listed; out: DEVICE float32, row-major.
  * Returns LAMP_OK or an error code after synchronising `stream`.
  */

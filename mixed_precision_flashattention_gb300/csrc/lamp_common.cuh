@@ -78,6 +78,20 @@ __device__ __forceinline__ uint32_t swz_offset(int r, int x, int rows, int row_b
   return (uint32_t)(col * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + chunk * 16 + (w & 15));
 }
 
+// f16x2 values of fl8(e^x) for the two E4M3 codes in x8 (non-positive x):
+// e^x in fp32 (ex2 of x log2 e: relative error below 2^-20), then one E4M3
+// rounding to nearest even.  Exact for every such code: among the E4M3
+// values x <= 0 with e^x >= 2^-11, the one whose e^x lies closest to an E4M3
+// rounding boundary is x = -2^-5, at 2^-11 relative -- far beyond the fp32
+// error; below 2^-11, e^x rounds to 0 either way.
+__device__ __forceinline__ uint32_t exp8_f16x2(uint32_t x8) {
+  const uint32_t h = e4m3x2_to_f16x2((uint16_t)x8);
+  __half2 xv;
+  memcpy(&xv, &h, 4);
+  const float2 xf = __fmul2_rn(make_float2(__low2float(xv), __high2float(xv)), make_float2(kLog2e, kLog2e));
+  return e4m3x2_to_f16x2(cvt_e4m3x2(ex2_approx(xf.y), ex2_approx(xf.x)));
+}
+
 // Exact product of two E4M3 codes, times 2^18 (an integer below 2^36): every
 // finite code is (significand <= 15) * 2^(shift - 9) with shift in 0..14.
 __device__ __forceinline__ long long e4m3_prod_2p18(uint32_t a, uint32_t b) {

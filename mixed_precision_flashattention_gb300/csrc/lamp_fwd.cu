@@ -295,15 +295,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     fence_mbar_init();
   }
   if (warp == C::MMA_WARP) tmem_alloc(bar(M_TMEM), C::TMEM_COLS);  // the first MMA warp owns TMEM
-  // the exp8 table: codes (for the detector's comparisons with delta) and
-  // values as f16 in both halves of a word (P8 pairs are put together with
-  // one byte permute)
-  __shared__ uint32_t s_exp8v[256];
-  if (threadIdx.x < 256) {
-    const uint8_t code = p.exp8[threadIdx.x];
-    misc[M_EXP8 + threadIdx.x] = code;
-    s_exp8v[threadIdx.x] = (e4m3x2_to_f16x2((uint16_t)code) & 0xFFFFu) * 0x00010001u;
-  }
+  // the exp8 table of codes, for the detector's comparisons with delta
+  // (the P8 values themselves are computed, exp8_f16x2)
+  if (threadIdx.x < 256) misc[M_EXP8 + threadIdx.x] = p.exp8[threadIdx.x];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -838,8 +832,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
 
       if constexpr (!kSweep) {
       // ---- x8 = fl8(S8 - m) (fp16 difference, then one E4M3 rounding: equal
-      // to the single rounding for E4M3 operands), P8 from the exp8 table;
-      // rows of flagged sub-blocks take P16 below instead
+      // to the single rounding for E4M3 operands), P8 = fl8(e^x8) (exact,
+      // exp8_f16x2); rows of flagged sub-blocks take P16 below instead
       uint32_t pw[NC / 2];
 #pragma unroll
       for (int i = 0; i < NC / 2; ++i) pw[i] = 0u;
@@ -849,8 +843,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
 #pragma unroll
         for (int i = 0; i < NC / 2; ++i) {
           const __half2 xh = __hsub2(as_half2(s8h[i]), mh);
-          const uint32_t x8 = cvt_e4m3x2_f16x2(xh);
-          const uint32_t v = __byte_perm(s_exp8v[x8 & 0xFFu], s_exp8v[x8 >> 8], 0x7610);
+          const uint32_t v = exp8_f16x2(cvt_e4m3x2_f16x2(xh));
           pw[i] = want_p8 ? v : 0u;
         }
       }

@@ -4,6 +4,8 @@
 //   which 0: S = A8 . B8^T, A8 [128 x D], B8 [64 x D] E4M3 codes, out [128 x 64]
 //   which 1: S = A . B^T,  A [128 x D], B [64 x D] BF16,          out [128 x 64]
 //   which 2: O = P . V,    P [128 x 64], V [64 x D] FP16,         out [128 x D]
+// and the scalar helpers of the fused kernel: which 3 the exact 8-bit
+// re-derivation, which 4 the 8-bit exponential P8 = fl8(e^x).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -92,6 +94,15 @@ __global__ void lamp_round_selftest_kernel(const long long* acc, const double* s
   out[i] = __half2float(__ushort_as_half((unsigned short)h));
 }
 
+// out[i] = fl8(e^x) for the E4M3 code codes[i] (x <= 0), as the fused kernel
+// computes it (exp8_f16x2)
+__global__ void lamp_exp8_selftest_kernel(const uint8_t* codes, float* out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint32_t h = exp8_f16x2((uint32_t)codes[i] * 0x0101u);
+  out[i] = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
 template <int D>
 static cudaError_t run_selftest(int which, const void* a, const void* b, float* out, unsigned int* status,
                                 cudaStream_t st) {
@@ -105,8 +116,8 @@ static cudaError_t run_selftest(int which, const void* a, const void* b, float* 
 }  // namespace lamp
 
 extern "C" int lamp_selftest(int which, const void* a, const void* b, float* out, int d, void* stream) {
-  if (!a || !b || !out || which < 0 || which > 3) return LAMP_ERR_INVALID_ARG;
-  if (which == 3 ? (d < 1 || d > 65536) : (d != 64 && d != 128 && d != 256)) return LAMP_ERR_UNSUPPORTED;
+  if (!a || !b || !out || which < 0 || which > 4) return LAMP_ERR_INVALID_ARG;
+  if (which >= 3 ? (d < 1 || d > 65536) : (d != 64 && d != 128 && d != 256)) return LAMP_ERR_UNSUPPORTED;
   int dev = 0, maj = 0, min = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LAMP_ERR_CUDA;
   cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev);
@@ -119,6 +130,9 @@ extern "C" int lamp_selftest(int which, const void* a, const void* b, float* out
   cudaError_t e = cudaSuccess;
   if (which == 3) {
     lamp::lamp_round_selftest_kernel<<<(d + 255) / 256, 256, 0, st>>>((const long long*)a, (const double*)b, out, d);
+    e = cudaGetLastError();
+  } else if (which == 4) {
+    lamp::lamp_exp8_selftest_kernel<<<(d + 255) / 256, 256, 0, st>>>((const uint8_t*)a, out, d);
     e = cudaGetLastError();
   } else {
     e = d == 64    ? lamp::run_selftest<64>(which, a, b, out, status, st)

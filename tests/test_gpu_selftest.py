@@ -223,3 +223,17 @@ def test_fp8_accumulation_adversarial(lamp, d):
           f" max |err|/sum|q_i k_i| = {rel1.max():.3e} (2^{np.log2(rel1.max() + 1e-300):.1f})")
     bound_m = tc_fp8_error_bound(d, np.linalg.norm(a8, axis=1)[:, None], np.linalg.norm(b8, axis=1)[None, :])
     assert np.all(np.abs(out - exact) <= bound_m)
+
+
+def test_exp8_arithmetic_exact(lamp):
+    """P8 = fl8(e^x) as the fused kernel computes it (fp32 ex2, one E4M3
+    rounding) equals the correctly rounded 8-bit exponential of the oracle
+    for every non-positive E4M3 code (the only inputs the kernel gives it:
+    x8 = fl8(S8 - m) <= 0), the saturated -448 and -0 included."""
+    codes = np.array([0] + list(range(0x80, 0xFF)), dtype=np.uint8)  # 0x7F / 0xFF are NaN
+    a = torch.from_numpy(codes).cuda()
+    got = lamp.selftest(4, a, a, len(codes)).cpu().numpy().astype(np.float64)
+    x = np.array([F.e4m3_decode(int(c)) for c in codes])
+    want = F.exp8(x)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(hex(codes[i]), x[i], got[i], want[i]) for i in bad[:5]]
