@@ -67,7 +67,7 @@ struct Cfg {
   static constexpr int TILE_COLS = D + 2 * kBN;
   static constexpr int TMEM_COLS = 512;
   static_assert(NT * TILE_COLS <= TMEM_COLS, "TMEM budget");
-  static_assert(SMEM + 1024 <= 227 * 1024, "shared memory budget (+ the static exp8 value table)");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
 // misc area (byte offsets inside OFF_MISC); per-tile barriers at + 8 * t

@@ -39,19 +39,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of a phase (for polling several barriers).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      "selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // try_wait that lets the hardware suspend the thread until the phase
 // completes (or about hint_ns passes), instead of spinning in software.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
@@ -196,15 +183,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -216,25 +194,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-// acc + (fp16 half of h selected by hi), in fp32
 // acc_lo += low half of h, acc_hi += high half of h (f16 values added to
 // float accumulators with one rounding each).
 __device__ __forceinline__ void add_f32_f16x2(float& acc_lo, float& acc_hi, uint32_t h) {
   asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
       "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
       : "+f"(acc_lo), "+f"(acc_hi) : "r"(h));
-}
-__device__ __forceinline__ float add_f32_f16lo(float acc, uint32_t h) {
-  float r;
-  const uint16_t v = (uint16_t)(h & 0xFFFFu);
-  asm("add.rn.f32.f16 %0, %1, %2;" : "=f"(r) : "h"(v), "f"(acc));
-  return r;
-}
-__device__ __forceinline__ float add_f32_f16hi(float acc, uint32_t h) {
-  float r;
-  const uint16_t v = (uint16_t)(h >> 16);
-  asm("add.rn.f32.f16 %0, %1, %2;" : "=f"(r) : "h"(v), "f"(acc));
-  return r;
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
