@@ -184,17 +184,38 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic(workload: str):
-    """DRAM bytes per launch of the fused kernel from the committed ncu
-    capture, if it was taken on this workload with the current kernel source
-    (else None)."""
+def _capture(workload: str):
+    """The committed ncu capture of one fused-kernel launch, if it was taken
+    on this workload with the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", "lamp_fwd_traffic.json")
     if not os.path.exists(path):
         return None
     d = json.load(open(path))
     if d.get("workload") != workload or d.get("source_sha") != kernel_source_sha():
         return None
-    return float(d["dram_bytes_read"]) + float(d["dram_bytes_write"])
+    return d
+
+
+def _traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel (committed capture)."""
+    d = _capture(workload)
+    return None if d is None else float(d["dram_bytes_read"]) + float(d["dram_bytes_write"])
+
+
+def _issue_roofline(workload: str, ms_main: float, sm_mhz):
+    """The fused kernel is bound by instruction issue in its softmax warps:
+    the floor its warp-instruction count (committed capture) allows at one
+    instruction per clock on each of the 4 schedulers of every SM, at the
+    SM clock sampled in the timed region, against the measured time."""
+    d = _capture(workload)
+    if d is None or "warp_instructions" not in d or not sm_mhz:
+        return None
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    rate = 4.0 * sms * sm_mhz * 1e6  # warp instructions per second
+    floor_ms = float(d["warp_instructions"]) / rate * 1e3
+    return {"bound": "issue", "warp_instructions": float(d["warp_instructions"]), "sms": sms,
+            "sm_mhz": sm_mhz, "floor_ms": floor_ms, "measured_ms": ms_main, "frac": floor_ms / ms_main}
 
 
 def _peaks():
@@ -405,7 +426,8 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": achieved / fp8_peak, "traffic": _traffic(w.name),
                      "kernel": "lamp_fwd_kernel", "peak_basis": f"2 x {peak_src} bf16 burst {bf16_peak} (dense FP8:BF16 = 2)",
-                     "mixed_tc_time_frac": t_tc / (ms_main * 1e-3)},
+                     "mixed_tc_time_frac": t_tc / (ms_main * 1e-3),
+                     "issue": _issue_roofline(w.name, ms_main, (clocks or {}).get("sm_mhz"))},
         "ms_main_kernel": ms_main, "ms_prepass": statistics.mean(t_prep), "wall_s": t_wall,
         "stats": {n: int(c[i]) for i, n in enumerate(lamp.COUNTER_NAMES)},
         "subblock16_frac": float(c[6]) / max(1, c[4]),
