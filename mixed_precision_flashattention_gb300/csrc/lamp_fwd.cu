@@ -64,7 +64,10 @@ struct Cfg {
   static constexpr int O_COLS = D;
   static constexpr int S8_OFF = D;
   static constexpr int S16_OFF = D + kBN;
-  static constexpr int TILE_COLS = D + 2 * kBN;
+  // one K/V stage (d = 256, one tile): two S16 buffers, so QK16 of a step
+  // can be issued while the softmax may still read the previous step's S16
+  static constexpr int S16_BUFS = (NS == 1) ? 2 : 1;
+  static constexpr int TILE_COLS = D + (1 + S16_BUFS) * kBN;
   static constexpr int TMEM_COLS = 512;
   static_assert(NT * TILE_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -77,7 +80,7 @@ enum : int {
   M_Q_FULL = 48,
   M_S_FULL = 56,      // [2 tiles] QK8 result in TMEM
   M_DEC = 72,         // [2 tiles] the softmax has read S8 (the buffer is free)
-  M_S16_FULL = 88,    // [2 tiles] QK16 result in TMEM
+  M_S16_FULL = 88,    // [2 tiles] QK16 result in TMEM (one tile, d = 256: [2 S16 buffers])
   M_P_FULL = 104,     // [2 tiles] P written, O rescaled, S16 read
   M_PV_DONE = 120,    // [2 tiles]
   M_DRAIN = 136,      // [2 tiles]
@@ -85,6 +88,8 @@ enum : int {
   M_ABORT = 156,      // u32 abort flag
   M_SFLAG = 160,      // u32 [2 tiles][2 step parities][4 warps] strip bits
   M_Q8_READY = 224,   // [2 tiles] Q8 made from the Q16 tile (bf16 q)
+  M_V_FULL = 240,     // one K/V stage: its V part landed
+  M_V_EMPTY = 248,    // one K/V stage: its V part is free (P.V done)
   M_EXP8 = 256,       // u8 [256] exp8 table: code of fl8(exp(x)) per code of x
   M_XCH = 512,        // f32 [2 tiles][2 halves][128 rows] values exchanged between a row's two threads
   M_XB = 2560,        // u32 [2 tiles][2 halves][128 rows] bits exchanged between a row's two threads
@@ -291,6 +296,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       mbar_init(bar(M_Q8_READY + 8 * s), C::SM_THREADS);
     }
     mbar_init(bar(M_Q_FULL), 1);
+    mbar_init(bar(M_V_FULL), 1);
+    mbar_init(bar(M_V_EMPTY), 1);
     *(volatile uint32_t*)(misc + M_ABORT) = 0u;
     fence_mbar_init();
   }
@@ -325,11 +332,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(qd + C::Q8_BYTES + c * kBM * 128, &p.tmQ16, bar(M_Q_FULL), c * 64, q0 + t * kBM, h, b);
       }
-      int uses0 = 0, uses1 = 0;
+      int uses0 = 0, uses1 = 0, uses2 = 0;
       uint32_t rel = 0u;  // releases waited for so far, one bit of parity per (tile, stage)
       if (C::NS == 1 && !kSweep) {
-        // one stage, filled in two parts with their own barriers: K8
-        // (KV_FULL / KV_EMPTY slot 0) and K16 + V (slot 1)
+        // one stage, filled in three parts with their own barriers: K8
+        // (KV_FULL / KV_EMPTY slot 0, free once the softmax has published
+        // the step), K16 (slot 1, free once the step's QK16 is done) and V
+        // (V_FULL / V_EMPTY, free once the step's P.V is done) -- so the
+        // next key's K16 lands long before its QK16, and only V waits for
+        // the P.V
         const uint32_t st = sbase + C::OFF_ST;
         for (int j = J0; j < J1 && !*cx.abort; ++j) {
           const int u = j - J0, key0 = j * kBN;
@@ -339,13 +350,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
             tma_load_4d(st + c * kBN * 128, &p.tmK8, bar(M_KV_FULL), c * C::F8_SWZ_ROW, key0, g, b);
           uses0 = u + 1;
           if (u >= 1 && !wait_bar(cx, bar(M_KV_EMPTY + 16), (u - 1) & 1)) break;
-          const uint32_t fb = bar(M_KV_FULL + 8);
-          mbar_expect_tx(fb, C::K16_BYTES + C::V_BYTES);
+          mbar_expect_tx(bar(M_KV_FULL + 8), C::K16_BYTES);
           for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(st + C::K8_BYTES + c * kBN * 128, &p.tmK16, fb, c * 64, key0, g, b);
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(st + C::K8_BYTES + C::K16_BYTES + c * kBN * 128, &p.tmV, fb, c * 64, key0, g, b);
+            tma_load_4d(st + C::K8_BYTES + c * kBN * 128, &p.tmK16, bar(M_KV_FULL + 8), c * 64, key0, g, b);
           uses1 = u + 1;
+          if (u >= 1 && !wait_bar(cx, bar(M_V_EMPTY), (u - 1) & 1)) break;
+          mbar_expect_tx(bar(M_V_FULL), C::V_BYTES);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(st + C::K8_BYTES + C::K16_BYTES + c * kBN * 128, &p.tmV, bar(M_V_FULL), c * 64, key0, g, b);
+          uses2 = u + 1;
         }
       }
       for (int j = J0; j < J1 && !*cx.abort && !(C::NS == 1 && !kSweep); ++j) {
@@ -379,6 +392,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       if (*cx.abort) {  // let every load in flight land before the CTA exits
         if (uses0 > 0) drain_wait(bar(M_KV_FULL), (uses0 - 1) & 1);
         if (uses1 > 0) drain_wait(bar(M_KV_FULL + 8), (uses1 - 1) & 1);
+        if (uses2 > 0) drain_wait(bar(M_V_FULL), (uses2 - 1) & 1);
         drain_wait(bar(M_Q_FULL), 0);
       }
     }
@@ -427,12 +441,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         ok = false;  // nothing more to issue
       }
       if (C::NS == 1 && !kSweep) {
-        // One K/V stage (d = 256, one query tile): its K8 part and its
-        // K16 + V part are filled and handed back separately -- K8 once the
-        // softmax has published the step (its re-derivations read K8 until
-        // then), K16 + V after the step's P.V -- so the next key's K8 lands
-        // while the softmax still works on this step.
-        static_assert(C::NS != 1 || C::NT == 1, "one stage only with one query tile");
+        // One K/V stage (d = 256, one query tile) in three parts (K8, K16,
+        // V), each handed back on its own: K8 once the softmax has published
+        // the step (its re-derivations read K8 until then), K16 once the
+        // step's QK16 is done, V after the step's P.V.  QK16(i) goes right
+        // after QK8(i), into the S16 buffer of parity i (the softmax may
+        // still read the other one); P.V(i - 1) follows once P(i - 1) is in.
+        static_assert(C::NS != 1 || (C::NT == 1 && C::S16_BUFS == 2), "one stage: one query tile, two S16 buffers");
         for (int i = 0; ok && i < n; ++i) {
           const int j = jlo + i;
           const uint32_t ph = (uint32_t)(j - J0) & 1u;
@@ -446,21 +461,27 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           tc_fence_after();
           Mma<D>::qk8(tm + C::S8_OFF, qbase, kv(j));
           mma_commit(bar(M_S_FULL));
+          ok = wait_bar(cx, bar(M_KV_FULL + 8), ph);
+          if (!ok) break;
+          tc_fence_after();
+          // one barrier per S16 buffer: a single one could complete twice
+          // (QK16(i), QK16(i + 1)) before the softmax waits for QK16(i),
+          // and a parity wait cannot tell those phases apart
+          Mma<D>::qk16(tm + C::S16_OFF + (i & 1) * kBN, qbase + C::Q8_BYTES, kv(j) + C::K8_BYTES);
+          mma_commit(bar(M_S16_FULL + 8 * (i & 1)));
+          mma_commit(bar(M_KV_EMPTY + 16));  // K16 of key j
           if (i > 0) {
             ok = wait_bar(cx, bar(M_P_FULL), (i - 1) & 1);
+            if (ok) ok = wait_bar(cx, bar(M_V_FULL), (ph ^ 1u));
             if (!ok) break;
             tc_fence_after();
             Mma<D>::pv(tm, sbase + C::OFF_P, kv(j - 1) + C::K8_BYTES + C::K16_BYTES, i - 1 > 0);
             mma_commit(bar(M_PV_DONE));
-            mma_commit(bar(M_KV_EMPTY + 16));  // K16 + V of key j - 1
+            mma_commit(bar(M_V_EMPTY));  // V of key j - 1
           }
-          ok = wait_bar(cx, bar(M_KV_FULL + 8), ph);
-          if (!ok) break;
-          tc_fence_after();
-          Mma<D>::qk16(tm + C::S16_OFF, qbase + C::Q8_BYTES, kv(j) + C::K8_BYTES);
-          mma_commit(bar(M_S16_FULL));
         }
         if (ok) ok = wait_bar(cx, bar(M_P_FULL), (n - 1) & 1);
+        if (ok) ok = wait_bar(cx, bar(M_V_FULL), (uint32_t)(jlo + n - 1 - J0) & 1u);
         if (ok) {
           tc_fence_after();
           Mma<D>::pv(tm, sbase + C::OFF_P, kv(jlo + n - 1) + C::K8_BYTES + C::K16_BYTES, n - 1 > 0);
@@ -874,11 +895,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
 
       // ---- 16-bit recompute for the rows of flagged sub-blocks
       // (the QK16 of every step is computed; a step without flags skips it)
-      if (any && !fail) fail = !wait_bar_warp(cx, bar(M_S16_FULL + 8 * tt), jj & 1);
+      // two S16 buffers (one stage): buffer jj & 1 completes every other step
+      const uint32_t s16_bar = C::S16_BUFS == 2 ? bar(M_S16_FULL + 8 * (jj & 1)) : bar(M_S16_FULL + 8 * tt);
+      const uint32_t s16_par = C::S16_BUFS == 2 ? (uint32_t)(jj >> 1) & 1u : (uint32_t)jj & 1u;
+      if (any && !fail) fail = !wait_bar_warp(cx, s16_bar, s16_par);
       if (any && !fail) {
         tc_fence_after();
         uint32_t r16[NC];
-        tmem_ld32(lane_base + C::S16_OFF + col0, r16);
+        tmem_ld32(lane_base + C::S16_OFF + (C::S16_BUFS == 2 ? (jj & 1) * kBN : 0) + col0, r16);
         tmem_wait_ld();
         if (my_flag && rowvis) {
           const float sl2 = sig * kLog2e, ml = m_new * kLog2e;
