@@ -54,7 +54,10 @@ struct Cfg {
   static constexpr int P_BYTES = kBM * kBN * 2;
   static constexpr int OFF_Q = 0;  // tile t: Q8 at t*QT_BYTES, Q16 right after
   static constexpr int OFF_ST = NT * QT_BYTES;
-  static constexpr int OFF_P = OFF_ST + NS * STAGE_BYTES;  // tile t at + t*P_BYTES
+  // one stage (d = 256): a second K8 slot, so the next key's K8 is loaded
+  // while the softmax still re-derives from the current one
+  static constexpr int OFF_K8B = OFF_ST + NS * STAGE_BYTES;
+  static constexpr int OFF_P = OFF_K8B + (NS == 1 ? K8_BYTES : 0);  // tile t at + t*P_BYTES
   static constexpr int OFF_MISC = OFF_P + NT * P_BYTES;
   static constexpr int MISC_BYTES = 5120;
   static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
@@ -93,6 +96,8 @@ enum : int {
   M_EXP8 = 256,       // u8 [256] exp8 table: code of fl8(exp(x)) per code of x
   M_XCH = 512,        // f32 [2 tiles][2 halves][128 rows] values exchanged between a row's two threads
   M_XB = 2560,        // u32 [2 tiles][2 halves][128 rows] bits exchanged between a row's two threads
+  M_K8B_FULL = 4608,  // one stage: the second K8 slot landed
+  M_K8B_EMPTY = 4616, // one stage: the second K8 slot is free
 };
 
 struct Ctx {
@@ -298,6 +303,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     mbar_init(bar(M_Q_FULL), 1);
     mbar_init(bar(M_V_FULL), 1);
     mbar_init(bar(M_V_EMPTY), 1);
+    mbar_init(bar(M_K8B_FULL), 1);
+    mbar_init(bar(M_K8B_EMPTY), 1);
     *(volatile uint32_t*)(misc + M_ABORT) = 0u;
     fence_mbar_init();
   }
@@ -332,28 +339,40 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(qd + C::Q8_BYTES + c * kBM * 128, &p.tmQ16, bar(M_Q_FULL), c * 64, q0 + t * kBM, h, b);
       }
-      int uses0 = 0, uses1 = 0, uses2 = 0;
+      int uses0 = 0, uses1 = 0, uses2 = 0, uses3 = 0;
       uint32_t rel = 0u;  // releases waited for so far, one bit of parity per (tile, stage)
       if (C::NS == 1 && !kSweep) {
-        // one stage, filled in three parts with their own barriers: K8
-        // (KV_FULL / KV_EMPTY slot 0, free once the softmax has published
-        // the step), K16 (slot 1, free once the step's QK16 is done) and V
-        // (V_FULL / V_EMPTY, free once the step's P.V is done) -- so the
-        // next key's K16 lands long before its QK16, and only V waits for
-        // the P.V
+        // one stage, filled in parts with their own barriers: K8 in two
+        // slots by key parity (KV_FULL / KV_EMPTY and K8B_FULL / K8B_EMPTY,
+        // a slot free once the softmax has published its key's step), K16
+        // (slot 1 of KV_FULL / KV_EMPTY, free once the key's QK16 is done)
+        // and V (V_FULL / V_EMPTY, free once the key's P.V is done).  Order
+        // per key j: K16(j), K8(j + 1), V(j) -- each waits for an event
+        // earlier than the next one's, so K8 and K16 land a step ahead and
+        // only V waits for the P.V.
         const uint32_t st = sbase + C::OFF_ST;
-        for (int j = J0; j < J1 && !*cx.abort; ++j) {
-          const int u = j - J0, key0 = j * kBN;
-          if (u >= 1 && !wait_bar(cx, bar(M_KV_EMPTY), (u - 1) & 1)) break;
-          mbar_expect_tx(bar(M_KV_FULL), C::K8_BYTES);
+        const int nk = J1 - J0;
+        auto load_k8 = [&](int u) {
+          const uint32_t fb = (u & 1) ? bar(M_K8B_FULL) : bar(M_KV_FULL);
+          const uint32_t dst = (u & 1) ? sbase + C::OFF_K8B : st;
+          mbar_expect_tx(fb, C::K8_BYTES);
           for (int c = 0; c < D / C::F8_SWZ_ROW; ++c)
-            tma_load_4d(st + c * kBN * 128, &p.tmK8, bar(M_KV_FULL), c * C::F8_SWZ_ROW, key0, g, b);
-          uses0 = u + 1;
+            tma_load_4d(dst + c * kBN * 128, &p.tmK8, fb, c * C::F8_SWZ_ROW, (J0 + u) * kBN, g, b);
+          if (u & 1) uses3 = (u >> 1) + 1; else uses0 = (u >> 1) + 1;
+        };
+        if (nk > 0) load_k8(0);
+        for (int u = 0; u < nk && !*cx.abort; ++u) {
+          const int key0 = (J0 + u) * kBN;
           if (u >= 1 && !wait_bar(cx, bar(M_KV_EMPTY + 16), (u - 1) & 1)) break;
           mbar_expect_tx(bar(M_KV_FULL + 8), C::K16_BYTES);
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(st + C::K8_BYTES + c * kBN * 128, &p.tmK16, bar(M_KV_FULL + 8), c * 64, key0, g, b);
           uses1 = u + 1;
+          if (u + 1 < nk) {
+            const int v = u + 1;  // its slot held key v - 2
+            if (v >= 2 && !wait_bar(cx, (v & 1) ? bar(M_K8B_EMPTY) : bar(M_KV_EMPTY), ((v - 2) >> 1) & 1)) break;
+            load_k8(v);
+          }
           if (u >= 1 && !wait_bar(cx, bar(M_V_EMPTY), (u - 1) & 1)) break;
           mbar_expect_tx(bar(M_V_FULL), C::V_BYTES);
           for (int c = 0; c < D / 64; ++c)
@@ -393,6 +412,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         if (uses0 > 0) drain_wait(bar(M_KV_FULL), (uses0 - 1) & 1);
         if (uses1 > 0) drain_wait(bar(M_KV_FULL + 8), (uses1 - 1) & 1);
         if (uses2 > 0) drain_wait(bar(M_V_FULL), (uses2 - 1) & 1);
+        if (uses3 > 0) drain_wait(bar(M_K8B_FULL), (uses3 - 1) & 1);
         drain_wait(bar(M_Q_FULL), 0);
       }
     }
@@ -454,12 +474,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           if (i > 0) {
             ok = wait_bar(cx, bar(M_DEC), (i - 1) & 1);
             if (!ok) break;
-            mbar_arrive(bar(M_KV_EMPTY));  // K8 of key j - 1
+            mbar_arrive(((i - 1) & 1) ? bar(M_K8B_EMPTY) : bar(M_KV_EMPTY));  // K8 slot of key j - 1
           }
-          ok = wait_bar(cx, bar(M_KV_FULL), ph);
+          ok = wait_bar(cx, (i & 1) ? bar(M_K8B_FULL) : bar(M_KV_FULL), (uint32_t)(i >> 1) & 1u);
           if (!ok) break;
           tc_fence_after();
-          Mma<D>::qk8(tm + C::S8_OFF, qbase, kv(j));
+          Mma<D>::qk8(tm + C::S8_OFF, qbase, (i & 1) ? sbase + C::OFF_K8B : kv(j));
           mma_commit(bar(M_S_FULL));
           ok = wait_bar(cx, bar(M_KV_FULL + 8), ph);
           if (!ok) break;
@@ -676,7 +696,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       bool gmx_ok = all_full;  // group maxima still describe s8h (no fix-up, no hidden key)
       if (__any_sync(0xffffffffu, unc != 0u)) {
         if (unc) gmx_ok = false;
-        const uint8_t* sK8 = smem + C::OFF_ST + ((jt - J0) % C::NS) * C::STAGE_BYTES;
+        const uint8_t* sK8 = (C::NS == 1 && !kSweep && ((jt - J0) & 1))
+                                 ? smem + C::OFF_K8B  // the second K8 slot of the one-stage layout
+                                 : smem + C::OFF_ST + ((jt - J0) % C::NS) * C::STAGE_BYTES;
         for (;;) {
           const unsigned who = __ballot_sync(0xffffffffu, unc != 0u);
           if (!who) break;
