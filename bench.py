@@ -177,10 +177,19 @@ KERNEL_SOURCES = ["mixed_precision_flashattention_gb300/csrc/lamp_fwd.cu",
 
 
 def kernel_source_sha() -> str:
+    """Hash of the fused kernel's code: comments and blank lines do not count
+    (an edit of a comment leaves the compiled kernel, and so a capture of it,
+    unchanged)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, f), "rb").read())
+        src = open(os.path.join(ROOT, f), encoding="utf-8").read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for line in src.splitlines():
+            line = line.split("//", 1)[0].strip()
+            if line:
+                h.update(line.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -461,10 +461,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         ok = false;  // nothing more to issue
       }
       if (C::NS == 1 && !kSweep) {
-        // One K/V stage (d = 256, one query tile) in three parts (K8, K16,
-        // V), each handed back on its own: K8 once the softmax has published
-        // the step (its re-derivations read K8 until then), K16 once the
-        // step's QK16 is done, V after the step's P.V.  QK16(i) goes right
+        // One K/V stage (d = 256, one query tile) in three parts (K8 in two
+        // slots by key parity, K16, V), each handed back on its own: K8 once
+        // the softmax has published the step (its re-derivations read K8
+        // until then), K16 once the step's QK16 is done, V after the step's
+        // P.V.  QK16(i) goes right
         // after QK8(i), into the S16 buffer of parity i (the softmax may
         // still read the other one); P.V(i - 1) follows once P(i - 1) is in.
         static_assert(C::NS != 1 || (C::NT == 1 && C::S16_BUFS == 2), "one stage: one query tile, two S16 buffers");
