@@ -288,6 +288,7 @@ def main():
 
     # rank r holds its own shard of the job: the workload's shape with seed + r
     q, k, v = synth.make(w, seed=args.seed + rank)
+    config["inputs_sha256"] = synth.digest(q, k, v)  # of the generated float arrays
     if world > 1:
         config["shard"] = f"rank r of {world}: its own {w.batch} sequences (seed {args.seed} + r)"
 
@@ -364,6 +365,14 @@ def main():
     t_prep = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     t_main = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     ms, c = reduce_over_ranks(statistics.mean(t_step), cnt.cpu().numpy(), world, dev)
+    pct = np.percentile(np.array(t_step), [10, 50, 90]).tolist()
+    # the same steps with L2 left warm (no flush): information only
+    warm = []
+    for i in range(min(K, 20)):
+        step(ev[i])
+        warm.append(ev[i])
+    torch.cuda.synchronize()
+    warm_ms = statistics.median(e[0].elapsed_time(e[2]) for e in warm)
     ms_main = statistics.mean(t_main)
 
     # end to end through the public call on host buffers: pinned host in,
@@ -438,6 +447,7 @@ def main():
                      "mixed_tc_time_frac": t_tc / (ms_main * 1e-3),
                      "issue": _issue_roofline(w.name, ms_main, (clocks or {}).get("sm_mhz"))},
         "ms_main_kernel": ms_main, "ms_prepass": statistics.mean(t_prep), "wall_s": t_wall,
+        "ms_per_step_p10_p50_p90": pct, "ms_per_step_l2_warm": warm_ms,
         "stats": {n: int(c[i]) for i, n in enumerate(lamp.COUNTER_NAMES)},
         "subblock16_frac": float(c[6]) / max(1, c[4]),
         "tiles_0_1_2plus": [float(c[1]) / max(1, c[0]), float(c[2]) / max(1, c[0]), float(c[3]) / max(1, c[0])],
