@@ -358,6 +358,8 @@ def main():
         flush.zero_()
         step(ev[i])
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     clk.mark_end()
     t_wall = time.perf_counter() - t_wall
     clocks = clk.stop()
