@@ -32,7 +32,9 @@ std::mutex g_scratch_mu;
 
 // Device address of the array on the current device.  In host code the
 // array's name only stands in for the symbol; the address has to come from
-// cudaGetSymbolAddress with that device current (once per device).
+// cudaGetSymbolAddress with that device current (once per device, kept for
+// the life of the process: a cudaDeviceReset of that device would leave it
+// stale, so after a reset this entry point must not be used again).
 int scratch_on_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LAMP_ERR_CUDA;
@@ -53,7 +55,13 @@ extern "C" int lamp_attn_fwd_noalloc(const void* q, const void* k, const void* v
                                      lamp_stats* stats) {
   if (!shapes) return LAMP_ERR_INVALID_ARG;
   const size_t need = lamp_attn_workspace_bytes(shapes);
-  if (need == 0) return LAMP_ERR_INVALID_ARG;
+  if (need == 0) {
+    // the same status lamp_attn_fwd gives: shapes that are valid except for
+    // the head dimension are unsupported, anything else is an argument error
+    lamp_shapes probe = *shapes;
+    probe.head_dim = 128;
+    return lamp_attn_workspace_bytes(&probe) != 0 ? LAMP_ERR_UNSUPPORTED : LAMP_ERR_INVALID_ARG;
+  }
   if (need > (size_t)LAMP_NOALLOC_SCRATCH_BYTES) return LAMP_ERR_TOO_LARGE;
   void* scratch = nullptr;
   const int st = scratch_on_current_device(&scratch);

@@ -58,3 +58,48 @@ def test_noalloc_rejects_shapes_beyond_the_array():
     code, *_ = _call(lib.lamp_attn_fwd_noalloc, qd, kd, vd)
     assert code == lamp.LAMP_ERR_TOO_LARGE
     assert b"LAMP_NOALLOC_SCRATCH_BYTES" in lib.lamp_strerror(code)
+
+
+def test_noalloc_call_allocates_no_device_memory():
+    """After a first call (which loads the kernels and looks up the array's
+    address), a call on a non-default stream leaves the device's free
+    memory unchanged: nothing is allocated."""
+    lib = lamp.load()
+    q, k, v = synth.gen_outlier_sink(1, 512, 2, 1, 128, seed=54)
+    qd, kd, vd = to_device(q, k, v, "bf16")
+    B, N, Hq, d = qd.shape
+    out = torch.empty_like(qd)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=qd.device)
+    mb, cnt = lamp.new_stats(B, Hq, N)
+    s = torch.cuda.Stream()
+    sh = lamp.make_shapes(qd, kd, vd, out, stream=s)
+    st = lamp.LampStats()
+    st.mask, st.counters = mb.data_ptr(), cnt.data_ptr()
+
+    def call():
+        code = lib.lamp_attn_fwd_noalloc(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), out.data_ptr(),
+                                         lse.data_ptr(), ctypes.byref(sh), lamp.MASK["causal"],
+                                         ctypes.c_float(2.0 ** -8), ctypes.c_float(0.5), ctypes.byref(st))
+        s.synchronize()
+        return code
+
+    assert call() == lamp.LAMP_OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    assert call() == lamp.LAMP_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 >= free0, f"free device memory dropped by {free0 - free1} bytes"
+    assert int(cnt[9].item()) == 0
+
+
+def test_noalloc_unsupported_head_dim():
+    """A head dimension the kernels do not support gets the status
+    lamp_attn_fwd gives (LAMP_ERR_UNSUPPORTED), not an argument error."""
+    lib = lamp.load()
+    q, k, v = synth.gen_iid(1, 64, 1, 1, 96, seed=55)
+    qd, kd, vd = to_device(q, k, v, "bf16")
+    code_fwd, *_ = _call(lib.lamp_attn_fwd, qd, kd, vd)
+    code, *_ = _call(lib.lamp_attn_fwd_noalloc, qd, kd, vd)
+    assert code_fwd == lamp.LAMP_ERR_UNSUPPORTED
+    assert code == lamp.LAMP_ERR_UNSUPPORTED
