@@ -20,6 +20,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -106,13 +107,12 @@ class ClockSampler:
     def __init__(self, index=0):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"lamp_bench_clocks_{os.getpid()}.csv")
         self.t0 = self.t1 = None
 
     def start(self):
         """Start sampling; returns once the first sample is written (or after 5 s)."""
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -153,6 +153,7 @@ class ClockSampler:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) >= 10:
                 rows.append(parts)
+        os.remove(self.path)
         if not rows:
             return None
         inside = rows
@@ -264,11 +265,18 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--generator", default=None, choices=sorted(synth.GENERATORS),
+                    help="input generator in place of the workload's own (same shape)")
+    ap.add_argument("--parity-tiles", type=int, default=64,
+                    help="query tiles of the timed inputs checked against the oracle (0: none)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     w = synth.WORKLOADS[args.workload]
+    if args.generator is not None and args.generator != w.gen:
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}_{args.generator}", gen=args.generator)
     flops = w.flops()
     config = {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "heads_q": w.heads_q,
               "heads_kv": w.heads_kv, "head_dim": w.head_dim, "mask": w.mask, "window": w.window,
@@ -278,9 +286,10 @@ def main():
     if args.impl == "reference" and rank != 0:
         return  # the oracle arm runs on rank 0 only
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    want_parity = rank == 0 and args.impl == "lamp" and args.parity_tiles > 0
     pool = None
     ncores = os.cpu_count() or 1
-    if args.impl == "reference" or want_cpu:
+    if args.impl == "reference" or want_cpu or want_parity:
         # spawn the oracle's workers before any CUDA call, one BLAS thread each
         for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             os.environ[var] = "1"
@@ -363,6 +372,10 @@ def main():
     clk.mark_end()
     t_wall = time.perf_counter() - t_wall
     clocks = clk.stop()
+    if want_parity:  # outputs of the last timed step, for the parity check below
+        out_h = out.float().cpu().numpy().astype(np.float64)
+        lse_h = lse.cpu().numpy().astype(np.float64)
+        mask_h = mbytes.cpu().numpy()
     t_step = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
     t_prep = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     t_main = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
@@ -436,6 +449,8 @@ def main():
     f_pv = kv_steps * 2.0 * 128 * 64 * d
     f_rec = float(c[10] + c[11]) * 2.0 * 128 * 64 * d  # 16-bit products of every step, used or not
     f_rec_used = float(c[10]) * 2.0 * 128 * 64 * d
+    # tensor-core time of the issued work at the peaks: the fastest this
+    # kernel design could run on these inputs if the tensor pipe never idled
     t_tc = (f_qk8 / (fp8_peak * 1e12) + (f_pv + f_rec) / (bf16_peak * 1e12))
     res = {
         "metric": METRIC, "value": flops / (ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "n_gpus": world,
@@ -447,6 +462,7 @@ def main():
                      "frac": achieved / fp8_peak, "traffic": _traffic(w.name),
                      "kernel": "lamp_fwd_kernel", "peak_basis": f"2 x {peak_src} bf16 burst {bf16_peak} (dense FP8:BF16 = 2)",
                      "mixed_tc_time_frac": t_tc / (ms_main * 1e-3),
+                     "ceiling_fp8_frac": flops / t_tc / 1e12 / fp8_peak,
                      "issue": _issue_roofline(w.name, ms_main, (clocks or {}).get("sm_mhz"))},
         "ms_main_kernel": ms_main, "ms_prepass": statistics.mean(t_prep), "wall_s": t_wall,
         "ms_per_step_p10_p50_p90": pct, "ms_per_step_l2_warm": warm_ms,
@@ -468,6 +484,17 @@ def main():
         tcpu = run_cpu_oracle(pool, tasks)
         res["cpu_baseline"] = {"value": sflops / tcpu / 1e12, "unit": "TFLOP/s", "cores": ncores, "kind": "oracle",
                                "sample": f"{sum(len(x[3]) for x in tasks)} query tiles of {w.name}, {tcpu:.1f} s"}
+    if want_parity:
+        from tests import sampled_parity as sp
+        tiles = sp.sample_tiles(w.batch, w.heads_q, w.seqlen, args.parity_tiles, seed=args.seed)
+        ptasks, pkeys = sp.make_tasks(q, k, v, tiles, bf16=w.dtype == "bf16", heads_q=w.heads_q,
+                                      heads_kv=w.heads_kv, mask=w.mask, window=w.window, delta=args.delta,
+                                      tau=args.tau, out_dtype=w.dtype)
+        presults = pool.map(sp.oracle_task, ptasks)
+        par = sp.compare(presults, pkeys, out_h, lse_h, mask_h, w.dtype, w.seqlen, w.mask, w.window)
+        par["sample"] = (f"{par['tiles']} query tiles (64 rows, all their keys) of the last timed step's "
+                         f"inputs and outputs, seed {args.seed}")
+        res["parity"] = par
     if pool is not None:
         pool.close()
     if rank == 0:

@@ -163,8 +163,11 @@ size_t lamp_attn_workspace_bytes(const lamp_shapes* shapes);
  * cudaMalloc, cudaFree or other allocating call is made.
  *
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress with that device current); make that first call
- * before any stream capture.  All calls share the array and it keeps the
+ * (cudaGetSymbolAddress with that device current) and keeps it for the life
+ * of the process; make that first call before any stream capture, and do
+ * not call this entry point again after a cudaDeviceReset of that device
+ * (the kept address would be stale).  Status codes as lamp_attn_fwd
+ * (LAMP_ERR_UNSUPPORTED for a head_dim other than 64, 128, 256).  All calls share the array and it keeps the
  * last call's contents (each call clears what must start at zero); calls
  * whose work overlaps on the GPU race on it and must be serialised.
  */
@@ -265,6 +268,11 @@ void lamp_exp8_table(uint8_t out[256]);
  *   which 4: out[i] = fl8(exp(x)) as the fused kernel computes it, for the
  *            E4M3 code a[i] of x <= 0 (a: uint8[d]; b: any non-NULL device
  *            pointer, unused); d = count, 1..65536.
+ *   which 5: out[i] = x8 = fl8(S8 - m) as the fused kernel's P8 path
+ *            computes it (f16 difference, then E4M3 rounding), for the E4M3
+ *            codes a[i] of S8 and b[i] of m (a, b: uint8[d]); d = count,
+ *            1..65536.
+ *   which 6: as 5, through the fp32 difference the detector uses.
  * a, b: DEVICE, row-major as listed; out: DEVICE float32, row-major.
  * Returns LAMP_OK or an error code after synchronising `stream`.
  */

@@ -5,7 +5,9 @@
 //   which 1: S = A . B^T,  A [128 x D], B [64 x D] BF16,          out [128 x 64]
 //   which 2: O = P . V,    P [128 x 64], V [64 x D] FP16,         out [128 x D]
 // and the scalar helpers of the fused kernel: which 3 the exact 8-bit
-// re-derivation, which 4 the 8-bit exponential P8 = fl8(e^x).
+// re-derivation, which 4 the 8-bit exponential P8 = fl8(e^x), which 5 and 6
+// the 8-bit difference x8 = fl8(S8 - m) (5: through the f16 difference the
+// P8 path uses, 6: through the fp32 difference the detector uses).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -103,6 +105,30 @@ __global__ void lamp_exp8_selftest_kernel(const uint8_t* codes, float* out, int 
   out[i] = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
 }
 
+// out[i] = x8 = fl8(S8 - m) for the E4M3 codes s8[i] of S8 and m8[i] of m,
+// as the fused kernel computes it: via_f16 -- the f16x2 difference of the
+// two values rounded once more to E4M3 (the P8 path); otherwise the fp32
+// difference (exact for E4M3 operands) rounded to E4M3 (the detector)
+__global__ void lamp_x8_selftest_kernel(const uint8_t* s8, const uint8_t* m8, float* out, int n, bool via_f16) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint32_t sh = e4m3x2_to_f16x2((uint16_t)((uint32_t)s8[i] * 0x0101u));
+  const uint32_t mh = e4m3x2_to_f16x2((uint16_t)((uint32_t)m8[i] * 0x0101u));
+  __half2 sv, mv;
+  memcpy(&sv, &sh, 4);
+  memcpy(&mv, &mh, 4);
+  uint32_t code;
+  if (via_f16) {
+    // the kernel holds m as a float and converts it with __float2half2_rn
+    const __half2 mk = __float2half2_rn(__low2float(mv));
+    code = cvt_e4m3x2_f16x2(__hsub2(sv, mk)) & 0xFFu;
+  } else {
+    code = cvt_e4m3x2(0.0f, __low2float(sv) - __low2float(mv)) & 0xFFu;
+  }
+  const uint32_t h = e4m3x2_to_f16x2((uint16_t)code);
+  out[i] = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
 template <int D>
 static cudaError_t run_selftest(int which, const void* a, const void* b, float* out, unsigned int* status,
                                 cudaStream_t st) {
@@ -116,7 +142,7 @@ static cudaError_t run_selftest(int which, const void* a, const void* b, float* 
 }  // namespace lamp
 
 extern "C" int lamp_selftest(int which, const void* a, const void* b, float* out, int d, void* stream) {
-  if (!a || !b || !out || which < 0 || which > 4) return LAMP_ERR_INVALID_ARG;
+  if (!a || !b || !out || which < 0 || which > 6) return LAMP_ERR_INVALID_ARG;
   if (which >= 3 ? (d < 1 || d > 65536) : (d != 64 && d != 128 && d != 256)) return LAMP_ERR_UNSUPPORTED;
   int dev = 0, maj = 0, min = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LAMP_ERR_CUDA;
@@ -133,6 +159,10 @@ extern "C" int lamp_selftest(int which, const void* a, const void* b, float* out
     e = cudaGetLastError();
   } else if (which == 4) {
     lamp::lamp_exp8_selftest_kernel<<<(d + 255) / 256, 256, 0, st>>>((const uint8_t*)a, out, d);
+    e = cudaGetLastError();
+  } else if (which == 5 || which == 6) {
+    lamp::lamp_x8_selftest_kernel<<<(d + 255) / 256, 256, 0, st>>>((const uint8_t*)a, (const uint8_t*)b, out, d,
+                                                                   which == 5);
     e = cudaGetLastError();
   } else {
     e = d == 64    ? lamp::run_selftest<64>(which, a, b, out, status, st)

@@ -264,9 +264,10 @@ def exp8_table() -> bytes:
 def selftest(which: int, a, b, d: int):
     """Run a device building-block check; returns the float32 result
     (which 3: the exact 8-bit re-derivation of a[i] * 2^-18 * b[0], d values;
-    which 4: fl8(e^x) for the E4M3 codes a[i], d values)."""
+    which 4: fl8(e^x) for the E4M3 codes a[i], d values; which 5 / 6:
+    fl8(S8 - m) for the E4M3 codes a[i] of S8 and b[i] of m, d values)."""
     lib = load()
-    if which in (3, 4):
+    if which in (3, 4, 5, 6):
         out = torch.full((d,), float("nan"), dtype=torch.float32, device=a.device)
     else:
         out = torch.full((128, d if which == 2 else 64), float("nan"), dtype=torch.float32, device=a.device)

@@ -63,6 +63,36 @@ def fp64_attention(q, k, v, *, mask="causal", window=0, scale=None):
     return out, lse
 
 
+def fp64_attention_rows(q, k, v, rows, *, b=0, h=0, mask="causal", window=0, scale=None):
+    """fp64_attention for the given query rows of head (b, h) only: out
+    [len(rows), d] and lse [len(rows)], the textbook softmax of the visible
+    keys (rows past the end get out 0, LSE -inf)."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    n, d = q.shape[1], q.shape[3]
+    g = h // (q.shape[2] // k.shape[2])
+    sigma = (1.0 / np.sqrt(float(d))) if scale is None else float(scale)
+    rows = np.asarray(rows)
+    out = np.zeros((rows.size, d))
+    lse = np.full(rows.size, -np.inf)
+    cols = np.arange(n)
+    for i, r in enumerate(rows):
+        if r >= n:
+            continue
+        vis = np.ones(n, bool)
+        if mask == "causal":
+            vis = cols <= r
+        elif mask == "sliding":
+            vis = (cols <= r) & (cols > r - window)
+        s = sigma * (k[b, vis, g, :] @ q[b, r, h, :])
+        mx = s.max()
+        p = np.exp(s - mx)
+        out[i] = (p @ v[b, vis, g, :]) / p.sum()
+        lse[i] = mx + np.log(p.sum())
+    return out, lse
+
+
 def bf16_attention(q, k, v, **kw):
     """fp64_attention on BF16-rounded q, k, v (plain 16-bit attention)."""
     return fp64_attention(bf16_round(q), bf16_round(k), bf16_round(v), **kw)
@@ -140,5 +170,5 @@ def e4m3_sorted_values():
     return np.array(vals)
 
 
-__all__ = ["fp64_attention", "bf16_attention", "lamp8_rowloop",
+__all__ = ["fp64_attention", "fp64_attention_rows", "bf16_attention", "lamp8_rowloop",
            "e4m3_sorted_values", "e4m3_encode"]

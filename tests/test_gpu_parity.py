@@ -99,6 +99,14 @@ def test_all16_matches_fp64_on_iid():
     _compare(q, k, v, "bf16", out_dtype="fp32", force="all16", fp64_gate=True)
 
 
+def test_all16_matches_fp64_on_outliers():
+    """Forced 16-bit on the outlier-channel + sink-key generator: within
+    2e-3 / 1e-3 of FP64 attention on the same bf16 inputs (the case that
+    separates an fp16 P16 from a bf16 one, see the oracle pin)."""
+    q, k, v = synth.gen_outlier_sink(1, 512, 4, 1, 128, seed=21)
+    _compare(q, k, v, "bf16", out_dtype="fp32", force="all16", fp64_gate=True)
+
+
 def test_qwen3_8b_full_size_sampled():
     """The bench's launch (B4 N4096 Hq32 Hkv8 d128 causal bf16) checked on
     sampled query tiles the oracle computes one by one."""

@@ -237,3 +237,24 @@ def test_exp8_arithmetic_exact(lamp):
     want = F.exp8(x)
     bad = np.nonzero(got != want)[0]
     assert bad.size == 0, [(hex(codes[i]), x[i], got[i], want[i]) for i in bad[:5]]
+
+
+@pytest.mark.parametrize("which", [5, 6], ids=["f16_difference", "fp32_difference"])
+def test_x8_exhaustive(lamp, which):
+    """x8 = fl8(S8 - m) as the fused kernel computes it -- the P8 path takes
+    the f16 difference of the two E4M3 values and rounds it to E4M3 again
+    (which 5), the detector takes the fp32 difference (which 6) -- equals the
+    single rounding of the exact difference for every pair of finite E4M3
+    codes (254 x 254 pairs; the kernel only ever has S8 <= m, the test
+    covers both signs)."""
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    s8c, m8c = np.meshgrid(codes, codes, indexing="ij")
+    s8c, m8c = s8c.ravel(), m8c.ravel()
+    got = lamp.selftest(which, torch.from_numpy(s8c).cuda(), torch.from_numpy(m8c).cuda(),
+                        len(s8c)).cpu().numpy().astype(np.float64)
+    want = F.e4m3_round(F.E4M3_TABLE[s8c] - F.E4M3_TABLE[m8c])
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(F.E4M3_TABLE[s8c[i]], F.E4M3_TABLE[m8c[i]], got[i], want[i]) for i in bad[:5]]
+    # the same on the subset the kernel meets (S8 <= m): x8 <= 0, so P8 = exp8(x8) <= 1
+    sub = F.E4M3_TABLE[s8c] <= F.E4M3_TABLE[m8c]
+    assert np.all(got[sub] <= 0.0)

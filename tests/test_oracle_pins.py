@@ -70,6 +70,22 @@ def test_fp64_attention_against_scalar_loop():
                 assert abs(lse[0, h, r] - (mx + math.log(den))) < 1e-12
 
 
+def test_all16_outlier_workload_pins_p16_format():
+    """Forcing every sub-block to 16 bits on the outlier-channel + sink-key
+    generator stays within 2e-3 (out) / 1e-3 (LSE) of FP64 attention on the
+    same bf16 inputs.  This case separates the two 16-bit readings of the
+    exponential: with P16 in fp16 (the oracle's reading, 2^-11 steps) the
+    error is 8e-4, with P16 in bf16 (2^-8 steps) it is 5e-3, so an oracle
+    that rounded P16 to bf16 fails here although the i.i.d. case above may
+    not show it."""
+    q, k, v = synth.gen_outlier_sink(1, 512, 4, 1, 128, seed=21)
+    qb, kb, vb = _bf16(q), _bf16(k), _bf16(v)
+    r = oracle.lamp_forward(qb, kb, vb, force="all16", out_dtype="fp32")
+    o64, l64 = oracle.fp64_attention(qb, kb, vb)
+    assert np.abs(r.out - o64).max() <= 2e-3
+    assert np.abs(r.lse - l64).max() <= 1e-3
+
+
 def test_all16_equals_plain_16bit_attention():
     """Forcing every sub-block to 16 bits is 16-bit attention: within the
     tolerance of FP64 attention on the 16-bit inputs (iid N(0,1))."""
@@ -194,3 +210,19 @@ def test_ragged_lengths(n):
     assert np.abs(r.out - o64).max() <= 2e-3
     assert r.counters[C_STRIPS] == sum(min(16, n - 16 * s) > 0 for s in range((n + 15) // 16)) + \
         (0 if n <= 64 else sum(1 for s in range(4) if 64 + 16 * s < n))
+
+
+def test_fp64_attention_rows_equals_full():
+    """The row-restricted FP64 attention (used for sampled parity of
+    full-size runs) gives the rows of the full-head computation, which is
+    itself pinned to a scalar loop above."""
+    rng = np.random.default_rng(9)
+    q = rng.standard_normal((2, 150, 4, 16))
+    k = rng.standard_normal((2, 150, 2, 16))
+    v = rng.standard_normal((2, 150, 2, 16))
+    for mask, window in (("causal", 0), ("none", 0), ("sliding", 40)):
+        out, lse = oracle.fp64_attention(q, k, v, mask=mask, window=window)
+        rows = np.array([0, 1, 63, 64, 100, 149])
+        o, l = oracle.fp64_attention_rows(q, k, v, rows, b=1, h=3, mask=mask, window=window)
+        assert np.allclose(o, out[1, rows, 3], atol=1e-13, rtol=0)
+        assert np.allclose(l, lse[1, 3, rows], atol=1e-13, rtol=0)
