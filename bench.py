@@ -447,7 +447,7 @@ def main():
     kv_steps *= B * Hq
     f_qk8 = kv_steps * 2.0 * 128 * 64 * d
     f_pv = kv_steps * 2.0 * 128 * 64 * d
-    f_rec = float(c[10] + c[11]) * 2.0 * 128 * 64 * d  # 16-bit products of every step, used or not
+    f_rec = float(c[10] + c[11]) * 2.0 * 128 * 64 * d  # 16-bit products issued: used, or ahead and not needed
     f_rec_used = float(c[10]) * 2.0 * 128 * 64 * d
     # tensor-core time of the issued work at the peaks: the fastest this
     # kernel design could run on these inputs if the tensor pipe never idled

@@ -79,11 +79,23 @@ enum {
   LAMP_CNT_STAGE1 = 5,      /* sub-blocks passing the first stage */
   LAMP_CNT_FLAGGED = 6,     /* sub-blocks recomputed in 16 bits */
   LAMP_CNT_SAT = 7,         /* visible logits with |S8| = 448 */
-  LAMP_CNT_FIXUPS = 8,      /* logits re-derived exactly (near an 8-bit rounding boundary) */
+  LAMP_CNT_FIXUPS = 8,      /* logits re-derived exactly (near an 8-bit rounding boundary,
+                               where the two candidate codes could differ in a result) */
   LAMP_CNT_STATUS = 9,      /* device-side status (lamp_status), 0 = ok */
-  LAMP_CNT_RECOMP_STEPS = 10, /* 128x64 kernel steps whose 16-bit recompute was used */
-  LAMP_CNT_SPEC_WASTE = 11, /* 128x64 kernel steps whose 16-bit products, computed
-                               ahead of the decision, were not needed */
+  LAMP_CNT_RECOMP_STEPS = 10, /* 128-query x 64-key kernel steps with a flagged
+                                 sub-block: their 16-bit products are computed and used */
+  LAMP_CNT_SPEC_WASTE = 11, /* steps whose 16-bit products were computed ahead of the
+                               decision (the first step of a 128-query tile, or the
+                               step before had a flagged sub-block) but not needed;
+                               16-bit QK work issued = RECOMP_STEPS + this */
+  LAMP_CNT_RECOMP_LATE = 12, /* steps with a flagged sub-block whose 16-bit products were
+                                computed only after the decision (the step before had
+                                none) */
+  LAMP_CNT_GUARD_RESOLVED = 13, /* logits near an 8-bit rounding boundary whose two
+                                   candidate codes give the same P8, flag and
+                                   saturation results (no exact re-derivation needed) */
+  LAMP_CNT_FIXUPS_MAX = 14, /* of LAMP_CNT_FIXUPS: logits re-derived because they could
+                               be their row's maximum in the tile */
   LAMP_NUM_COUNTERS = 16
 };
 
@@ -234,7 +246,8 @@ size_t lamp_attn_host_buffer_bytes(const lamp_shapes* shapes);
  *   hist      DEVICE uint64 [ntau][4]: visited tiles, tiles with 0, 1, 2+
  *             flagged sub-blocks at taus[i] (zeroed, then written).
  *   stats     optional; counters as for lamp_attn_fwd except the flag-based
- *             ones (HIST0..2, FLAGGED, RECOMP_STEPS, SPEC_WASTE stay 0);
+ *             ones (HIST0..2, FLAGGED, RECOMP_STEPS, SPEC_WASTE, RECOMP_LATE
+ *             stay 0);
  *             stats->mask is not written.
  * Asynchronous on shapes->stream; errors as lamp_attn_fwd.
  */

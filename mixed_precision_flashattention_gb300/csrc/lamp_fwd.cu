@@ -9,16 +9,20 @@
 //   warps 8t..8t+7  softmax of tile t: two threads per query row (warps
 //              8t+w and 8t+4+w hold TMEM lanes 32w.. for key columns 0-31
 //              and 32-63 of each step).  Per step: 8-bit logits S8 (with an
-//              exactness guard), running max, the two-stage detector,
-//              sub-block flags, mask byte + histogram, FP16 P (P8 from a
-//              table of exact 8-bit exponentials, or P16 for flagged rows),
-//              O rescale in TMEM, the row sum l in registers.
-//   warp 8*NT  TMA producer: Q8/Q16 of every tile once, then K8/K16/V16
-//              per step into a ring of stages.
-//   warp 8*NT+1  TMEM owner and MMA issuer: S = Q8 K8^T (kind::f8f6f4),
-//              S16 = Q16 K16^T (kind::f16, into the same TMEM columns once
-//              S8 has been read, only when a sub-block of the step is
-//              flagged), O += P V16 (kind::f16, V MN-major).
+//              exactness guard: two candidate roundings per logit, settled
+//              by a cheap check or an exact integer re-derivation), running
+//              max, the two-stage detector, sub-block flags, mask byte +
+//              histogram, FP16 P (P8 = fl8(e^x8) computed with an fp32 ex2
+//              and one E4M3 rounding, or P16 for the rows of flagged
+//              sub-blocks), O rescale in TMEM, the row sum l in registers.
+//   warp 8*NT  TMA producer: Q (Q16, and Q8 for fp32 q) of every tile once,
+//              then K8/K16/V16 per step into a ring of stages.
+//   warp 8*NT+1+t  MMA issuer of tile t (the first one also owns TMEM):
+//              S = Q8 K8^T (kind::f8f6f4) into the S8 buffer; S16 = Q16 K16^T
+//              (kind::f16, BF16) into its own S16 buffer, only for steps with
+//              a flagged sub-block -- issued ahead of the decision for the
+//              first step and after a flagged step, else once the decision
+//              is published; O += P V16 (kind::f16, V MN-major).
 //
 // The method follows "LampAttention: Look-Ahead Mixed-Precision
 // FlashAttention for Dedicated Accelerators" (abstract: 8-bit key-query
@@ -59,7 +63,7 @@ struct Cfg {
   static constexpr int OFF_K8B = OFF_ST + NS * STAGE_BYTES;
   static constexpr int OFF_P = OFF_K8B + (NS == 1 ? K8_BYTES : 0);  // tile t at + t*P_BYTES
   static constexpr int OFF_MISC = OFF_P + NT * P_BYTES;
-  static constexpr int MISC_BYTES = 5120;
+  static constexpr int MISC_BYTES = 9216;
   static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
   // TMEM columns per tile (fp32): O (d values), the 64-column S8 buffer and
   // the 64-column S16 buffer.  QK16 of a step is computed ahead, while the
@@ -98,6 +102,9 @@ enum : int {
   M_XB = 2560,        // u32 [2 tiles][2 halves][128 rows] bits exchanged between a row's two threads
   M_K8B_FULL = 4608,  // one stage: the second K8 slot landed
   M_K8B_EMPTY = 4616, // one stage: the second K8 slot is free
+  M_ANY = 4624,       // u8 [2 tiles][2 step parities]: the step has a flagged sub-block
+  M_XLH = 5120,       // f32x2 [2 tiles][2 halves][128 rows] bounds of the tile max exchanged
+  M_RCNT = 4632,      // u32 [2 tiles][3]: recompute steps used, computed ahead unused, computed late
 };
 
 struct Ctx {
@@ -153,6 +160,12 @@ __device__ __forceinline__ __half2 as_half2(uint32_t u) {
   __half2 r;
   memcpy(&r, &u, 4);
   return r;
+}
+
+__device__ __forceinline__ uint32_t as_u32(__half2 h) {
+  uint32_t u;
+  memcpy(&u, &h, 4);
+  return u;
 }
 
 __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
@@ -469,6 +482,33 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         // after QK8(i), into the S16 buffer of parity i (the softmax may
         // still read the other one); P.V(i - 1) follows once P(i - 1) is in.
         static_assert(C::NS != 1 || (C::NT == 1 && C::S16_BUFS == 2), "one stage: one query tile, two S16 buffers");
+        // QK16(i) is issued right after QK8(i) for the first step and when
+        // step i - 1 had a flagged sub-block, else once DEC(i) says step i
+        // has one (the softmax follows the same rule); a step without flags
+        // hands its K16 slot back without one.
+        auto any_of = [&](int i) { return *(volatile uint8_t*)(misc + M_ANY + (i & 1)) != 0; };
+        auto qk16 = [&](int i) {  // K16 of key jlo + i is in its slot
+          // one barrier per S16 buffer: a single one could complete twice
+          // (QK16(i), QK16(i + 1)) before the softmax waits for QK16(i),
+          // and a parity wait cannot tell those phases apart
+          Mma<D>::qk16(tm + C::S16_OFF + (i & 1) * kBN, qbase + C::Q8_BYTES, kv(jlo + i) + C::K8_BYTES);
+          mma_commit(bar(M_S16_FULL + 8 * (i & 1)));
+          mma_commit(bar(M_KV_EMPTY + 16));  // K16 of key jlo + i
+        };
+        // step i decided: its QK16 now, or its K16 slot back unused -- in
+        // both cases only once the slot's copy has landed (the producer
+        // re-arms the slot's barrier for the next key when it gets it back)
+        auto decided = [&](int i) -> bool {
+          if (!wait_bar(cx, bar(M_KV_FULL + 8), (uint32_t)(jlo + i - J0) & 1u)) return false;
+          if (any_of(i)) {
+            tc_fence_after();
+            qk16(i);
+          } else {
+            mbar_arrive(bar(M_KV_EMPTY + 16));
+          }
+          return true;
+        };
+        bool spec = true;  // QK16 of the current step is issued ahead of its decision (always the first)
         for (int i = 0; ok && i < n; ++i) {
           const int j = jlo + i;
           const uint32_t ph = (uint32_t)(j - J0) & 1u;
@@ -476,21 +516,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
             ok = wait_bar(cx, bar(M_DEC), (i - 1) & 1);
             if (!ok) break;
             mbar_arrive(((i - 1) & 1) ? bar(M_K8B_EMPTY) : bar(M_KV_EMPTY));  // K8 slot of key j - 1
+            if (!spec) ok = decided(i - 1);
+            if (!ok) break;
+            spec = any_of(i - 1);
           }
           ok = wait_bar(cx, (i & 1) ? bar(M_K8B_FULL) : bar(M_KV_FULL), (uint32_t)(i >> 1) & 1u);
           if (!ok) break;
           tc_fence_after();
           Mma<D>::qk8(tm + C::S8_OFF, qbase, (i & 1) ? sbase + C::OFF_K8B : kv(j));
           mma_commit(bar(M_S_FULL));
-          ok = wait_bar(cx, bar(M_KV_FULL + 8), ph);
-          if (!ok) break;
-          tc_fence_after();
-          // one barrier per S16 buffer: a single one could complete twice
-          // (QK16(i), QK16(i + 1)) before the softmax waits for QK16(i),
-          // and a parity wait cannot tell those phases apart
-          Mma<D>::qk16(tm + C::S16_OFF + (i & 1) * kBN, qbase + C::Q8_BYTES, kv(j) + C::K8_BYTES);
-          mma_commit(bar(M_S16_FULL + 8 * (i & 1)));
-          mma_commit(bar(M_KV_EMPTY + 16));  // K16 of key j
+          if (spec) {
+            ok = wait_bar(cx, bar(M_KV_FULL + 8), ph);
+            if (!ok) break;
+            tc_fence_after();
+            qk16(i);
+          }
           if (i > 0) {
             ok = wait_bar(cx, bar(M_P_FULL), (i - 1) & 1);
             if (ok) ok = wait_bar(cx, bar(M_V_FULL), (ph ^ 1u));
@@ -501,6 +541,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
             mma_commit(bar(M_V_EMPTY));  // V of key j - 1
           }
         }
+        if (ok) ok = wait_bar(cx, bar(M_DEC), (n - 1) & 1);
+        if (ok && !spec) ok = decided(n - 1);
         if (ok) ok = wait_bar(cx, bar(M_P_FULL), (n - 1) & 1);
         if (ok) ok = wait_bar(cx, bar(M_V_FULL), (uint32_t)(jlo + n - 1 - J0) & 1u);
         if (ok) {
@@ -510,10 +552,33 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         }
         ok = false;
       }
+      // The 16-bit products of step i are computed only if the step needs
+      // them: ahead of its decision for the first step and when step i - 1
+      // had a flagged sub-block (flags come in runs, so the recompute then
+      // finds them ready), else once the decision (DEC(i)) says so.  The
+      // softmax applies the same rule, so both sides count the same S16
+      // phases.
+      auto any_of = [&](int i) {  // the decision of step i, published before DEC(i)
+        return *(volatile uint8_t*)(misc + M_ANY + 2 * t + (i & 1)) != 0;
+      };
+      auto qk16 = [&](int i) {
+        Mma<D>::qk16(tm + C::S16_OFF, qbase + C::Q8_BYTES, kv(jlo + i) + C::K8_BYTES);
+        mma_commit(bar(M_S16_FULL + 8 * t));
+      };
+      bool spec = true;  // QK16 of the current step is issued ahead of its decision (always the first)
       for (int i = 0; ok && i < n; ++i) {
         const int j = jlo + i;
-        if (i > 0) ok = wait_bar(cx, bar(M_DEC + 8 * t), (i - 1) & 1);
-        if (ok) ok = wait_bar(cx, bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1);
+        if (i > 0) {
+          ok = wait_bar(cx, bar(M_DEC + 8 * t), (i - 1) & 1);
+          if (!ok) break;
+          const bool prev = any_of(i - 1);
+          if (prev && !spec) {  // step i - 1 decided to recompute: its products now
+            tc_fence_after();
+            qk16(i - 1);
+          }
+          spec = prev;
+        }
+        ok = wait_bar(cx, bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1);
         if (!ok) break;
         tc_fence_after();
         Mma<D>::qk8(tm + C::S8_OFF, qbase, kv(j));
@@ -524,8 +589,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           tc_fence_after();
           pv(i - 1);
         }
-        Mma<D>::qk16(tm + C::S16_OFF, qbase + C::Q8_BYTES, kv(j) + C::K8_BYTES);
-        mma_commit(bar(M_S16_FULL + 8 * t));
+        if (spec) qk16(i);
+      }
+      if (ok) ok = wait_bar(cx, bar(M_DEC + 8 * t), (n - 1) & 1);
+      if (ok && any_of(n - 1) && !spec) {
+        tc_fence_after();
+        qk16(n - 1);
       }
       if (ok) ok = wait_bar(cx, bar(M_P_FULL + 8 * t), (n - 1) & 1);
       if (ok) {
@@ -583,7 +652,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     // exactness guard: |A_tc - A| * sigma <= gq * (max ||k8|| + 2^-6)
     const float gq = p.guard * p.sigma_f * (nq + 0x1p-6f), satq = p.sigma_f * nq * (1.0f + p.guard);
     uint32_t c_h0 = 0, c_h1 = 0, c_h2 = 0, c_strips = 0, c_st1 = 0, c_fl = 0, c_sat = 0, c_fix = 0,
-             c_rec = 0, c_spec = 0;  // per-thread counts (a CTA sees at most 2^21 logits per thread slot)
+             c_res = 0, c_fmax = 0;  // per-thread counts (a CTA sees at most 2^21 logits per thread slot)
+    volatile uint32_t* rcnt = (volatile uint32_t*)(misc + M_RCNT) + 3 * tt;  // thread t == 0, hf == 0 only
+    if (t == 0 && hf == 0) rcnt[0] = rcnt[1] = rcnt[2] = 0u;
+    // S16 phases of the tile so far, and whether this step's QK16 was
+    // issued ahead of the decision: for the first step, and when the step
+    // before had a flagged sub-block (the MMA warp follows the same rule)
+    uint32_t n16 = 0u;
+    bool prev_any = true;
     const int qtile = (q0 + tt * kBM) / kBN + (rw >> 1);  // 64-row query tile of this warp
     // this query tile's row of the mask, or of the tau-sweep records
     uint8_t* mrow = nullptr;
@@ -629,35 +705,38 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
 #pragma unroll
         for (int c = 0; c < NC; ++c) a32[c] = 0u;
       }
-      // S8 = fl8(A sigma) is certain unless y = A_tc sigma lies within G of an
-      // E4M3 rounding boundary (the roundings of y -+ G then differ).  Of
-      // those, only logits that can change m, P8, the detector or the
-      // saturation count need the exact value: m (the running max before
+      // S8 = fl8(A sigma) is one of the E4M3 values from cl = fl8(y - G) to
+      // ch = fl8(y + G) (y = A_tc sigma, G bounds the tensor core's error),
+      // so it is certain when the two agree -- almost always.  Of the
+      // others, only logits that can change m, P8, the detector or the
+      // saturation count may need the exact value: m (the running max before
       // this tile) is exact and <= the new max, and a logit whose largest
-      // possible value fl8(y + G) is <= m - 6.75 rounds x8 to <= -7 (P8 = 0,
-      // below any delta > 0) and is not the maximum.  With delta = 0, or when
-      // the tile can reach the 8-bit limit, all count.  A group of 8 logits
-      // is looked at only if one of them is uncertain and its largest S8 is
-      // close enough to m: with S8 the lower rounding, y - G is at most S8
-      // plus half a gap (<= |S8|/16 + 2^-10), and one more rounding of
-      // y + G adds at most |.|/16 + 2^-10, so the exact values are at most
-      // S8 + 0.13 |S8| + 2.2 G + 2^-8: below m - 6.75 nothing in it counts.
-      uint32_t s8h[NC / 2];  // S8 pairs as f16x2 (exact)
+      // possible value ch is <= m - 6.75 rounds x8 to <= -7 (P8 = 0, below
+      // any delta > 0) and is not the maximum.  With delta = 0, or when the
+      // tile can reach the 8-bit limit, all count.  A group of 8 logits is
+      // looked at only if one of them is uncertain and its largest cl is
+      // close enough to m: with cl the lower rounding, y - G is at most cl
+      // plus half a gap (<= |cl|/16 + 2^-10), and one more rounding of y + G
+      // adds at most |.|/16 + 2^-10, so the exact values are at most
+      // cl + 0.13 |cl| + 2.2 G + 2^-8: below m - 6.75 nothing in it counts.
+      // Those uncertain logits are resolved once the tile maximum is known.
+      uint32_t s8h[NC / 2];  // S8 pairs as f16x2 (exact values; cl until resolved)
       uint32_t gmx[NC / 8];  // per group of 8: max of the pairs (f16x2)
-      uint32_t unc = 0u;     // logits to re-derive exactly
+      uint32_t unc = 0u;     // visible logits whose candidates differ and that may matter
+      uint32_t hmx = 0xFC00FC00u;  // f16x2 max of their high candidates ch (-inf: none)
+      const float2 gp = make_float2(G, G);
       {
         // delta = 0 (first stage off): stage 1 holds for every visible entry,
-        // so besides the logits near m only those whose two roundings lie on
-        // both sides of +tau_abs or -tau_abs can move the flag (the tile-max
-        // test and the negative scan); the sweep pass needs the largest |S8|
-        // and keeps every uncertain logit
+        // so besides the logits near m only those whose candidates lie on
+        // both sides of +tau_abs or -tau_abs can move the flag; the sweep
+        // pass with delta = 0 needs every |S8|
         const bool tsplit = kNoStage1 && T > 0.0f;
         const float thr = (satp || (kSweep && dcode == 0u)) ? -INFINITY : m - 6.75f;
         const __half2 lthr = __half2half2(__float2half_rd(thr));
-        const float c = thr - 2.2f * G - 0x1p-8f;  // S8 + 0.13 |S8| > c  <=>  S8 > c / 1.13 or c / 0.87
+        const float c = thr - 2.2f * G - 0x1p-8f;  // cl + 0.13 |cl| > c  <=>  cl > c / 1.13 or c / 0.87
         const __half2 sthr =
             __half2half2(__float2half_rd(kNoStage1 ? -INFINITY : (c >= 0.0f ? 0.884f * c : 1.15f * c)));
-        const float2 gm = make_float2(-G, -G), gp = make_float2(G, G);
+        const float2 gm = make_float2(-G, -G);
 #pragma unroll
         for (int g4 = 0; g4 < NC / 8; ++g4) {  // 4 pairs at a time, one branch
           uint32_t d4 = 0u, d16[4], ch4[4];
@@ -674,59 +753,34 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           }
           const __half2 mg = __hmax2(__hmax2(as_half2(s8h[4 * g4]), as_half2(s8h[4 * g4 + 1])),
                                      __hmax2(as_half2(s8h[4 * g4 + 2]), as_half2(s8h[4 * g4 + 3])));
-          gmx[g4] = *reinterpret_cast<const uint32_t*>(&mg);
-          if (d4 != 0u && __hgt2_mask(mg, sthr) != 0u) {  // rare: a logit near a boundary, maybe relevant
+          gmx[g4] = as_u32(mg);
+          // rare: a logit near a boundary, maybe relevant (needed by some lane
+          // of the warp for about one group in ten on the outlier workload).
+          // The vote makes it a warp-uniform branch: a per-lane condition
+          // lets the compiler run the body predicated on every group.
+          const bool grp_unc = d4 != 0u && __hgt2_mask(mg, sthr) != 0u;
+          if (__any_sync(0xffffffffu, grp_unc)) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int i = 4 * g4 + k;
-              const __half2 hh = as_half2(e4m3x2_to_f16x2((uint16_t)ch4[k]));
+              const uint32_t hb = e4m3x2_to_f16x2((uint16_t)ch4[k]);
+              const __half2 hh = as_half2(hb);
               uint32_t rel = __hgt2_mask(hh, lthr);
               if (tsplit) {  // T and -T are E4M3 values: exact in f16
                 const __half2 tpos = __half2half2(__float2half_rn(T)), tneg = __hneg2(tpos);
                 const __half2 hl = as_half2(s8h[i]);
                 rel |= (__hlt2_mask(hl, tpos) & __hge2_mask(hh, tpos)) | (__hle2_mask(hl, tneg) & __hgt2_mask(hh, tneg));
               }
-              if ((d16[k] & 0xFFu) && (rel & 0xFFFFu)) unc |= 1u << (2 * i);
-              if ((d16[k] >> 8) && (rel >> 16)) unc |= 1u << (2 * i + 1);
+              uint32_t u = grp_unc ? rel & (((d16[k] & 0xFFu) ? 0x0000FFFFu : 0u) | ((d16[k] >> 8) ? 0xFFFF0000u : 0u)) : 0u;
+              if (!all_full)
+                u &= (((vm >> (2 * i)) & 1u) ? 0x0000FFFFu : 0u) | (((vm >> (2 * i + 1)) & 1u) ? 0xFFFF0000u : 0u);
+              unc |= ((u & 1u) << (2 * i)) | (((u >> 16) & 1u) << (2 * i + 1));
+              hmx = as_u32(__hmax2(as_half2(hmx), as_half2((hb & u) | (0xFC00FC00u & ~u))));
             }
           }
         }
       }
-      unc &= vm;
       if (fail) unc = 0u;
-      bool gmx_ok = all_full;  // group maxima still describe s8h (no fix-up, no hidden key)
-      if (__any_sync(0xffffffffu, unc != 0u)) {
-        if (unc) gmx_ok = false;
-        const uint8_t* sK8 = (C::NS == 1 && !kSweep && ((jt - J0) & 1))
-                                 ? smem + C::OFF_K8B  // the second K8 slot of the one-stage layout
-                                 : smem + C::OFF_ST + ((jt - J0) % C::NS) * C::STAGE_BYTES;
-        for (;;) {
-          const unsigned who = __ballot_sync(0xffffffffu, unc != 0u);
-          if (!who) break;
-          const int src = __ffs(who) - 1;
-          const int cb = __shfl_sync(0xffffffffu, unc ? (__ffs(unc) - 1) : 0, src);
-          const long long acc = exact_dot<D>(sQ8, sK8, rw * 32 + src, col0 + cb, lane);
-          if (lane == src) {
-            const uint32_t hv = e4m3_f16_of_scaled(acc, p.sig_m, p.sig_e);
-            // replace half (cb & 1) of pair cb >> 1: a switch with constant
-            // indices keeps s8h in registers
-            static_assert(NC == 32, "the switch below lists 16 pairs");
-            const uint32_t keep = (cb & 1) ? 0x0000FFFFu : 0xFFFF0000u;
-            const uint32_t put = (hv * 0x00010001u) & ~keep;
-            switch (cb >> 1) {
-#define LAMP_FIX_CASE(i) case i: s8h[i] = (s8h[i] & keep) | put; break;
-              LAMP_FIX_CASE(0) LAMP_FIX_CASE(1) LAMP_FIX_CASE(2) LAMP_FIX_CASE(3)
-              LAMP_FIX_CASE(4) LAMP_FIX_CASE(5) LAMP_FIX_CASE(6) LAMP_FIX_CASE(7)
-              LAMP_FIX_CASE(8) LAMP_FIX_CASE(9) LAMP_FIX_CASE(10) LAMP_FIX_CASE(11)
-              LAMP_FIX_CASE(12) LAMP_FIX_CASE(13) LAMP_FIX_CASE(14) LAMP_FIX_CASE(15)
-#undef LAMP_FIX_CASE
-              default: break;
-            }
-            unc &= unc - 1u;
-          }
-          if (lane == 0) ++c_fix;
-        }
-      }
       // hidden keys take -inf: they are never the max and x8 saturates to -448 (P8 = 0)
       if (!all_full) {
 #pragma unroll
@@ -736,21 +790,136 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         }
       }
 
-      // ---- tile max over both halves, running max
-      float m_tile;
+      // ---- tile max over both halves.  The largest cl is a lower bound of
+      // it and the largest ch of the uncertain logits an upper bound; they
+      // agree unless an uncertain logit may be the maximum (rare).
+      float2* xlh = (float2*)(misc + M_XLH) + tt * 2 * kBM;
+      float lo_row, hi_row;
       {
         __half2 mx;
-        if (gmx_ok) {
+        if (all_full) {
           mx = __hmax2(__hmax2(as_half2(gmx[0]), as_half2(gmx[1])), __hmax2(as_half2(gmx[2]), as_half2(gmx[3])));
         } else {
           mx = as_half2(s8h[0]);
 #pragma unroll
           for (int i = 1; i < NC / 2; ++i) mx = __hmax2(mx, as_half2(s8h[i]));
         }
-        const float mine = fmaxf(__low2float(mx), __high2float(mx));
-        xch[hf * kBM + t] = mine;
+        const float lo = fmaxf(__low2float(mx), __high2float(mx));
+        const __half2 hx = as_half2(hmx);
+        const float hi = fmaxf(lo, fmaxf(__low2float(hx), __high2float(hx)));
+        xlh[hf * kBM + t] = make_float2(lo, hi);
         bar_sync(pair_bar, 64);
-        m_tile = fmaxf(mine, xch[(1 - hf) * kBM + t]);
+        const float2 o = xlh[(1 - hf) * kBM + t];
+        lo_row = fmaxf(lo, o.x);
+        hi_row = fmaxf(hi, o.y);
+      }
+      // Uncertain logits are settled in up to two passes.  Pass 0 (only if
+      // an uncertain logit may be a row's maximum; the same decision in both
+      // warps of the row group, which hold the same rows): those whose ch
+      // exceeds the row's largest cl are re-derived exactly, then the maximum
+      // is exchanged again.  Pass 1, with the maximum exact: cl stands for a
+      // logit if every value from cl to ch gives the same P8 code (P8 is
+      // monotone in S8, so the ends decide), the same side of tau_abs (the
+      // flag and the negative-logit scan), the same saturation count and
+      // (tau sweep) the same half-ulp8; otherwise it is re-derived too.
+      float m_tile = lo_row;
+      const bool max_unc = __any_sync(0xffffffffu, hi_row > lo_row);
+#pragma unroll 1
+      for (int pass = max_unc ? 0 : (__any_sync(0xffffffffu, unc != 0u) ? 1 : 2); pass < 2; ++pass) {
+        uint32_t ex = 0u;  // logits to re-derive exactly in this pass
+        uint32_t wor = __reduce_or_sync(0xffffffffu, unc);
+        if (wor) {
+          const float mref = pass == 0 ? lo_row : (rowvis ? fmaxf(m, m_tile) : m);
+          const __half2 mh = __float2half2_rn(mref);
+          const __half2 tp = __float2half2_rn(T), zero2 = __float2half2_rn(0.0f);
+          const float2 gm = make_float2(-G, -G);
+          tc_fence_after();
+          // one pair of logits at a time (a pair any lane of the warp has an
+          // uncertain logit in); both candidates come from the accumulators
+#pragma unroll 1
+          while (wor) {
+            const int i = (__ffs(wor) - 1) >> 1;
+            wor &= ~(3u << (2 * i));
+            uint32_t ar[2];
+            tmem_ld2(lane_base + C::S8_OFF + col0 + 2 * i, ar);
+            tmem_wait_ld();
+            const uint32_t ub = (unc >> (2 * i)) & 3u;
+            if (ub) {
+              const float2 av = make_float2(__uint_as_float(ar[0]), __uint_as_float(ar[1]));
+              const float2 yl = __ffma2_rn(av, sig2, gm), yh = __ffma2_rn(av, sig2, gp);
+              const __half2 ll = as_half2(e4m3x2_to_f16x2(cvt_e4m3x2(yl.y, yl.x)));
+              const __half2 hh = as_half2(e4m3x2_to_f16x2(cvt_e4m3x2(yh.y, yh.x)));
+              uint32_t sel;  // per half: re-derive
+              if (pass == 0) {
+                sel = __hgt2_mask(hh, mh);
+              } else {
+                const __half2 al = __habs2(ll), ah = __habs2(hh);
+                const uint32_t xl = cvt_e4m3x2_f16x2(__hsub2(ll, mh)), xh = cvt_e4m3x2_f16x2(__hsub2(hh, mh));
+                sel = __hge2_mask(al, tp) ^ __hge2_mask(ah, tp);
+                // a sign change between the ends passes |S8| = 0
+                const uint32_t straddle = __hlt2_mask(ll, zero2) & __hgt2_mask(hh, zero2);
+                if (T > 0.0f) sel |= straddle & __hge2_mask(__hmax2(al, ah), tp);
+                if (satp) {
+                  const __half2 sat2 = __float2half2_rn(448.0f);
+                  sel |= __heq2_mask(al, sat2) ^ __heq2_mask(ah, sat2);
+                }
+                if constexpr (kSweep) {  // the same half-ulp8: the same binade (all below 2^-6 share one)
+                  const __half2 lo6 = __float2half2_rn(0x1p-6f), lo5 = __float2half2_rn(0x1p-5f);
+                  const uint32_t e = (as_u32(__hmax2(al, lo6)) ^ as_u32(__hmax2(ah, lo6))) & 0x7C007C00u;
+                  sel |= ((e & 0xFFFFu) ? 0x0000FFFFu : 0u) | ((e >> 16) ? 0xFFFF0000u : 0u);
+                  sel |= straddle & __hge2_mask(__hmax2(al, ah), lo5);
+                }
+                if (((xl ^ xh) & 0xFFu) && tab[xl & 0xFFu] != tab[xh & 0xFFu]) sel |= 0x0000FFFFu;
+                if (((xl ^ xh) >> 8) && tab[xl >> 8] != tab[xh >> 8]) sel |= 0xFFFF0000u;
+              }
+              ex |= (ub & ((sel & 1u) | ((sel >> 15) & 2u))) << (2 * i);
+            }
+          }
+          if (pass == 1) c_res += __popc(unc & ~ex);
+          else c_fmax += __popc(ex);
+          unc = pass == 1 ? 0u : (unc & ~ex);
+        }
+        // exact re-derivation, one logit at a time over the warp
+        if (__any_sync(0xffffffffu, ex != 0u)) {
+          const uint8_t* sK8 = (C::NS == 1 && !kSweep && ((jt - J0) & 1))
+                                   ? smem + C::OFF_K8B  // the second K8 slot of the one-stage layout
+                                   : smem + C::OFF_ST + ((jt - J0) % C::NS) * C::STAGE_BYTES;
+          for (;;) {
+            const unsigned who = __ballot_sync(0xffffffffu, ex != 0u);
+            if (!who) break;
+            const int src = __ffs(who) - 1;
+            const int cb = __shfl_sync(0xffffffffu, ex ? (__ffs(ex) - 1) : 0, src);
+            const long long acc = exact_dot<D>(sQ8, sK8, rw * 32 + src, col0 + cb, lane);
+            if (lane == src) {
+              const uint32_t hv = e4m3_f16_of_scaled(acc, p.sig_m, p.sig_e);
+              // replace half (cb & 1) of pair cb >> 1: a switch with constant
+              // indices keeps s8h in registers
+              static_assert(NC == 32, "the switch below lists 16 pairs");
+              const uint32_t keep = (cb & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+              const uint32_t put = (hv * 0x00010001u) & ~keep;
+              switch (cb >> 1) {
+#define LAMP_FIX_CASE(i) case i: s8h[i] = (s8h[i] & keep) | put; break;
+                LAMP_FIX_CASE(0) LAMP_FIX_CASE(1) LAMP_FIX_CASE(2) LAMP_FIX_CASE(3)
+                LAMP_FIX_CASE(4) LAMP_FIX_CASE(5) LAMP_FIX_CASE(6) LAMP_FIX_CASE(7)
+                LAMP_FIX_CASE(8) LAMP_FIX_CASE(9) LAMP_FIX_CASE(10) LAMP_FIX_CASE(11)
+                LAMP_FIX_CASE(12) LAMP_FIX_CASE(13) LAMP_FIX_CASE(14) LAMP_FIX_CASE(15)
+#undef LAMP_FIX_CASE
+                default: break;
+              }
+              ex &= ex - 1u;
+            }
+            if (lane == 0) ++c_fix;
+          }
+        }
+        if (pass == 0) {  // the maximum again, from the exact values (both warps of the row group)
+          __half2 mx = as_half2(s8h[0]);
+#pragma unroll
+          for (int i = 1; i < NC / 2; ++i) mx = __hmax2(mx, as_half2(s8h[i]));
+          const float mine = fmaxf(__low2float(mx), __high2float(mx));
+          xch[hf * kBM + t] = mine;
+          bar_sync(pair_bar, 64);
+          m_tile = fmaxf(mine, xch[(1 - hf) * kBM + t]);
+        }
       }
       const float m_new = rowvis ? fmaxf(m, m_tile) : m;
 
@@ -815,11 +984,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         bar_sync(pair_bar, 64);
         if (maybe_neg) flg = (mine | xb[(1 - hf) * kBM + t]) != 0u;
       }
-      if (rowvis && satp) {
+      if (__any_sync(0xffffffffu, rowvis && satp)) {  // warp-uniform: rare
 #pragma unroll
         for (int i = 0; i < NC / 2; ++i) {
           const __half2 sv = as_half2(s8h[i]);
-          c_sat += (fabsf(__low2float(sv)) == 448.0f) + (fabsf(__high2float(sv)) == 448.0f);
+          if (rowvis && satp) c_sat += (fabsf(__low2float(sv)) == 448.0f) + (fabsf(__high2float(sv)) == 448.0f);
         }
       }
 
@@ -846,10 +1015,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       const bool any = bar_red_or(tile_bar, C::SM_THREADS, my_flag);
 
       if (t == 0 && hf == 0 && !fail) {  // every S8 read is done: the buffer may take the next QK8
+        *(volatile uint8_t*)(misc + M_ANY + 2 * tt + (jj & 1)) = any ? 1 : 0;
         mbar_arrive(bar(M_DEC + 8 * tt));
-        if (any) ++c_rec; else ++c_spec;
+        if (any) rcnt[0] += 1u;
+        if (prev_any != any) rcnt[any ? 2 : 1] += 1u;
       }
-      if (lane == 0 && hf == 0 && (rw & 1) == 0 && !fail) {
+      if (hf == 0 && (rw & 1) == 0 && __any_sync(0xffffffffu, !fail))  // the tile's two owner warps
+      if (lane == 0 && !fail) {
         // lane 0 of row groups 0 and 2 owns the 64-row query tile of groups (rw, rw+1)
         const unsigned long long ww = *(volatile unsigned long long*)(sflag + 4 * rw);  // rw even: 8-byte aligned
         const uint32_t w0 = (uint32_t)ww, w1 = (uint32_t)(ww >> 32);
@@ -919,9 +1091,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       // ---- 16-bit recompute for the rows of flagged sub-blocks
       // (the QK16 of every step is computed; a step without flags skips it)
       // two S16 buffers (one stage): buffer jj & 1 completes every other step
+      // (two S16 buffers: n16 counts the phases of each in one half-word)
       const uint32_t s16_bar = C::S16_BUFS == 2 ? bar(M_S16_FULL + 8 * (jj & 1)) : bar(M_S16_FULL + 8 * tt);
-      const uint32_t s16_par = C::S16_BUFS == 2 ? (uint32_t)(jj >> 1) & 1u : (uint32_t)jj & 1u;
-      if (any && !fail) fail = !wait_bar_warp(cx, s16_bar, s16_par);
+      const uint32_t s16_sh = C::S16_BUFS == 2 ? 16u * (uint32_t)(jj & 1) : 0u;
+      if (any && !fail) fail = !wait_bar_warp(cx, s16_bar, (n16 >> s16_sh) & 1u);
+      n16 += (any || prev_any) ? (1u << s16_sh) : 0u;  // QK16 of this step was issued
+      prev_any = any;
       if (any && !fail) {
         tc_fence_after();
         uint32_t r16[NC];
@@ -1025,8 +1200,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       c_sat = __reduce_add_sync(0xffffffffu, c_sat);
       if (lane == 0 && c_sat) atomicAdd(&p.counters[7], (u64)c_sat);
       if (lane == 0 && c_fix) atomicAdd(&p.counters[8], (u64)c_fix);
-      if (!kSweep && t == 0 && hf == 0 && c_rec) atomicAdd(&p.counters[10], (u64)c_rec);
-      if (!kSweep && t == 0 && hf == 0 && c_spec) atomicAdd(&p.counters[11], (u64)c_spec);
+      c_res = __reduce_add_sync(0xffffffffu, c_res);
+      if (lane == 0 && c_res) atomicAdd(&p.counters[13], (u64)c_res);
+      c_fmax = __reduce_add_sync(0xffffffffu, c_fmax);
+      if (lane == 0 && c_fmax) atomicAdd(&p.counters[14], (u64)c_fmax);
+      if (!kSweep && t == 0 && hf == 0) {
+        if (rcnt[0]) atomicAdd(&p.counters[10], (u64)rcnt[0]);
+        if (rcnt[1]) atomicAdd(&p.counters[11], (u64)rcnt[1]);
+        if (rcnt[2]) atomicAdd(&p.counters[12], (u64)rcnt[2]);
+      }
     }
   }
 

@@ -22,7 +22,8 @@ FORCE = {"off": 0, "all16": 1, "all8": 2}
 DT = {torch.bfloat16: 0, torch.float32: 1}
 NUM_COUNTERS = 16
 COUNTER_NAMES = ["tiles", "hist0", "hist1", "hist2p", "strips", "stage1", "flagged",
-                 "s8_saturated", "fixups", "status", "recompute_steps", "spec_waste"]
+                 "s8_saturated", "fixups", "status", "recompute_steps", "spec_waste", "recompute_late",
+                 "guard_resolved", "fixups_max"]
 EXPORTS = ["lamp_attn_fwd", "lamp_attn_fwd_noalloc", "lamp_attn_workspace_bytes", "lamp_strerror",
            "lamp_version", "lamp_exp8_table", "lamp_selftest", "lamp_attn_fwd_host",
            "lamp_attn_host_buffer_bytes", "lamp_attn_tau_sweep"]
