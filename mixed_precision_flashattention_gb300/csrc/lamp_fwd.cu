@@ -104,7 +104,6 @@ enum : int {
   M_K8B_EMPTY = 4616, // one stage: the second K8 slot is free
   M_ANY = 4624,       // u8 [2 tiles][2 step parities]: the step has a flagged sub-block
   M_XLH = 5120,       // f32x2 [2 tiles][2 halves][128 rows] bounds of the tile max exchanged
-  M_RCNT = 4632,      // u32 [2 tiles][3]: recompute steps used, computed ahead unused, computed late
 };
 
 struct Ctx {
@@ -450,6 +449,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         mma_commit(bar(M_PV_DONE + 8 * t));
         mma_commit(bar(M_KV_EMPTY + 16 * stage_of(jlo + i) + 8 * t));
       };
+      // recompute steps: used, issued ahead and not used, issued after the decision
+      uint32_t o_rec = 0, o_spec = 0, o_late = 0;
+      auto count = [&](bool dec, bool ahead) {
+        o_rec += dec;
+        o_spec += ahead && !dec;
+        o_late += dec && !ahead;
+      };
       bool ok = wait_bar(cx, bar(M_Q_FULL), 0);
       if (ok && !kSweep && p.q8_in_cta) ok = wait_bar(cx, bar(M_Q8_READY + 8 * t), 0);
       if (kSweep) {
@@ -516,15 +522,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
             ok = wait_bar(cx, bar(M_DEC), (i - 1) & 1);
             if (!ok) break;
             mbar_arrive(((i - 1) & 1) ? bar(M_K8B_EMPTY) : bar(M_KV_EMPTY));  // K8 slot of key j - 1
-            if (!spec) ok = decided(i - 1);
-            if (!ok) break;
-            spec = any_of(i - 1);
           }
           ok = wait_bar(cx, (i & 1) ? bar(M_K8B_FULL) : bar(M_KV_FULL), (uint32_t)(i >> 1) & 1u);
           if (!ok) break;
           tc_fence_after();
           Mma<D>::qk8(tm + C::S8_OFF, qbase, (i & 1) ? sbase + C::OFF_K8B : kv(j));
           mma_commit(bar(M_S_FULL));
+          if (i > 0) {  // the decision of step i - 1, read once QK8(i) is on its way
+            count(any_of(i - 1), spec);
+            if (!spec) ok = decided(i - 1);
+            if (!ok) break;
+            spec = any_of(i - 1);
+          }
           if (spec) {
             ok = wait_bar(cx, bar(M_KV_FULL + 8), ph);
             if (!ok) break;
@@ -542,6 +551,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           }
         }
         if (ok) ok = wait_bar(cx, bar(M_DEC), (n - 1) & 1);
+        if (ok) count(any_of(n - 1), spec);
         if (ok && !spec) ok = decided(n - 1);
         if (ok) ok = wait_bar(cx, bar(M_P_FULL), (n - 1) & 1);
         if (ok) ok = wait_bar(cx, bar(M_V_FULL), (uint32_t)(jlo + n - 1 - J0) & 1u);
@@ -568,22 +578,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       bool spec = true;  // QK16 of the current step is issued ahead of its decision (always the first)
       for (int i = 0; ok && i < n; ++i) {
         const int j = jlo + i;
-        if (i > 0) {
-          ok = wait_bar(cx, bar(M_DEC + 8 * t), (i - 1) & 1);
-          if (!ok) break;
-          const bool prev = any_of(i - 1);
-          if (prev && !spec) {  // step i - 1 decided to recompute: its products now
-            tc_fence_after();
-            qk16(i - 1);
-          }
-          spec = prev;
-        }
-        ok = wait_bar(cx, bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1);
+        if (i > 0) ok = wait_bar(cx, bar(M_DEC + 8 * t), (i - 1) & 1);
+        if (ok) ok = wait_bar(cx, bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1);
         if (!ok) break;
         tc_fence_after();
         Mma<D>::qk8(tm + C::S8_OFF, qbase, kv(j));
         mma_commit(bar(M_S_FULL + 8 * t));
         if (i > 0) {
+          // the decision of step i - 1, read once QK8(i) is on its way
+          const bool prev = any_of(i - 1);
+          count(prev, spec);
+          if (prev && !spec) qk16(i - 1);  // step i - 1 decided to recompute: its products now
+          spec = prev;
           ok = wait_bar(cx, bar(M_P_FULL + 8 * t), (i - 1) & 1);
           if (!ok) break;
           tc_fence_after();
@@ -592,9 +598,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         if (spec) qk16(i);
       }
       if (ok) ok = wait_bar(cx, bar(M_DEC + 8 * t), (n - 1) & 1);
-      if (ok && any_of(n - 1) && !spec) {
-        tc_fence_after();
-        qk16(n - 1);
+      if (ok) {
+        count(any_of(n - 1), spec);
+        if (any_of(n - 1) && !spec) {
+          tc_fence_after();
+          qk16(n - 1);
+        }
       }
       if (ok) ok = wait_bar(cx, bar(M_P_FULL + 8 * t), (n - 1) & 1);
       if (ok) {
@@ -604,6 +613,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       // make sure no MMA of this warp still writes TMEM before it is released
       mma_commit(bar(M_DRAIN + 8 * t));
       drain_wait(bar(M_DRAIN + 8 * t), 0);
+      if (p.counters && !kSweep) {
+        typedef unsigned long long u64;
+        if (o_rec) atomicAdd(&p.counters[10], (u64)o_rec);
+        if (o_spec) atomicAdd(&p.counters[11], (u64)o_spec);
+        if (o_late) atomicAdd(&p.counters[12], (u64)o_late);
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -653,8 +668,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
     const float gq = p.guard * p.sigma_f * (nq + 0x1p-6f), satq = p.sigma_f * nq * (1.0f + p.guard);
     uint32_t c_h0 = 0, c_h1 = 0, c_h2 = 0, c_strips = 0, c_st1 = 0, c_fl = 0, c_sat = 0, c_fix = 0,
              c_res = 0, c_fmax = 0;  // per-thread counts (a CTA sees at most 2^21 logits per thread slot)
-    volatile uint32_t* rcnt = (volatile uint32_t*)(misc + M_RCNT) + 3 * tt;  // thread t == 0, hf == 0 only
-    if (t == 0 && hf == 0) rcnt[0] = rcnt[1] = rcnt[2] = 0u;
     // S16 phases of the tile so far, and whether this step's QK16 was
     // issued ahead of the decision: for the first step, and when the step
     // before had a flagged sub-block (the MMA warp follows the same rule)
@@ -1017,8 +1030,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       if (t == 0 && hf == 0 && !fail) {  // every S8 read is done: the buffer may take the next QK8
         *(volatile uint8_t*)(misc + M_ANY + 2 * tt + (jj & 1)) = any ? 1 : 0;
         mbar_arrive(bar(M_DEC + 8 * tt));
-        if (any) rcnt[0] += 1u;
-        if (prev_any != any) rcnt[any ? 2 : 1] += 1u;
       }
       if (hf == 0 && (rw & 1) == 0 && __any_sync(0xffffffffu, !fail))  // the tile's two owner warps
       if (lane == 0 && !fail) {
@@ -1204,11 +1215,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       if (lane == 0 && c_res) atomicAdd(&p.counters[13], (u64)c_res);
       c_fmax = __reduce_add_sync(0xffffffffu, c_fmax);
       if (lane == 0 && c_fmax) atomicAdd(&p.counters[14], (u64)c_fmax);
-      if (!kSweep && t == 0 && hf == 0) {
-        if (rcnt[0]) atomicAdd(&p.counters[10], (u64)rcnt[0]);
-        if (rcnt[1]) atomicAdd(&p.counters[11], (u64)rcnt[1]);
-        if (rcnt[2]) atomicAdd(&p.counters[12], (u64)rcnt[2]);
-      }
     }
   }
 
