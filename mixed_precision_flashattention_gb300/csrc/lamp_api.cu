@@ -245,12 +245,7 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   fp.q8_in_cta = s.in_dtype == LAMP_DT_BF16 && !sweep;
   fp.sigma_f = (float)sigma_d;
   fp.sigma_d = sigma_d;
-  {
-    int e = 0;
-    const double f = std::frexp(sigma_d, &e);  // sigma_d = f * 2^e, f in [0.5, 1)
-    fp.sig_m = (unsigned long long)std::ldexp(f, 53);
-    fp.sig_e = e - 53;
-  }
+  fp.sig18 = std::ldexp(sigma_d, -18);
   fp.guard = guard_factor(D);
   fp.tau_abs = host_tau_abs(tau);
   fp.delta_code = host_delta_code(delta);

@@ -34,8 +34,7 @@ struct FwdParams {
   int q8_in_cta;        // bf16 q: Q8 = fl8(Q16 tile) in shared memory, row norms in the kernel
   float sigma_f;       // softmax scale rounded to float
   double sigma_d;      // softmax scale in double
-  unsigned long long sig_m;  // sigma_d = sig_m * 2^sig_e, 2^52 <= sig_m < 2^53
-  int sig_e;
+  double sig18;        // sigma_d * 2^-18 (exact re-derivations: acc * sig18 = A sigma)
   float guard;         // relative bound on |y_tc - y| per unit sigma*|q|*|k|
   float tau_abs;       // flag iff |S8| >= tau_abs (derived from tau)
   uint32_t delta_code; // stage 1 iff P8 code >= delta_code
@@ -103,50 +102,19 @@ __device__ __forceinline__ long long e4m3_prod_2p18(uint32_t a, uint32_t b) {
   return ((a ^ b) & 0x80u) ? -v : v;
 }
 
-// E4M3 value, as f16 bits, of the logit with exact dot product
-// acc * 2^-18 and softmax scale sigma = sig_m * 2^sig_e (sig_m the 53-bit
-// significand of the double scale): the product is rounded to double
-// precision (to nearest even, as one float64 multiply does) and then to
-// E4M3 (to nearest even, saturating to +-448).  Integer arithmetic only.
-__device__ __forceinline__ uint32_t e4m3_f16_of_scaled(long long acc, unsigned long long sig_m, int sig_e) {
-  const uint32_t neg = acc < 0 ? 0x80u : 0u;
-  const unsigned long long a = acc < 0 ? (unsigned long long)(-acc) : (unsigned long long)acc;  // < 2^43
-  uint32_t code = 0u;
-  if (a != 0ull) {
-    // P = a * sig_m < 2^96, value = P * 2^(sig_e - 18)
-    const unsigned long long lo = a * sig_m, hi = __umul64hi(a, sig_m);
-    const int msb = hi ? 127 - __clzll((long long)hi) : 63 - __clzll((long long)lo);
-    unsigned long long m53;  // value = m53 * 2^e2 with 2^52 <= m53 < 2^53
-    int e2;
-    if (msb <= 52) {
-      m53 = lo << (52 - msb);
-      e2 = sig_e - 18 - (52 - msb);
-    } else {  // drop sh (1..43) bits, round to nearest even
-      const int sh = msb - 52;
-      m53 = (hi << (64 - sh)) | (lo >> sh);
-      const unsigned long long rem = lo & ((1ull << sh) - 1ull), half = 1ull << (sh - 1);
-      m53 += (rem > half || (rem == half && (m53 & 1ull))) ? 1ull : 0ull;
-      e2 = sig_e - 18 + sh;
-      if (m53 >> 53) { m53 >>= 1; ++e2; }
-    }
-    int E = e2 + 52;  // value in [2^E, 2^(E+1))
-    if (E >= -6) {    // normal range: keep 4 significant bits
-      unsigned long long q = m53 >> 49;
-      const unsigned long long r = m53 & ((1ull << 49) - 1ull), h = 1ull << 48;
-      q += (r > h || (r == h && (q & 1ull))) ? 1ull : 0ull;
-      if (q == 16ull) { q = 8ull; ++E; }
-      code = (E > 8 || (E == 8 && q > 14ull)) ? 0x7Eu : (uint32_t)(((E + 7) << 3) | (int)(q - 8ull));
-    } else {          // subnormal: multiples of 2^-9
-      const int s = -(e2 + 9);  // >= 50
-      if (s <= 53) {
-        unsigned long long q = m53 >> s;
-        const unsigned long long r = m53 & ((1ull << s) - 1ull), h = 1ull << (s - 1);
-        q += (r > h || (r == h && (q & 1ull))) ? 1ull : 0ull;
-        code = (uint32_t)q;  // q = 8 is the code of 2^-6
-      }
-    }
-  }
-  return e4m3x2_to_f16x2((uint16_t)(code | neg)) & 0xFFFFu;
+// E4M3 value, as f16 bits, of the logit with exact dot product acc * 2^-18
+// and softmax scale sigma, sig18 = sigma * 2^-18: the product is rounded
+// to double precision (one float64 multiply; acc < 2^53 converts exactly),
+// which is the reading's y = A sigma, and then to E4M3 (to nearest even,
+// saturating to +-448).  The second rounding goes through float32 rounded
+// to odd -- truncated, with the last bit set when anything was cut off --
+// so that the float32 -> E4M3 rounding to nearest gives the same result as
+// one rounding of y (float32 keeps more than two bits beyond E4M3's four).
+__device__ __forceinline__ uint32_t e4m3_f16_of_product(long long acc, double sig18) {
+  const double y = (double)acc * sig18;
+  float f = __double2float_rz(y);
+  if ((double)f != y) f = __uint_as_float(__float_as_uint(f) | 1u);
+  return e4m3x2_to_f16x2(cvt_e4m3x2(0.0f, f)) & 0xFFFFu;
 }
 
 // Host: E4M3 code of the round-to-nearest-even, saturating conversion of a

@@ -904,7 +904,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
             const int cb = __shfl_sync(0xffffffffu, ex ? (__ffs(ex) - 1) : 0, src);
             const long long acc = exact_dot<D>(sQ8, sK8, rw * 32 + src, col0 + cb, lane);
             if (lane == src) {
-              const uint32_t hv = e4m3_f16_of_scaled(acc, p.sig_m, p.sig_e);
+              const uint32_t hv = e4m3_f16_of_product(acc, p.sig18);
               // replace half (cb & 1) of pair cb >> 1: a switch with constant
               // indices keeps s8h in registers
               static_assert(NC == 32, "the switch below lists 16 pairs");

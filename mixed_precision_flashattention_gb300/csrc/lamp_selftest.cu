@@ -89,10 +89,7 @@ __global__ void __launch_bounds__(128, 1)
 __global__ void lamp_round_selftest_kernel(const long long* acc, const double* sigma, float* out, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
-  int e = 0;
-  const double f = frexp(*sigma, &e);
-  const unsigned long long m = (unsigned long long)ldexp(f, 53);
-  const uint32_t h = e4m3_f16_of_scaled(acc[i], m, e - 53);
+  const uint32_t h = e4m3_f16_of_product(acc[i], ldexp(*sigma, -18));
   out[i] = __half2float(__ushort_as_half((unsigned short)h));
 }
 
