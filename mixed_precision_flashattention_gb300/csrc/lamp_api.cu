@@ -71,7 +71,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* bas
 }
 
 struct WsLayout {
-  size_t q8, k8, v16, q16, k16, nq, nk, abort, total;
+  size_t q8, k8, v16, q16, k16, nq, nqc, nk, nkc, abort, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -89,7 +89,9 @@ WsLayout ws_layout(const lamp_shapes& s) {
     w.k16 = o; o = align256(o + B * Hkv * N * D * 2);
   }
   w.nq = o; o = align256(o + B * Hq * N * 4);
-  w.nk = o; o = align256(o + B * Hkv * T * 4);
+  w.nqc = o; o = align256(o + B * Hq * N * (D / 32) * 4);
+  w.nk = o; o = align256(o + B * Hkv * T * 4);   // nk, nkc and abort are zeroed by one memset
+  w.nkc = o; o = align256(o + B * Hkv * T * (D / 32) * 4);
   w.abort = o; o = align256(o + 4);
   w.total = o;
   return w;
@@ -233,6 +235,8 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   fp.counters = stats ? (unsigned long long*)stats->counters : nullptr;
   fp.nq = (const float*)(ws + w.nq);
   fp.nkmax = (const float*)(ws + w.nk);
+  fp.nqc = (const float*)(ws + w.nqc);
+  fp.nkc = (const float*)(ws + w.nkc);
   for (int i = 0; i < 3; ++i) fp.o_stride[i] = s.o_stride[i];
   fp.B = B; fp.N = N; fp.Hq = Hq; fp.Hkv = Hkv; fp.T = T;
   fp.nqb = (N + kBM - 1) / kBM;
@@ -261,7 +265,8 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
     return fail(LAMP_ERR_CUDA);
   if (sweep && cudaMemsetAsync(records, 0, (size_t)B * Hq * T * T * 4, stream) != cudaSuccess)
     return fail(LAMP_ERR_CUDA);
-  // norms of the key tiles and the abort word are contiguous: one memset
+  // norms of the key tiles (whole and per chunk) and the abort word are
+  // contiguous: one memset
   if (cudaMemsetAsync(ws + w.nk, 0, w.total - w.nk, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
 
   PrepParams pp{};
@@ -272,6 +277,7 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   pp.q16 = s.in_dtype == LAMP_DT_FP32 ? (void*)(ws + w.q16) : nullptr;
   pp.k16 = s.in_dtype == LAMP_DT_FP32 ? (void*)(ws + w.k16) : nullptr;
   pp.nq = (float*)(ws + w.nq); pp.nkmax = (float*)(ws + w.nk);
+  pp.nqc = (float*)(ws + w.nqc); pp.nkc = (float*)(ws + w.nkc);
   pp.B = B; pp.N = N; pp.Hq = Hq; pp.Hkv = Hkv; pp.T = T; pp.in_f32 = s.in_dtype == LAMP_DT_FP32;
   auto mark = [&](int i) {
     return !s.stage_events[i] || cudaEventRecord((cudaEvent_t)s.stage_events[i], stream) == cudaSuccess;

@@ -28,6 +28,8 @@ struct FwdParams {
   uint32_t* records;   // tau-sweep pass: [B, Hq, T, T] tile records
   const float* nq;     // [B, Hq, N]   ||fl8(q_r)||_2 (upper bound)
   const float* nkmax;  // [B, Hkv, T]  max over the tile of ||fl8(k_c)||_2
+  const float* nqc;    // [B, Hq, N, D/32] the same per 32-element chunk of d
+  const float* nkc;    // [B, Hkv, T, D/32] max over the tile of the chunk norms, + 2^-6
   long long o_stride[3];
   int B, N, Hq, Hkv, T, nqb;
   int window, mask_kind, force, out_f32;
@@ -56,6 +58,8 @@ struct PrepParams {
   void* k16;                      // [B, Hkv, N, D] bf16 (fp32 input only)
   float* nq;                      // [B, Hq, N]
   float* nkmax;                   // [B, Hkv, T] (zeroed before the launch)
+  float* nqc;                     // [B, Hq, N, D/32] chunk norms
+  float* nkc;                     // [B, Hkv, T, D/32] max chunk norms + 2^-6 (zeroed before the launch)
   int B, N, Hq, Hkv, T, in_f32;
   int skip_q;  // the fused kernel makes Q8 and the q norms itself
   // division by Hq, Hkv and N as multiply and shift (set by the launcher)

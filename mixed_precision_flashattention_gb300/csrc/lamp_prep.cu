@@ -148,14 +148,25 @@ __device__ __forceinline__ void prep_store(const PrepParams& p, int col, int lan
     for (int i = 0; i < 4; ++i) w[i] = cvt_f16x2_sat(x[2 * i + 1], x[2 * i]);
     *reinterpret_cast<uint4*>((__half*)p.v16 + o) = make_uint4(w[0], w[1], w[2], w[3]);
   }
-  // row norm: sum over the row's lanes (all lanes take part in the shuffles)
+  // norms of the row's 32-element chunks (4 lanes each), then of the row;
+  // all lanes take part in the shuffles.  Upper bounds: the float sums of
+  // squares are rounded up.
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+  if ((isq || isk) && (lane % 4) == 0) {
+    constexpr int C = D / 32;
+    const int c = (lane % LPR) / 4;
+    const float nrm = sqrtf(ss) * (1.0f + 0x1p-16f);
+    if (isq) p.nqc[s.orow * (Off)C + c] = nrm;
+    else  // non-negative floats order like their bit patterns
+      atomicMax((int*)&p.nkc[s.nki * (Off)C + c], __float_as_int(nrm + 0x1p-6f));
+  }
 #pragma unroll
-  for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  for (int o = LPR / 2; o > 2; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((isq || isk) && (lane % LPR) == 0) {
-    // upper bound of the norm: the float sum of squares is rounded up
     const float nrm = sqrtf(ss) * (1.0f + 0x1p-16f);
     if (isq) p.nq[s.orow] = nrm;
-    else  // non-negative floats order like their bit patterns
+    else
       atomicMax((int*)&p.nkmax[s.nki], __float_as_int(nrm));
   }
 }

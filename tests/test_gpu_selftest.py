@@ -185,6 +185,9 @@ def test_fp8_accumulation_model(lamp, d, kind):
     assert bad.size == 0, [(tuple(ix), out[tuple(ix)], model[tuple(ix)], (a8 @ b8.T)[tuple(ix)]) for ix in bad[:4]]
     bound = tc_fp8_error_bound(d, np.linalg.norm(a8, axis=1)[:, None], np.linalg.norm(b8, axis=1)[None, :])
     assert np.all(np.abs(out - a8 @ b8.T) <= bound)
+    # and below the per-chunk bound the fused kernel's guard uses
+    from tests.test_guard_bound import chunk_guard
+    assert np.all(np.abs(out - a8 @ b8.T) <= chunk_guard(a8, b8, factor=37.0))
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
