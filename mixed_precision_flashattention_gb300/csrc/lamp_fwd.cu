@@ -886,8 +886,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
 #pragma unroll 1
       for (int pass = max_unc ? 0 : (__any_sync(0xffffffffu, unc != 0u) ? 1 : 2); pass < 2; ++pass) {
         uint32_t ex = 0u;  // logits to re-derive exactly in this pass
+        if constexpr (kNoStage1) {
+          // first stage off: most uncertain logits straddle +-tau_abs, where
+          // the comparison of the candidates cannot settle them (measured:
+          // half of them); they are re-derived without it
+          if (pass == 1) {
+            ex = unc;
+            unc = 0u;
+          }
+        }
         uint32_t wor = __reduce_or_sync(0xffffffffu, unc);
-        if (wor) {
+        if (wor && !(kNoStage1 && pass == 1)) {
           const float mref = pass == 0 ? lo_row : (rowvis ? fmaxf(m, m_tile) : m);
           const __half2 mh = __float2half2_rn(mref);
           const __half2 tp = __float2half2_rn(T), zero2 = __float2half2_rn(0.0f);
