@@ -40,6 +40,10 @@ the rest supports (each is listed in the design notes):
      (float64); out = O / l, LSE = m + ln l.
   R9 a tile is visited iff it holds at least one visible (row, key) pair;
      the per-tile histogram counts flagged sub-blocks of visited tiles.
+  R14 (optional mode pv="fp8"; the pages do not say in which precision
+     P.V runs) rows of unflagged sub-blocks multiply their P8 (already
+     E4M3) with V8 = fl8(v), one saturating RNE rounding from the input
+     values; rows of flagged sub-blocks keep P16 . V16 as in R8.
 """
 from __future__ import annotations
 
@@ -86,7 +90,7 @@ def visibility(rows: np.ndarray, cols: np.ndarray, n: int, mask: str,
 
 
 def _qtile_block(q_rows, k_h, v_h, rows, n, sigma, mask, window, delta, tau,
-                 force):
+                 force, pv="fp16"):
     """One head, a stack of query tiles: q_rows [nI, 64, d] (values as given),
     rows [nI, 64] absolute row indices.  Returns O, l, m, mask bytes, counts."""
     nI = q_rows.shape[0]
@@ -96,6 +100,7 @@ def _qtile_block(q_rows, k_h, v_h, rows, n, sigma, mask, window, delta, tau,
     k8 = e4m3_round(k_h)
     k16 = bf16_round(k_h)
     v16 = f16_round(v_h)
+    v8 = e4m3_round(v_h) if pv == "fp8" else None  # R14
     d = q_rows.shape[-1]
 
     # R2: exact sum of 8-bit products, scaled in float64, rounded once
@@ -150,8 +155,13 @@ def _qtile_block(q_rows, k_h, v_h, rows, n, sigma, mask, window, delta, tau,
             alpha = np.where(np.isneginf(m), 0.0, np.exp(m - m_new))
         vj = np.zeros((TILE, d))
         vj[: c1 - c0] = v16[c0:c1]
+        PV = P @ vj
+        if v8 is not None:  # R14: 8-bit V for the rows of unflagged sub-blocks
+            vj8 = np.zeros((TILE, d))
+            vj8[: c1 - c0] = v8[c0:c1]
+            PV = np.where(frow[..., None], PV, P @ vj8)
         l = alpha * l + P.sum(axis=-1)
-        O = alpha[..., None] * O + P @ vj
+        O = alpha[..., None] * O + PV
         m = m_new
 
         bits = np.zeros(nI, dtype=np.int64)
@@ -173,12 +183,13 @@ def _qtile_block(q_rows, k_h, v_h, rows, n, sigma, mask, window, delta, tau,
 
 def lamp_forward(q, k, v, *, mask="causal", window=0, scale=None,
                  delta=2.0 ** -8, tau=2.0 ** -1, force="off", out_dtype="bf16",
-                 tiles=None, chunk_elems=1 << 24) -> LampResult:
+                 tiles=None, chunk_elems=1 << 24, pv="fp16") -> LampResult:
     """The LAMP emulation on float64 arrays holding the input values.
 
     q [B, N, Hq, d], k/v [B, N, Hkv, d].  ``tiles``: None for every query
     tile, else an iterable of (b, h, i) query tiles to compute (others are
-    left NaN / zero).  ``out_dtype`` in {"bf16", "fp32"}."""
+    left NaN / zero).  ``out_dtype`` in {"bf16", "fp32"}.  ``pv`` in
+    {"fp16", "fp8"}: the P.V operands of unflagged sub-blocks (R8 / R14)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -188,6 +199,8 @@ def lamp_forward(q, k, v, *, mask="causal", window=0, scale=None,
         raise ValueError("heads_q must be a multiple of heads_kv")
     if force not in FORCE:
         raise ValueError(force)
+    if pv not in ("fp16", "fp8"):
+        raise ValueError(pv)
     sigma = (1.0 / np.sqrt(float(d))) if scale is None else float(scale)
     T = (n + TILE - 1) // TILE
     grp = Hq // Hkv
@@ -218,7 +231,7 @@ def lamp_forward(q, k, v, *, mask="causal", window=0, scale=None,
             q_rows[ok] = q[b, rows[ok], h, :]
             O, l, m, mb, cn = _qtile_block(q_rows, k[b, :, g, :], v[b, :, g, :],
                                            rows, n, sigma, mask, window,
-                                           delta, tau, force)
+                                           delta, tau, force, pv)
             cnt += cn
             mbytes[b, h, idx, :] = mb
             with np.errstate(invalid="ignore", divide="ignore"):

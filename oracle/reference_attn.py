@@ -104,8 +104,10 @@ def _e4m3_int(x):
 
 
 def lamp8_rowloop(q, k, v, *, mask="causal", window=0, scale=None,
-                  delta=2.0 ** -8, tau=2.0 ** -1, rows=None, b=0, h=0):
+                  delta=2.0 ** -8, tau=2.0 ** -1, rows=None, b=0, h=0, pv="fp16"):
     """All-8-bit path, one row at a time, for rows of head (b, h).
+
+    ``pv``: the V operand of P.V, "fp16" (f16(v)) or "fp8" (fl8(v)).
 
     Returns dict row -> (out_row, lse, {tile: (stage1_bit, flag_bit)}),
     where the per-tile bits say whether that row alone would pass stage 1 /
@@ -119,7 +121,7 @@ def lamp8_rowloop(q, k, v, *, mask="causal", window=0, scale=None,
     T = (n + 63) // 64
     qi = _e4m3_int(q[b, :, h, :])
     ki = _e4m3_int(k[b, :, g, :])
-    v16 = f16_round(v[b, :, g, :])
+    vrow = (e4m3_round if pv == "fp8" else f16_round)(v[b, :, g, :])
     res = {}
     for r in (range(n) if rows is None else rows):
         m = -math.inf
@@ -154,7 +156,7 @@ def lamp8_rowloop(q, k, v, *, mask="causal", window=0, scale=None,
                     if float(half_ulp_e4m3(s8[c])) >= tau:
                         fl = True
                 l += p8
-                o += p8 * v16[c]
+                o += p8 * vrow[c]
             bits[j] = (st1, fl)
             m = m_new
         if l > 0:

@@ -125,6 +125,70 @@ def test_all8_equals_independent_row_loop():
             assert r8.mask[0, 0, i, j] == exp_byte & 0xF0
 
 
+def test_pv8_all8_equals_independent_row_loop():
+    """FP8 P.V (reading R14) on the all-8-bit path against a row loop that
+    adds P8 * fl8(v) key by key."""
+    q, k, v = synth.gen_tiny(1, 130, 1, 1, 16, seed=6)
+    r8 = oracle.lamp_forward(q, k, v, force="all8", out_dtype="fp32", pv="fp8")
+    rows = oracle.lamp8_rowloop(q, k, v, pv="fp8")
+    for row, (o, lse, _) in rows.items():
+        assert np.allclose(r8.out[0, row, 0], o, atol=1e-9, rtol=0)
+        assert abs(r8.lse[0, 0, row] - lse) < 1e-9
+    # the mode changes the result: fl8(v) is not f16(v)
+    r16 = oracle.lamp_forward(q, k, v, force="all8", out_dtype="fp32")
+    assert np.abs(r8.out - r16.out).max() > 1e-3
+    assert np.array_equal(r8.lse, r16.lse)
+
+
+def test_pv8_flagged_rows_keep_16bit_v():
+    """Rows of flagged sub-blocks take P16 . V16 in both modes: forcing
+    every sub-block to 16 bits makes the modes identical, and under the
+    detector a row flagged in every tile it visits has the same output."""
+    q, k, v = synth.gen_outlier_sink(1, 192, 2, 1, 64, seed=12)
+    q, k, v = _bf16(q), _bf16(k), _bf16(v)
+    a = oracle.lamp_forward(q, k, v, force="all16", out_dtype="fp32", pv="fp8")
+    b = oracle.lamp_forward(q, k, v, force="all16", out_dtype="fp32")
+    assert np.array_equal(a.out, b.out) and np.array_equal(a.lse, b.lse)
+    # tau = 4: some rows flagged in every tile, some in none
+    a = oracle.lamp_forward(q, k, v, out_dtype="fp32", tau=4.0, pv="fp8")
+    b = oracle.lamp_forward(q, k, v, out_dtype="fp32", tau=4.0)
+    assert np.array_equal(a.mask, b.mask) and np.array_equal(a.counters, b.counters)
+    same = differ = 0
+    for h in range(2):
+        for row in range(192):
+            i, s = row // 64, (row % 64) // 16
+            visited = [j for j in range(i + 1)]
+            if all((b.mask[0, h, i, j] >> s) & 1 for j in visited):
+                assert np.array_equal(a.out[0, row, h], b.out[0, row, h])
+                same += 1
+            elif not any((b.mask[0, h, i, j] >> s) & 1 for j in visited):
+                differ += not np.array_equal(a.out[0, row, h], b.out[0, row, h])
+    assert same > 0 and differ > 0
+
+
+def test_pv8_v_on_the_e4m3_grid_changes_nothing():
+    """With v already on the E4M3 grid, fl8(v) = f16(v) = v: both modes
+    give the same mask, output and LSE."""
+    q, k, v = synth.gen_outlier_sink(1, 130, 2, 1, 64, seed=13)
+    v = F.e4m3_round(v)
+    a = oracle.lamp_forward(q, k, v, out_dtype="fp32", pv="fp8")
+    b = oracle.lamp_forward(q, k, v, out_dtype="fp32")
+    assert np.array_equal(a.mask, b.mask)
+    assert np.array_equal(a.out, b.out) and np.array_equal(a.lse, b.lse)
+
+
+def test_pv8_zero_queries_closed_form():
+    """q = 0: every logit is 0, every visible P8 is 1 and nothing is
+    flagged, so row r's output is the mean of fl8(v) over keys 0..r."""
+    q, k, v = synth.gen_iid(1, 150, 1, 1, 32, seed=9)
+    q[:] = 0
+    r = oracle.lamp_forward(q, k, v, out_dtype="fp32", pv="fp8")
+    v8 = F.e4m3_round(v[0, :, 0, :])
+    for row in range(150):
+        assert np.allclose(r.out[0, row, 0], v8[: row + 1].mean(axis=0), atol=1e-12)
+    assert r.counters[C_FLAGGED] == 0
+
+
 def test_weights_sum_to_one():
     q, k, v = synth.gen_outlier_sink(1, 192, 2, 1, 64, seed=7)
     ones = np.ones_like(v)
