@@ -36,10 +36,10 @@ FLUSH_BYTES = 256 << 20  # > 129 MB L2
 
 # ---------------------------------------------------------------- CPU oracle leg
 def _oracle_task(args):
-    qv, kv, vv, tiles, mask, window, delta, tau = args
+    qv, kv, vv, tiles, mask, window, delta, tau, pv = args
     import oracle
     t0 = time.perf_counter()
-    oracle.lamp_forward(qv, kv, vv, mask=mask, window=window, delta=delta, tau=tau, tiles=tiles)
+    oracle.lamp_forward(qv, kv, vv, mask=mask, window=window, delta=delta, tau=tau, tiles=tiles, pv=pv)
     return time.perf_counter() - t0
 
 
@@ -62,14 +62,14 @@ def _head_values(w, x, b, h):
     return (t.to(torch.bfloat16) if w.dtype == "bf16" else t).double().numpy()
 
 
-def cpu_sample_tasks(w, q, k, v, delta, tau, wall_budget_s, ncores, seed=0):
+def cpu_sample_tasks(w, q, k, v, delta, tau, wall_budget_s, ncores, seed=0, pv="fp16"):
     """Bounded sample of the workload for the CPU oracle: random
     (batch, head, query-tile) triples until the estimated wall time on
     ``ncores`` workers reaches ``wall_budget_s``.  One task per head."""
     T = (w.seqlen + 63) // 64
     grp = w.heads_q // w.heads_kv
     probe = (_head_values(w, q, 0, 0), _head_values(w, k, 0, 0), _head_values(w, v, 0, 0),
-             [(0, 0, T - 1)], w.mask, w.window, delta, tau)
+             [(0, 0, T - 1)], w.mask, w.window, delta, tau, pv)
     t_long = _oracle_task(probe)  # seconds for the longest query tile
     rng = np.random.default_rng(seed)
     picks, est, n = {}, 0.0, 0
@@ -85,7 +85,7 @@ def cpu_sample_tasks(w, q, k, v, delta, tau, wall_budget_s, ncores, seed=0):
     for (b, h), tiles in picks.items():
         g = h // grp
         tasks.append((_head_values(w, q, b, h), _head_values(w, k, b, g), _head_values(w, v, b, g),
-                      [(0, 0, i) for i in sorted(tiles)], w.mask, w.window, delta, tau))
+                      [(0, 0, i) for i in sorted(tiles)], w.mask, w.window, delta, tau, pv))
         flops += sum(_tile_flops(w, i) for i in tiles)
     return tasks, flops
 
@@ -194,30 +194,30 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def _capture(workload: str):
+def _capture(workload: str, pv: str = "fp16"):
     """The committed ncu capture of one fused-kernel launch, if it was taken
-    on this workload with the current kernel source (else None)."""
+    on this workload and P.V mode with the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", "lamp_fwd_traffic.json")
     if not os.path.exists(path):
         return None
     d = json.load(open(path))
-    if d.get("workload") != workload or d.get("source_sha") != kernel_source_sha():
+    if d.get("workload") != workload or d.get("source_sha") != kernel_source_sha() or d.get("pv", "fp16") != pv:
         return None
     return d
 
 
-def _traffic(workload: str):
+def _traffic(workload: str, pv: str = "fp16"):
     """DRAM bytes per launch of the fused kernel (committed capture)."""
-    d = _capture(workload)
+    d = _capture(workload, pv)
     return None if d is None else float(d["dram_bytes_read"]) + float(d["dram_bytes_write"])
 
 
-def _issue_roofline(workload: str, ms_main: float, sm_mhz):
+def _issue_roofline(workload: str, ms_main: float, sm_mhz, pv: str = "fp16"):
     """The fused kernel is bound by instruction issue in its softmax warps:
     the floor its warp-instruction count (committed capture) allows at one
     instruction per clock on each of the 4 schedulers of every SM, at the
     SM clock sampled in the timed region, against the measured time."""
-    d = _capture(workload)
+    d = _capture(workload, pv)
     if d is None or "warp_instructions" not in d or not sm_mhz:
         return None
     import torch
@@ -267,6 +267,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--generator", default=None, choices=sorted(synth.GENERATORS),
                     help="input generator in place of the workload's own (same shape)")
+    ap.add_argument("--pv", default="fp16", choices=["fp16", "fp8"],
+                    help="P.V precision of unflagged sub-blocks (fp8: the optional FP8 P.V mode)")
     ap.add_argument("--parity-tiles", type=int, default=64,
                     help="query tiles of the timed inputs checked against the oracle (0: none)")
     args = ap.parse_args()
@@ -281,7 +283,7 @@ def main():
     config = {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "heads_q": w.heads_q,
               "heads_kv": w.heads_kv, "head_dim": w.head_dim, "mask": w.mask, "window": w.window,
               "in_dtype": w.dtype, "tau": args.tau, "delta": args.delta,
-              "generator": w.gen, "seed": args.seed}
+              "generator": w.gen, "seed": args.seed, "pv": args.pv}
 
     if args.impl == "reference" and rank != 0:
         return  # the oracle arm runs on rank 0 only
@@ -305,7 +307,8 @@ def main():
         # about 4 x --cpu-seconds of estimated oracle time over the whole run
         # (the pool's transfers roughly double the estimate)
         tasks, sflops = cpu_sample_tasks(w, q, k, v, args.delta, args.tau,
-                                         args.cpu_seconds * 4 / max(1, args.steps + args.warmup), ncores)
+                                         args.cpu_seconds * 4 / max(1, args.steps + args.warmup), ncores,
+                                         pv=args.pv)
         for _ in range(args.warmup):
             run_cpu_oracle(pool, tasks)
         times = [run_cpu_oracle(pool, tasks) for _ in range(args.steps)]
@@ -336,12 +339,13 @@ def main():
     out = torch.empty_like(qd)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
     mbytes, cnt = lamp.new_stats(B, Hq, N, device=dev)
-    ws = torch.empty(lamp.workspace_bytes(qd, kd, vd, out), dtype=torch.uint8, device=dev)
+    ws = torch.empty(lamp.workspace_bytes(qd, kd, vd, out, pv=args.pv), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step(evs=None, o=out, l=lse, qq=qd, kk=kd, vv=vd):
         lamp.lamp_attn_fwd(qq, kk, vv, mask=w.mask, window=w.window, delta=args.delta, tau=args.tau,
-                           out=o, lse=l, mask_bytes=mbytes, counters=cnt, workspace=ws, stage_events=evs)
+                           out=o, lse=l, mask_bytes=mbytes, counters=cnt, workspace=ws, stage_events=evs,
+                           pv=args.pv)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -395,14 +399,14 @@ def main():
     qh, kh, vh = (x.cpu().pin_memory() for x in (qd, kd, vd))
     oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    hbuf = torch.empty(lamp.host_buffer_bytes(qh, kh, vh, oh), dtype=torch.uint8, device=dev)
+    hbuf = torch.empty(lamp.host_buffer_bytes(qh, kh, vh, oh, pv=args.pv), dtype=torch.uint8, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = []
     for i in range(max(3, K // 2) + 2):
         torch.cuda.synchronize()
         e0.record()
         lamp.lamp_attn_fwd_host(qh, kh, vh, mask=w.mask, window=w.window, delta=args.delta, tau=args.tau,
-                                out=oh, lse=lh, mask_bytes=mbytes, counters=cnt, dev_buffer=hbuf)
+                                out=oh, lse=lh, mask_bytes=mbytes, counters=cnt, dev_buffer=hbuf, pv=args.pv)
         e1.record()
         torch.cuda.synchronize()
         if i >= 2:
@@ -445,13 +449,17 @@ def main():
         else:
             kv_steps += last // 64 + 1 - max(0, qb * 128 - w.window + 1) // 64
     kv_steps *= B * Hq
-    f_qk8 = kv_steps * 2.0 * 128 * 64 * d
-    f_pv = kv_steps * 2.0 * 128 * 64 * d
-    f_rec = float(c[10] + c[11]) * 2.0 * 128 * 64 * d  # 16-bit products issued: used, or ahead and not needed
-    f_rec_used = float(c[10]) * 2.0 * 128 * 64 * d
+    f_step = 2.0 * 128 * 64 * d  # one MMA product of a 128-row x 64-key step
+    f_qk8 = kv_steps * f_step
+    f_rec = float(c[10] + c[11]) * f_step  # 16-bit products issued: used, or ahead and not needed
+    f_rec_used = float(c[10]) * f_step
+    if args.pv == "fp8":  # every step's P8.V8, plus P16.V16 for steps with a flagged sub-block
+        f_pv8, f_pv = kv_steps * f_step, float(c[10]) * f_step
+    else:
+        f_pv8, f_pv = 0.0, kv_steps * f_step
     # tensor-core time of the issued work at the peaks: the fastest this
     # kernel design could run on these inputs if the tensor pipe never idled
-    t_tc = (f_qk8 / (fp8_peak * 1e12) + (f_pv + f_rec) / (bf16_peak * 1e12))
+    t_tc = ((f_qk8 + f_pv8) / (fp8_peak * 1e12) + (f_pv + f_rec) / (bf16_peak * 1e12))
     res = {
         "metric": METRIC, "value": flops / (ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -459,28 +467,29 @@ def main():
         "config": {**config, "l2": "flushed between steps (256 MB write), per-step CUDA events"},
         "fp8_peak_frac": flops / (ms * 1e-3) / 1e12 / fp8_peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": achieved / fp8_peak, "traffic": _traffic(w.name),
+                     "frac": achieved / fp8_peak, "traffic": _traffic(w.name, args.pv),
                      "kernel": "lamp_fwd_kernel", "peak_basis": f"2 x {peak_src} bf16 burst {bf16_peak} (dense FP8:BF16 = 2)",
                      "mixed_tc_time_frac": t_tc / (ms_main * 1e-3),
                      "ceiling_fp8_frac": flops / t_tc / 1e12 / fp8_peak,
-                     "issue": _issue_roofline(w.name, ms_main, (clocks or {}).get("sm_mhz"))},
+                     "issue": _issue_roofline(w.name, ms_main, (clocks or {}).get("sm_mhz"), args.pv)},
         "ms_main_kernel": ms_main, "ms_prepass": statistics.mean(t_prep), "wall_s": t_wall,
         "ms_per_step_p10_p50_p90": pct, "ms_per_step_l2_warm": warm_ms,
         "stats": {n: int(c[i]) for i, n in enumerate(lamp.COUNTER_NAMES)},
         "subblock16_frac": float(c[6]) / max(1, c[4]),
         "tiles_0_1_2plus": [float(c[1]) / max(1, c[0]), float(c[2]) / max(1, c[0]), float(c[3]) / max(1, c[0])],
-        "tensor_flops_issued": {"qk_fp8": f_qk8, "pv_fp16": f_pv, "recompute_bf16": f_rec,
+        "tensor_flops_issued": {"qk_fp8": f_qk8, "pv_fp8": f_pv8, "pv_fp16": f_pv, "recompute_bf16": f_rec,
                                 "recompute_bf16_used": f_rec_used},
         "e2e": {"value": flops / (e2e_step * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world, "ms_per_step": e2e_step},
         "tau_sweep": {"taus": sweep_taus, "ms": sweep_ms, "forward_ms": ms, "speedup_vs_forward_per_tau":
                       len(sweep_taus) * ms / sweep_ms,
                       "tiles_0_1_2plus": [[float(x) / max(1, hrow[0]) for x in hrow[1:]] for hrow in sw_hist]},
-        "gpu_launches": 2 * K * world,  # pre-pass + fused kernel per step and rank
+        # pre-pass (+ the V8 copy for the FP8 P.V) + fused kernel per step and rank
+        "gpu_launches": (3 if args.pv == "fp8" else 2) * K * world,
         "clocks": clocks,
     }
     if want_cpu:
-        tasks, sflops = cpu_sample_tasks(w, q, k, v, args.delta, args.tau, args.cpu_seconds, ncores)
+        tasks, sflops = cpu_sample_tasks(w, q, k, v, args.delta, args.tau, args.cpu_seconds, ncores, pv=args.pv)
         tcpu = run_cpu_oracle(pool, tasks)
         res["cpu_baseline"] = {"value": sflops / tcpu / 1e12, "unit": "TFLOP/s", "cores": ncores, "kind": "oracle",
                                "sample": f"{sum(len(x[3]) for x in tasks)} query tiles of {w.name}, {tcpu:.1f} s"}
@@ -489,7 +498,7 @@ def main():
         tiles = sp.sample_tiles(w.batch, w.heads_q, w.seqlen, args.parity_tiles, seed=args.seed)
         ptasks, pkeys = sp.make_tasks(q, k, v, tiles, bf16=w.dtype == "bf16", heads_q=w.heads_q,
                                       heads_kv=w.heads_kv, mask=w.mask, window=w.window, delta=args.delta,
-                                      tau=args.tau, out_dtype=w.dtype)
+                                      tau=args.tau, out_dtype=w.dtype, pv=args.pv)
         presults = pool.map(sp.oracle_task, ptasks)
         par = sp.compare(presults, pkeys, out_h, lse_h, mask_h, w.dtype, w.seqlen, w.mask, w.window)
         par["sample"] = (f"{par['tiles']} query tiles (64 rows, all their keys) of the last timed step's "

@@ -69,6 +69,18 @@ typedef enum {
   LAMP_FORCE_ALL8 = 2    /* no sub-block is recomputed (plain 8-bit path) */
 } lamp_force;
 
+/* Precision of P.V.  The paper ("LampAttention: Look-Ahead Mixed-Precision
+ * FlashAttention for Dedicated Accelerators", abstract) puts the key-query
+ * products and their exponentials in 8 bits and does not say how P.V is
+ * computed. */
+typedef enum {
+  LAMP_PV_FP16 = 0,  /* P and V as FP16 for every row (P8 is exact in FP16) */
+  LAMP_PV_FP8 = 1    /* rows of unflagged sub-blocks: P8 . fl8(v) on the FP8
+                        tensor path (V rounded once, RNE, saturating); rows of
+                        flagged sub-blocks keep P16 . fp16(v).  head_dim 64 or
+                        128 (LAMP_ERR_UNSUPPORTED for 256) */
+} lamp_pv_mode;
+
 /* Counter slots of lamp_stats.counters (uint64 each). */
 enum {
   LAMP_CNT_TILES = 0,       /* visited 64x64 tiles (>= 1 visible entry) */
@@ -118,6 +130,8 @@ typedef struct {
   void* stage_events[3]; /* optional cudaEvent_t, recorded on `stream` before the
                             pre-pass, between it and the fused kernel, and after
                             the fused kernel (per-stage timing); NULL = none */
+  int32_t pv_mode;       /* lamp_pv_mode; 0 = LAMP_PV_FP16 (zero-initialised
+                            shapes keep the FP16 path) */
 } lamp_shapes;
 
 typedef struct {
@@ -153,8 +167,9 @@ int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out,
                   float delta, float tau, lamp_stats* stats);
 
 /* Bytes of device workspace lamp_attn_fwd needs for these shapes (E4M3
- * copies of q and k, an fp16 copy of v, bf16 copies of fp32 inputs, and
- * per-row norms).  0 on invalid shapes. */
+ * copies of q and k, an fp16 copy of v, bf16 copies of fp32 inputs,
+ * per-row norms and, for LAMP_PV_FP8, an E4M3 copy of v).  0 on invalid
+ * shapes. */
 size_t lamp_attn_workspace_bytes(const lamp_shapes* shapes);
 
 /*
@@ -249,6 +264,7 @@ size_t lamp_attn_host_buffer_bytes(const lamp_shapes* shapes);
  *             ones (HIST0..2, FLAGGED, RECOMP_STEPS, SPEC_WASTE, RECOMP_LATE
  *             stay 0);
  *             stats->mask is not written.
+ * shapes->pv_mode is not used (the pass computes no P.V).
  * Asynchronous on shapes->stream; errors as lamp_attn_fwd.
  */
 int lamp_attn_tau_sweep(const void* q, const void* k, const lamp_shapes* shapes,

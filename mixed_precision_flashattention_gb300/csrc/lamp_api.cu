@@ -14,7 +14,9 @@
 
 namespace lamp {
 cudaError_t launch_prep(const PrepParams& p, int d, cudaStream_t st);
-cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st, bool sweep);
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st, bool sweep, bool pv8);
+cudaError_t launch_v8t(const void* v, const int64_t* vs, bool in_f32, uint8_t* v8t, int B, int N, int Hkv, int D,
+                       cudaStream_t st);
 cudaError_t launch_sweep_hist(const uint32_t* rec, long long n, const SweepCodes& tcode, int ntau,
                               unsigned long long* hist, cudaStream_t st);
 
@@ -71,7 +73,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* bas
 }
 
 struct WsLayout {
-  size_t q8, k8, v16, q16, k16, nq, nqc, nk, nkc, abort, total;
+  size_t q8, k8, v16, q16, k16, v8t, nq, nqc, nk, nkc, abort, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -87,6 +89,9 @@ WsLayout ws_layout(const lamp_shapes& s) {
   if (s.in_dtype == LAMP_DT_FP32) {
     w.q16 = o; o = align256(o + B * Hq * N * D * 2);
     w.k16 = o; o = align256(o + B * Hkv * N * D * 2);
+  }
+  if (s.pv_mode == LAMP_PV_FP8) {  // [B, Hkv, D, T * 64]: keys contiguous
+    w.v8t = o; o = align256(o + B * Hkv * D * T * kBN);
   }
   w.nq = o; o = align256(o + B * Hq * N * 4);
   w.nqc = o; o = align256(o + B * Hq * N * (D / 32) * 4);
@@ -104,6 +109,7 @@ bool shapes_ok(const lamp_shapes* s) {
   if (s->in_dtype != LAMP_DT_BF16 && s->in_dtype != LAMP_DT_FP32) return false;
   if (s->out_dtype != LAMP_DT_BF16 && s->out_dtype != LAMP_DT_FP32) return false;
   if (s->force < LAMP_FORCE_OFF || s->force > LAMP_FORCE_ALL8) return false;
+  if (s->pv_mode != LAMP_PV_FP16 && s->pv_mode != LAMP_PV_FP8) return false;
   if (!(s->softmax_scale >= 0.0f) || std::isinf(s->softmax_scale)) return false;
   return true;
 }
@@ -131,7 +137,7 @@ const char* lamp_strerror(int status) {
   switch (status) {
     case LAMP_OK: return "ok";
     case LAMP_ERR_INVALID_ARG: return "invalid argument (pointer, shape, stride, dtype or threshold)";
-    case LAMP_ERR_UNSUPPORTED: return "unsupported (head_dim must be 64/128/256 on an sm_103 GPU)";
+    case LAMP_ERR_UNSUPPORTED: return "unsupported (head_dim must be 64/128/256, 64/128 with FP8 P.V, on an sm_103 GPU)";
     case LAMP_ERR_CUDA: return "CUDA runtime or driver error";
     case LAMP_ERR_TIMEOUT: return "a device-side wait exceeded its time limit";
     case LAMP_ERR_WORKSPACE: return "workspace smaller than lamp_attn_workspace_bytes()";
@@ -149,6 +155,7 @@ void lamp_exp8_table(uint8_t out[256]) {
 size_t lamp_attn_workspace_bytes(const lamp_shapes* shapes) {
   if (!shapes_ok(shapes)) return 0;
   if (shapes->head_dim != 64 && shapes->head_dim != 128 && shapes->head_dim != 256) return 0;
+  if (shapes->pv_mode == LAMP_PV_FP8 && shapes->head_dim == 256) return 0;  // no FP8 P.V at d = 256
   return ws_layout(*shapes).total;
 }
 
@@ -167,6 +174,10 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   const lamp_shapes& s = *shapes;
   const int D = s.head_dim;
   if (D != 64 && D != 128 && D != 256) return LAMP_ERR_UNSUPPORTED;
+  // FP8 P.V: the kernel's shared memory holds the extra P8 and V8 tiles only
+  // at d <= 128 (the tau sweep computes no P.V and ignores the mode)
+  const bool pv8 = !sweep && s.pv_mode == LAMP_PV_FP8;
+  if (pv8 && D == 256) return LAMP_ERR_UNSUPPORTED;
   if (mask_kind < LAMP_MASK_NONE || mask_kind > LAMP_MASK_SLIDING) return LAMP_ERR_INVALID_ARG;
   if (mask_kind == LAMP_MASK_SLIDING && s.window < 1) return LAMP_ERR_INVALID_ARG;
   if (!(delta >= 0.0f) || std::isnan(tau)) return LAMP_ERR_INVALID_ARG;
@@ -214,6 +225,11 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   if (!sweep)
     ok &= make_map(&fp.tmV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws + w.v16, D, N, Hkv, B, D, NDk, NDk * Hkv, 64, kBN,
                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (pv8) {  // V8t: dims (keys, d, Hkv, B), rows of T * 64 keys; keys >= N read as 0
+    const long long Np = (long long)T * kBN;
+    ok &= make_map(&fp.tmV8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ws + w.v8t, N, D, Hkv, B, Np, Np * D, Np * D * Hkv,
+                   kBN, D, CU_TENSOR_MAP_SWIZZLE_64B);
+  }
   if (s.in_dtype == LAMP_DT_FP32) {
     ok &= make_map(&fp.tmQ16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + w.q16, D, N, Hq, B, D, NDq, NDq * Hq, 64, kBM,
                    CU_TENSOR_MAP_SWIZZLE_128B);
@@ -284,9 +300,11 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   };
   if (!mark(0)) return fail(LAMP_ERR_CUDA);
   if (launch_prep(pp, D, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
+  if (pv8 && launch_v8t(v, s.v_stride, s.in_dtype == LAMP_DT_FP32, ws + w.v8t, B, N, Hkv, D, stream) != cudaSuccess)
+    return fail(LAMP_ERR_CUDA);
   if (!mark(1)) return fail(LAMP_ERR_CUDA);
 
-  if (launch_fwd(fp, D, stream, sweep) != cudaSuccess) return fail(LAMP_ERR_CUDA);
+  if (launch_fwd(fp, D, stream, sweep, pv8) != cudaSuccess) return fail(LAMP_ERR_CUDA);
   if (!mark(2)) return fail(LAMP_ERR_CUDA);
   if (own_ws && cudaFreeAsync(ws, stream) != cudaSuccess) return LAMP_ERR_CUDA;
   return LAMP_OK;

@@ -21,6 +21,7 @@ struct SweepCodes {
 // Kernel parameters (passed by value as a __grid_constant__).
 struct FwdParams {
   CUtensorMap tmQ8, tmQ16, tmK8, tmK16, tmV;
+  CUtensorMap tmV8;    // FP8 P.V: V8t = fl8(v) as [B, Hkv, D, keys] (keys contiguous)
   void* out;
   float* lse;
   uint8_t* mask;
@@ -81,6 +82,16 @@ __device__ __forceinline__ uint32_t swz_offset(int r, int x, int rows, int row_b
   return (uint32_t)(col * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + chunk * 16 + (w & 15));
 }
 
+// E4M3 codes (low byte: the low element) of fl8(e^x) for the two E4M3 codes
+// in x8 (non-positive x); exp8_f16x2 gives their values as f16x2.
+__device__ __forceinline__ uint32_t exp8_code2(uint32_t x8) {
+  const uint32_t h = e4m3x2_to_f16x2((uint16_t)x8);
+  __half2 xv;
+  memcpy(&xv, &h, 4);
+  const float2 xf = __fmul2_rn(make_float2(__low2float(xv), __high2float(xv)), make_float2(kLog2e, kLog2e));
+  return cvt_e4m3x2(ex2_approx(xf.y), ex2_approx(xf.x));
+}
+
 // f16x2 values of fl8(e^x) for the two E4M3 codes in x8 (non-positive x):
 // e^x in fp32 (ex2 of x log2 e: relative error below 2^-20), then one E4M3
 // rounding to nearest even.  Exact for every such code: among the E4M3
@@ -88,11 +99,7 @@ __device__ __forceinline__ uint32_t swz_offset(int r, int x, int rows, int row_b
 // rounding boundary is x = -2^-5, at 2^-11 relative -- far beyond the fp32
 // error; below 2^-11, e^x rounds to 0 either way.
 __device__ __forceinline__ uint32_t exp8_f16x2(uint32_t x8) {
-  const uint32_t h = e4m3x2_to_f16x2((uint16_t)x8);
-  __half2 xv;
-  memcpy(&xv, &h, 4);
-  const float2 xf = __fmul2_rn(make_float2(__low2float(xv), __high2float(xv)), make_float2(kLog2e, kLog2e));
-  return e4m3x2_to_f16x2(cvt_e4m3x2(ex2_approx(xf.y), ex2_approx(xf.x)));
+  return e4m3x2_to_f16x2((uint16_t)exp8_code2(x8));
 }
 
 // Exact product of two E4M3 codes, times 2^18 (an integer below 2^36): every
@@ -237,6 +244,18 @@ struct Mma {
       const uint64_t ad = make_sdesc(pbase + kk * 32, 16, 1024, kLayoutSW128);
       const uint64_t bd = make_sdesc(vbase + kk * 16 * 128, 64 * 128, 1024, kLayoutSW128);
       mma_f16(tmem_o, ad, bd, idesc_v, acc || kk > 0);
+    }
+  }
+  // O[128 x D] (+)= P8[128 x 64] . V8[64 x D]  (E4M3 operands, FP32
+  // accumulation).  Both K-major with 64-byte swizzled rows of 64 keys: the
+  // P8 tile [128 rows x 64 keys], V8t [D rows x 64 keys].
+  static __device__ __forceinline__ void pv8(uint32_t tmem_o, uint32_t p8base, uint32_t v8base, bool acc) {
+    constexpr uint32_t idesc = make_idesc(0, 0, 0, 128, D);
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const uint64_t ad = make_sdesc(p8base + kk * 32, 16, 512, kLayoutSW64);
+      const uint64_t bd = make_sdesc(v8base + kk * 32, 16, 512, kLayoutSW64);
+      mma_f8(tmem_o, ad, bd, idesc, acc || kk > 0);
     }
   }
 };

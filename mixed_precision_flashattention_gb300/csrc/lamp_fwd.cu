@@ -40,9 +40,11 @@
 
 namespace lamp {
 
-template <int D>
+template <int D, bool PV8 = false>
 struct Cfg {
-  static constexpr int NT = (D == 256) ? 1 : 2;  // query tiles of 128 rows per CTA
+  // query tiles of 128 rows per CTA: one at d = 256, and at d = 128 with the
+  // FP8 P.V (whose P8 and V8 tiles leave no room for a second tile)
+  static constexpr int NT = (D == 256 || (PV8 && D == 128)) ? 1 : 2;
   static constexpr int NS = (D == 256) ? 1 : 2;  // K/V stages
   static constexpr int SM_THREADS = 256;                // softmax threads per tile (2 per row)
   static constexpr int THREADS = 32 * (8 * NT + 1 + NT);
@@ -54,8 +56,14 @@ struct Cfg {
   static constexpr int K8_BYTES = kBN * D;
   static constexpr int K16_BYTES = kBN * D * 2;
   static constexpr int V_BYTES = (D / 64) * kBN * 128;
-  static constexpr int STAGE_BYTES = K8_BYTES + K16_BYTES + V_BYTES;
-  static constexpr int P_BYTES = kBM * kBN * 2;
+  // FP8 P.V: V8t [D rows x 64 keys] E4M3 after V16 in the stage, and the P8
+  // tile [128 rows x 64 keys] after the P16 tile (both 64-byte swizzled)
+  static_assert(!(PV8 && D == 256), "no FP8 P.V at d = 256");
+  static constexpr int V8_BYTES = PV8 ? kBN * D : 0;
+  static constexpr int OFF_V8 = K8_BYTES + K16_BYTES + V_BYTES;  // inside a stage
+  static constexpr int STAGE_BYTES = K8_BYTES + K16_BYTES + V_BYTES + V8_BYTES;
+  static constexpr int P16_BYTES = kBM * kBN * 2;
+  static constexpr int P_BYTES = P16_BYTES + (PV8 ? kBM * kBN : 0);
   static constexpr int OFF_Q = 0;  // tile t: Q8 at t*QT_BYTES, Q16 right after
   static constexpr int OFF_ST = NT * QT_BYTES;
   // one stage (d = 256): a second K8 slot, so the next key's K8 is loaded
@@ -272,11 +280,12 @@ __device__ __noinline__ float q8_from_q16(uint8_t* q8w, int t, int hf, uint32_t 
   return ss;
 }
 
-template <int D, int kMode>
-__global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __grid_constant__ FwdParams p) {
+template <int D, int kMode, bool kPV8>
+__global__ void __launch_bounds__(Cfg<D, kPV8>::THREADS, 1) lamp_fwd_kernel(const __grid_constant__ FwdParams p) {
   constexpr bool kSweep = kMode == 2;
   constexpr bool kNoStage1 = kMode == 1;
-  using C = Cfg<D>;
+  static_assert(!(kSweep && kPV8), "the sweep pass computes no P.V");
+  using C = Cfg<D, kPV8>;
   extern __shared__ uint8_t smem_raw[];
   // align by pointer arithmetic on the __shared__ array so that every access
   // through `smem` stays a shared-memory access
@@ -347,6 +356,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
         prefetch_tmap(&p.tmQ16);
         prefetch_tmap(&p.tmK16);
         prefetch_tmap(&p.tmV);
+        if (kPV8) prefetch_tmap(&p.tmV8);
       }
       // Q8 comes from the pre-pass, or (bf16 q) the softmax makes it from Q16
       const bool load_q8 = kSweep || !p.q8_in_cta;
@@ -426,6 +436,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
             tma_load_4d(st + C::K8_BYTES + c * kBN * 128, &p.tmK16, fb, c * 64, key0, g, b);
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(st + C::K8_BYTES + C::K16_BYTES + c * kBN * 128, &p.tmV, fb, c * 64, key0, g, b);
+          if (kPV8) tma_load_4d(st + C::OFF_V8, &p.tmV8, fb, key0, 0, g, b);  // V8t rows of d, 64 keys each
         }
         if (s) uses1 = u + 1; else uses0 = u + 1;
       }
@@ -453,8 +464,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       auto kv = [&](int j) { return sbase + C::OFF_ST + stage_of(j) * C::STAGE_BYTES; };
       const uint32_t tm = tmem + t * C::TILE_COLS;
       const uint32_t qbase = sbase + C::OFF_Q + t * C::QT_BYTES;
-      auto pv = [&](int i) {
-        Mma<D>::pv(tm, sbase + C::OFF_P + t * C::P_BYTES, kv(jlo + i) + C::K8_BYTES + C::K16_BYTES, i > 0);
+      // P.V of step i; any16: the step has a flagged sub-block
+      auto pv = [&](int i, bool any16) {
+        const uint32_t pb = sbase + C::OFF_P + t * C::P_BYTES, vb = kv(jlo + i) + C::K8_BYTES + C::K16_BYTES;
+        if constexpr (kPV8) {
+          // rows of unflagged sub-blocks: P8 . V8 (the P8 tile is 0 in the
+          // flagged rows); rows of flagged ones: P16 . V16, issued only when
+          // the step has one (the P16 tile is then 0 in the other rows)
+          Mma<D>::pv8(tm, pb + C::P16_BYTES, kv(jlo + i) + C::OFF_V8, i > 0);
+          if (any16) Mma<D>::pv(tm, pb, vb, true);
+        } else {
+          Mma<D>::pv(tm, pb, vb, i > 0);
+        }
         mma_commit(bar(M_PV_DONE + 8 * t));
         mma_commit(bar(M_KV_EMPTY + 16 * stage_of(jlo + i) + 8 * t));
       };
@@ -602,7 +623,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           ok = wait_bar(cx, bar(M_P_FULL + 8 * t), (i - 1) & 1);
           if (!ok) break;
           tc_fence_after();
-          pv(i - 1);
+          pv(i - 1, prev);
         }
         if (spec) qk16(i);
       }
@@ -617,7 +638,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       if (ok) ok = wait_bar(cx, bar(M_P_FULL + 8 * t), (n - 1) & 1);
       if (ok) {
         tc_fence_after();
-        pv(n - 1);
+        pv(n - 1, any_of(n - 1));
       }
       // make sure no MMA of this warp still writes TMEM before it is released
       mma_commit(bar(M_DRAIN + 8 * t));
@@ -1117,16 +1138,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
       // to the single rounding for E4M3 operands), P8 = fl8(e^x8) (exact,
       // exp8_f16x2); rows of flagged sub-blocks take P16 below instead
       uint32_t pw[NC / 2];
+      uint32_t pc[kPV8 ? NC / 4 : 1];  // FP8 P.V: the P8 codes, four a word
 #pragma unroll
       for (int i = 0; i < NC / 2; ++i) pw[i] = 0u;
+#pragma unroll
+      for (int i = 0; i < (kPV8 ? NC / 4 : 1); ++i) pc[i] = 0u;
       const bool want_p8 = rowvis && !my_flag;
       if (__any_sync(0xffffffffu, want_p8)) {  // warp-uniform: most warps have only flagged rows
         const __half2 mh = __float2half2_rn(m_new);
 #pragma unroll
         for (int i = 0; i < NC / 2; ++i) {
           const __half2 xh = __hsub2(as_half2(s8h[i]), mh);
-          const uint32_t v = exp8_f16x2(cvt_e4m3x2_f16x2(xh));
-          pw[i] = want_p8 ? v : 0u;
+          const uint32_t c2 = exp8_code2(cvt_e4m3x2_f16x2(xh));
+          pw[i] = want_p8 ? e4m3x2_to_f16x2((uint16_t)c2) : 0u;
+          if constexpr (kPV8) pc[i >> 1] |= (want_p8 ? c2 : 0u) << (16 * (i & 1));
         }
       }
 
@@ -1194,11 +1219,29 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
           for (int i = 0; i < NC / 2; ++i) add_f32_f16x2(ls[2 * (i & 1)], ls[2 * (i & 1) + 1], pw[i]);
           l = fmaf(alpha, l, (ls[0] + ls[1]) + (ls[2] + ls[3]));
         }
-        // P row half -> shared memory (K-major, 128-byte swizzle)
+        if constexpr (kPV8) {
+          // the P8 tile (K-major, 64-byte swizzle; 0 in rows of flagged
+          // sub-blocks) and, when the step has a flagged sub-block, the P16
+          // tile with P16 in those rows and 0 in the others
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 v4 = make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
-          *reinterpret_cast<uint4*>(sP + swz_offset(t, (4 * hf + k) * 16, kBM, 128)) = v4;
+          for (int k = 0; k < 2; ++k)
+            *reinterpret_cast<uint4*>(sP + C::P16_BYTES + swz_offset(t, hf * 32 + 16 * k, kBM, 64)) =
+                make_uint4(pc[4 * k], pc[4 * k + 1], pc[4 * k + 2], pc[4 * k + 3]);
+          if (any) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint4 v4 = my_flag ? make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3])
+                                       : make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(sP + swz_offset(t, (4 * hf + k) * 16, kBM, 128)) = v4;
+            }
+          }
+        } else {
+          // P row half -> shared memory (K-major, 128-byte swizzle)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 v4 = make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
+            *reinterpret_cast<uint4*>(sP + swz_offset(t, (4 * hf + k) * 16, kBM, 128)) = v4;
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -1280,30 +1323,35 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) lamp_fwd_kernel(const __gr
 }
 
 // ---------------------------------------------------------------- launcher
-template <int D, int kMode>
+template <int D, int kMode, bool kPV8>
 static cudaError_t launch_fwd_d(FwdParams p, cudaStream_t st) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kPV8>;
   cudaError_t e =
-      cudaFuncSetAttribute(lamp_fwd_kernel<D, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      cudaFuncSetAttribute(lamp_fwd_kernel<D, kMode, kPV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   p.nqb = (p.N + kBM * C::NT - 1) / (kBM * C::NT);
   const unsigned grid = (unsigned)p.nqb * (unsigned)p.B * (unsigned)p.Hq;
   if (grid == 0) return cudaSuccess;
-  lamp_fwd_kernel<D, kMode><<<grid, C::THREADS, C::SMEM, st>>>(p);
+  lamp_fwd_kernel<D, kMode, kPV8><<<grid, C::THREADS, C::SMEM, st>>>(p);
   return cudaGetLastError();
 }
 
 template <int D>
-static cudaError_t launch_fwd_mode(const FwdParams& p, cudaStream_t st, bool sweep) {
-  if (sweep) return launch_fwd_d<D, 2>(p, st);
-  return p.delta_code == 0u ? launch_fwd_d<D, 1>(p, st) : launch_fwd_d<D, 0>(p, st);
+static cudaError_t launch_fwd_mode(const FwdParams& p, cudaStream_t st, bool sweep, bool pv8) {
+  if (sweep) return launch_fwd_d<D, 2, false>(p, st);
+  if constexpr (D != 256) {
+    if (pv8) return p.delta_code == 0u ? launch_fwd_d<D, 1, true>(p, st) : launch_fwd_d<D, 0, true>(p, st);
+  } else {
+    if (pv8) return cudaErrorInvalidValue;
+  }
+  return p.delta_code == 0u ? launch_fwd_d<D, 1, false>(p, st) : launch_fwd_d<D, 0, false>(p, st);
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st, bool sweep) {
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st, bool sweep, bool pv8) {
   switch (d) {
-    case 64: return launch_fwd_mode<64>(p, st, sweep);
-    case 128: return launch_fwd_mode<128>(p, st, sweep);
-    case 256: return launch_fwd_mode<256>(p, st, sweep);
+    case 64: return launch_fwd_mode<64>(p, st, sweep, pv8);
+    case 128: return launch_fwd_mode<128>(p, st, sweep, pv8);
+    case 256: return launch_fwd_mode<256>(p, st, sweep, pv8);
     default: return cudaErrorInvalidValue;
   }
 }

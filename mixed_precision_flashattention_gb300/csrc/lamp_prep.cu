@@ -257,6 +257,71 @@ static cudaError_t launch_prep_d(const PrepParams& p0, cudaStream_t st) {
   return w64 ? launch_prep_t<D, false, true>(p, ngroups, st) : launch_prep_t<D, false, false>(p, ngroups, st);
 }
 
+// V8t = fl8(v) (E4M3, RNE, saturating, from the input values), transposed
+// per (batch, kv head) to [B, Hkv, D, Npad] bytes with the keys contiguous:
+// the K-major B operand of the FP8 P.V.  One block per 64 keys x 64
+// elements of d of one (batch, kv head), through shared memory: a thread
+// loads 16 consecutive elements of one key row and, after the transpose,
+// stores 16 consecutive keys of one row of d.  Keys >= N are written as 0.
+template <bool F32>
+__global__ void __launch_bounds__(256) lamp_v8t_kernel(const void* __restrict__ v, long long vs0, long long vs1,
+                                                       long long vs2, uint8_t* __restrict__ v8t, int N, int D,
+                                                       int Hkv, int Npad) {
+  __shared__ __align__(16) uint8_t tile[64][80];  // [element of d][key], rows padded to 80 bytes
+  const int k0 = blockIdx.x * 64, d0 = blockIdx.y * 64, bh = blockIdx.z;
+  const int b = bh / Hkv, g = bh - b * Hkv;
+  const int tid = threadIdx.x;
+  const int kr = tid >> 2, dc = (tid & 3) * 16, key = k0 + kr;
+  float x[16];
+  if (key < N) {
+    const long long off = (long long)b * vs0 + (long long)key * vs1 + (long long)g * vs2 + d0 + dc;
+    if constexpr (F32) {
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(v) + off);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 f = src[i];
+        x[4 * i] = f.x; x[4 * i + 1] = f.y; x[4 * i + 2] = f.z; x[4 * i + 3] = f.w;
+      }
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(v) + off);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint4 w = src[i];
+        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          x[8 * i + 2 * j] = __uint_as_float(wd[j] << 16);
+          x[8 * i + 2 * j + 1] = __uint_as_float(wd[j] & 0xFFFF0000u);
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = 0.0f;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const uint16_t c = cvt_e4m3x2(x[i + 1], x[i]);
+    tile[dc + i][kr] = (uint8_t)(c & 0xFFu);
+    tile[dc + i + 1][kr] = (uint8_t)(c >> 8);
+  }
+  __syncthreads();
+  const int dr = tid >> 2, kc = (tid & 3) * 16;
+  *reinterpret_cast<uint4*>(v8t + ((size_t)bh * D + d0 + dr) * (size_t)Npad + k0 + kc) =
+      *reinterpret_cast<const uint4*>(&tile[dr][kc]);
+}
+
+cudaError_t launch_v8t(const void* v, const int64_t* vs, bool in_f32, uint8_t* v8t, int B, int N, int Hkv, int D,
+                       cudaStream_t st) {
+  const int T = (N + kBN - 1) / kBN;
+  const dim3 grid((unsigned)T, (unsigned)(D / 64), (unsigned)(B * Hkv));
+  if (in_f32)
+    lamp_v8t_kernel<true><<<grid, 256, 0, st>>>(v, vs[0], vs[1], vs[2], v8t, N, D, Hkv, T * kBN);
+  else
+    lamp_v8t_kernel<false><<<grid, 256, 0, st>>>(v, vs[0], vs[1], vs[2], v8t, N, D, Hkv, T * kBN);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prep(const PrepParams& p, int d, cudaStream_t st) {
   switch (d) {
     case 64: return launch_prep_d<64>(p, st);

@@ -21,12 +21,12 @@ def values(t):
 
 
 def run_gpu(qd, kd, vd, *, mask="causal", window=0, delta=2.0 ** -8, tau=0.5, force="off",
-            out_dtype=None, scale=0.0):
+            out_dtype=None, scale=0.0, pv="fp16"):
     B, N, Hq, d = qd.shape
     mbytes, cnt = lamp.new_stats(B, Hq, N)
     out, lse, _, _ = lamp.lamp_attn_fwd(qd, kd, vd, mask=mask, window=window, delta=delta, tau=tau,
                                         force=force, out_dtype=out_dtype, mask_bytes=mbytes,
-                                        counters=cnt, scale=scale)
+                                        counters=cnt, scale=scale, pv=pv)
     torch.cuda.synchronize()
     return (out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
             mbytes.cpu().numpy(), cnt.cpu().numpy())

@@ -62,6 +62,26 @@ def test_workspace_bytes(lib):
     assert lib.lamp_attn_workspace_bytes(ctypes.byref(sh)) == 0
     sh = _shapes(dtype=1)
     assert lib.lamp_attn_workspace_bytes(ctypes.byref(sh)) > n
+    # FP8 P.V: plus an E4M3 copy of v, transposed to rows of T * 64 keys
+    sh = _shapes()
+    sh.pv_mode = 1
+    n8 = lib.lamp_attn_workspace_bytes(ctypes.byref(sh))
+    assert n + B * Hkv * d * 64 * 64 <= n8 <= n + B * Hkv * d * 64 * 64 + 256
+    sh.head_dim = 256
+    assert lib.lamp_attn_workspace_bytes(ctypes.byref(sh)) == 0
+    sh.pv_mode = 2
+    sh.head_dim = 128
+    assert lib.lamp_attn_workspace_bytes(ctypes.byref(sh)) == 0
+
+
+def test_shapes_struct_matches_the_header():
+    """The ctypes mirror ends with the same field as the C struct, at the
+    offset the C layout gives it (pv_mode after the three event handles)."""
+    assert lamp.LampShapes._fields_[-1][0] == "pv_mode"
+    assert lamp.LampShapes.pv_mode.offset == lamp.LampShapes.stage_events.offset + 3 * ctypes.sizeof(ctypes.c_void_p)
+    src = open(os.path.join(ROOT, "include", "lamp_attn.h")).read()
+    body = src[src.index("typedef struct {\n  int32_t batch"):src.index("} lamp_shapes;")]
+    assert body.rstrip().splitlines()[-2].strip().startswith("int32_t pv_mode;")
 
 
 def _call(lib, sh, ptrs=(16, 32, 48, 64), mask=1, delta=2 ** -8, tau=0.5):
@@ -84,6 +104,12 @@ def test_argument_errors_before_launch(lib):
     assert _call(lib, _shapes(), ptrs=(17, 32, 48, 64)) == lamp.LAMP_ERR_INVALID_ARG
     sh = _shapes()
     sh.seqlen = 0
+    assert _call(lib, sh) == lamp.LAMP_ERR_INVALID_ARG
+    sh = _shapes(d=256)
+    sh.pv_mode = 1  # no FP8 P.V at d = 256
+    assert _call(lib, sh) == lamp.LAMP_ERR_UNSUPPORTED
+    sh = _shapes()
+    sh.pv_mode = 3
     assert _call(lib, sh) == lamp.LAMP_ERR_INVALID_ARG
 
 
