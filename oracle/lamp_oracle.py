@@ -40,6 +40,12 @@ the rest supports (each is listed in the design notes):
      (float64); out = O / l, LSE = m + ln l.
   R9 a tile is visited iff it holds at least one visible (row, key) pair;
      the per-tile histogram counts flagged sub-blocks of visited tiles.
+  R15 (optional mode qk="chunk32"; a literal reading of "accumulated in
+     8-bit formats" with a 32-term dot-product unit) the products of each
+     32-element chunk of d are summed exactly, A_c, and the running 8-bit
+     value takes each chunk in ascending order:
+     a_c = fl8(a_{c-1} + A_c * sigma) (float64 product and sum), a_0 = 0,
+     S8 = the last a_c.  With one chunk (d <= 32) this is R2.
   R14 (optional mode pv="fp8"; the pages do not say in which precision
      P.V runs) rows of unflagged sub-blocks multiply their P8 (already
      E4M3) with V8 = fl8(v), one saturating RNE rounding from the input
@@ -90,7 +96,7 @@ def visibility(rows: np.ndarray, cols: np.ndarray, n: int, mask: str,
 
 
 def _qtile_block(q_rows, k_h, v_h, rows, n, sigma, mask, window, delta, tau,
-                 force, pv="fp16"):
+                 force, pv="fp16", qk="exact"):
     """One head, a stack of query tiles: q_rows [nI, 64, d] (values as given),
     rows [nI, 64] absolute row indices.  Returns O, l, m, mask bytes, counts."""
     nI = q_rows.shape[0]
@@ -103,10 +109,17 @@ def _qtile_block(q_rows, k_h, v_h, rows, n, sigma, mask, window, delta, tau,
     v8 = e4m3_round(v_h) if pv == "fp8" else None  # R14
     d = q_rows.shape[-1]
 
-    # R2: exact sum of 8-bit products, scaled in float64, rounded once
-    A = q8 @ k8.T  # [nI, 64, N]
-    y = A * sigma
-    S8 = e4m3_round(y)
+    if qk == "chunk32":
+        # R15: one 8-bit rounding after each 32-element chunk of d
+        S8 = np.zeros((nI, TILE, k8.shape[0]))
+        for c0 in range(0, d, 32):
+            Ac = q8[..., c0:c0 + 32] @ k8[:, c0:c0 + 32].T  # exact
+            S8 = e4m3_round(S8 + Ac * sigma)
+    else:
+        # R2: exact sum of 8-bit products, scaled in float64, rounded once
+        A = q8 @ k8.T  # [nI, 64, N]
+        y = A * sigma
+        S8 = e4m3_round(y)
 
     m = np.full((nI, TILE), -np.inf)
     l = np.zeros((nI, TILE))
@@ -183,13 +196,15 @@ def _qtile_block(q_rows, k_h, v_h, rows, n, sigma, mask, window, delta, tau,
 
 def lamp_forward(q, k, v, *, mask="causal", window=0, scale=None,
                  delta=2.0 ** -8, tau=2.0 ** -1, force="off", out_dtype="bf16",
-                 tiles=None, chunk_elems=1 << 24, pv="fp16") -> LampResult:
+                 tiles=None, chunk_elems=1 << 24, pv="fp16", qk="exact") -> LampResult:
     """The LAMP emulation on float64 arrays holding the input values.
 
     q [B, N, Hq, d], k/v [B, N, Hkv, d].  ``tiles``: None for every query
     tile, else an iterable of (b, h, i) query tiles to compute (others are
     left NaN / zero).  ``out_dtype`` in {"bf16", "fp32"}.  ``pv`` in
-    {"fp16", "fp8"}: the P.V operands of unflagged sub-blocks (R8 / R14)."""
+    {"fp16", "fp8"}: the P.V operands of unflagged sub-blocks (R8 / R14).
+    ``qk`` in {"exact", "chunk32"}: how the 8-bit logits accumulate (R2 /
+    R15)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -201,6 +216,8 @@ def lamp_forward(q, k, v, *, mask="causal", window=0, scale=None,
         raise ValueError(force)
     if pv not in ("fp16", "fp8"):
         raise ValueError(pv)
+    if qk not in ("exact", "chunk32"):
+        raise ValueError(qk)
     sigma = (1.0 / np.sqrt(float(d))) if scale is None else float(scale)
     T = (n + TILE - 1) // TILE
     grp = Hq // Hkv
@@ -231,7 +248,7 @@ def lamp_forward(q, k, v, *, mask="causal", window=0, scale=None,
             q_rows[ok] = q[b, rows[ok], h, :]
             O, l, m, mb, cn = _qtile_block(q_rows, k[b, :, g, :], v[b, :, g, :],
                                            rows, n, sigma, mask, window,
-                                           delta, tau, force, pv)
+                                           delta, tau, force, pv, qk)
             cnt += cn
             mbytes[b, h, idx, :] = mb
             with np.errstate(invalid="ignore", divide="ignore"):

@@ -104,10 +104,12 @@ def _e4m3_int(x):
 
 
 def lamp8_rowloop(q, k, v, *, mask="causal", window=0, scale=None,
-                  delta=2.0 ** -8, tau=2.0 ** -1, rows=None, b=0, h=0, pv="fp16"):
+                  delta=2.0 ** -8, tau=2.0 ** -1, rows=None, b=0, h=0, pv="fp16", chunk=None):
     """All-8-bit path, one row at a time, for rows of head (b, h).
 
     ``pv``: the V operand of P.V, "fp16" (f16(v)) or "fp8" (fl8(v)).
+    ``chunk``: None for one rounding of the whole dot product, else the
+    number of terms after which the running logit is rounded to 8 bits.
 
     Returns dict row -> (out_row, lse, {tile: (stage1_bit, flag_bit)}),
     where the per-tile bits say whether that row alone would pass stage 1 /
@@ -136,12 +138,16 @@ def lamp8_rowloop(q, k, v, *, mask="causal", window=0, scale=None,
                 continue
             s8 = {}
             for c in cols:
-                acc = 0
                 kc = ki[c]
-                for t in range(d):
-                    acc += qr[t] * int(kc[t])
-                y = (acc * 2.0 ** -18) * sigma  # exact integer -> float64, one product
-                s8[c] = float(e4m3_round(y))
+                step = d if chunk is None else chunk
+                run = 0.0  # the running 8-bit value
+                for t0 in range(0, d, step):
+                    acc = 0
+                    for t in range(t0, min(t0 + step, d)):
+                        acc += qr[t] * int(kc[t])
+                    # exact integer -> float64, one product, one sum
+                    run = float(e4m3_round(run + (acc * 2.0 ** -18) * sigma))
+                s8[c] = run
             m_new = max(m, max(s8.values()))
             alpha = 0.0 if m == -math.inf else math.exp(m - m_new)
             l *= alpha

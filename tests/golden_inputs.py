@@ -31,3 +31,16 @@ def detector_2tile_inputs(fx=None):
     rng = np.random.default_rng(7)
     v = rng.standard_normal((1, n, 1, d)).astype(np.float32)
     return q, k, v
+
+
+def chunk32_inputs():
+    """Inputs of chunk32_rounding.json: q, k, v float64 [1, 2, 1, 64]."""
+    d = 64
+    q = np.ones((1, 2, 1, d))
+    k = np.zeros((1, 2, 1, d))
+    k[0, 0, 0, :17] = 2.0
+    k[0, 0, 0, 32:34] = 1.0
+    v = np.zeros((1, 2, 1, d))
+    v[0, 0, 0, 0] = 1.0
+    v[0, 1, 0, 1] = 1.0
+    return q, k, v

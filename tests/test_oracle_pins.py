@@ -189,6 +189,79 @@ def test_pv8_zero_queries_closed_form():
     assert r.counters[C_FLAGGED] == 0
 
 
+def test_golden_chunk32_rounding():
+    """The hand-derived example: one 8-bit rounding of the whole dot
+    product gives 4.5, rounding after each 32-element chunk gives 4.0."""
+    fx = golden_inputs.load("chunk32_rounding.json")
+    q, k, v = golden_inputs.chunk32_inputs()
+    for mode, case in fx["cases"].items():
+        r = oracle.lamp_forward(q, k, v, out_dtype="fp32", qk=mode)
+        m, p8 = case["m"], case["p8"]
+        l1 = 1.0 + p8
+        assert r.lse[0, 0, 0] == m, mode
+        assert abs(r.lse[0, 0, 1] - (m + math.log(l1))) < 1e-12, mode
+        assert np.allclose(r.out[0, 1, 0, :2], [1.0 / l1, p8 / l1], atol=1e-15, rtol=0), mode
+        assert r.counters[C_FLAGGED] == 0 and r.counters[C_STAGE1] == r.counters[C_STRIPS]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_chunk32_all8_equals_independent_row_loop(d):
+    """Chunked accumulation (reading R15) on the all-8-bit path against the
+    row loop that rounds its Python-integer partial sums after every 32
+    terms; the detector bits OR-ed over rows match the forward pass."""
+    q, k, v = synth.gen_outlier_sink(1, 100, 1, 1, d, seed=14)
+    q, k, v = _bf16(q), _bf16(k), _bf16(v)
+    r8 = oracle.lamp_forward(q, k, v, force="all8", out_dtype="fp32", qk="chunk32")
+    roff = oracle.lamp_forward(q, k, v, out_dtype="fp32", qk="chunk32")
+    rows = oracle.lamp8_rowloop(q, k, v, chunk=32)
+    for row, (o, lse, _) in rows.items():
+        assert np.allclose(r8.out[0, row, 0], o, atol=1e-9, rtol=0)
+        assert abs(r8.lse[0, 0, row] - lse) < 1e-9
+    for i in range(2):
+        for j in range(i + 1):
+            exp_byte = 0
+            for s in range(4):
+                st = fl = False
+                for row in range(64 * i + 16 * s, min(64 * i + 16 * s + 16, 100)):
+                    b = rows[row][2].get(j)
+                    if b:
+                        st |= b[0]
+                        fl |= b[1]
+                exp_byte |= (int(fl) << s) | (int(st) << (4 + s))
+            assert roff.mask[0, 0, i, j] == exp_byte, (i, j)
+    # and it is not the one-rounding result on these inputs
+    rx = oracle.lamp_forward(q, k, v, force="all8", out_dtype="fp32")
+    assert not np.array_equal(r8.lse, rx.lse)
+
+
+def test_chunk32_single_chunk_is_the_exact_sum():
+    """d = 32 is one chunk, and keys with a single non-zero chunk add
+    zeros after it: both give R2's results bit for bit."""
+    q, k, v = synth.gen_outlier_sink(1, 130, 2, 1, 32, seed=15)
+    a = oracle.lamp_forward(q, k, v, out_dtype="fp32", qk="chunk32")
+    b = oracle.lamp_forward(q, k, v, out_dtype="fp32")
+    assert np.array_equal(a.mask, b.mask) and np.array_equal(a.out, b.out) and np.array_equal(a.lse, b.lse)
+    q, k, v = synth.gen_outlier_sink(1, 130, 2, 1, 128, seed=16)
+    k[..., :64] = 0.0
+    k[..., 96:] = 0.0  # only chunk 2 of the keys is non-zero
+    a = oracle.lamp_forward(q, k, v, out_dtype="fp32", qk="chunk32")
+    b = oracle.lamp_forward(q, k, v, out_dtype="fp32")
+    assert np.array_equal(a.mask, b.mask) and np.array_equal(a.out, b.out) and np.array_equal(a.lse, b.lse)
+
+
+def test_chunk32_all16_is_plain_16bit_attention():
+    """With every sub-block in 16 bits the 8-bit logits only set the
+    running max, which cancels in the softmax: still 16-bit attention
+    (i.i.d. inputs: with the outlier generator at d = 64 the 8-bit logits
+    saturate at 448 in either reading and P16 with them)."""
+    q, k, v = synth.gen_iid(1, 256, 2, 1, 128, seed=17)
+    qb, kb, vb = _bf16(q), _bf16(k), _bf16(v)
+    r = oracle.lamp_forward(qb, kb, vb, force="all16", out_dtype="fp32", qk="chunk32")
+    o64, l64 = oracle.fp64_attention(qb, kb, vb)
+    assert np.abs(r.out - o64).max() <= 2e-3
+    assert np.abs(r.lse - l64).max() <= 1e-3
+
+
 def test_weights_sum_to_one():
     q, k, v = synth.gen_outlier_sink(1, 192, 2, 1, 64, seed=7)
     ones = np.ones_like(v)
