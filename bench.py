@@ -36,10 +36,10 @@ FLUSH_BYTES = 256 << 20  # > 129 MB L2
 
 # ---------------------------------------------------------------- CPU oracle leg
 def _oracle_task(args):
-    qv, kv, vv, tiles, mask, window, delta, tau, pv = args
+    qv, kv, vv, tiles, mask, window, delta, tau, pv, qk = args
     import oracle
     t0 = time.perf_counter()
-    oracle.lamp_forward(qv, kv, vv, mask=mask, window=window, delta=delta, tau=tau, tiles=tiles, pv=pv)
+    oracle.lamp_forward(qv, kv, vv, mask=mask, window=window, delta=delta, tau=tau, tiles=tiles, pv=pv, qk=qk)
     return time.perf_counter() - t0
 
 
@@ -62,14 +62,14 @@ def _head_values(w, x, b, h):
     return (t.to(torch.bfloat16) if w.dtype == "bf16" else t).double().numpy()
 
 
-def cpu_sample_tasks(w, q, k, v, delta, tau, wall_budget_s, ncores, seed=0, pv="fp16"):
+def cpu_sample_tasks(w, q, k, v, delta, tau, wall_budget_s, ncores, seed=0, pv="fp16", qk="exact"):
     """Bounded sample of the workload for the CPU oracle: random
     (batch, head, query-tile) triples until the estimated wall time on
     ``ncores`` workers reaches ``wall_budget_s``.  One task per head."""
     T = (w.seqlen + 63) // 64
     grp = w.heads_q // w.heads_kv
     probe = (_head_values(w, q, 0, 0), _head_values(w, k, 0, 0), _head_values(w, v, 0, 0),
-             [(0, 0, T - 1)], w.mask, w.window, delta, tau, pv)
+             [(0, 0, T - 1)], w.mask, w.window, delta, tau, pv, qk)
     t_long = _oracle_task(probe)  # seconds for the longest query tile
     rng = np.random.default_rng(seed)
     picks, est, n = {}, 0.0, 0
@@ -85,7 +85,7 @@ def cpu_sample_tasks(w, q, k, v, delta, tau, wall_budget_s, ncores, seed=0, pv="
     for (b, h), tiles in picks.items():
         g = h // grp
         tasks.append((_head_values(w, q, b, h), _head_values(w, k, b, g), _head_values(w, v, b, g),
-                      [(0, 0, i) for i in sorted(tiles)], w.mask, w.window, delta, tau, pv))
+                      [(0, 0, i) for i in sorted(tiles)], w.mask, w.window, delta, tau, pv, qk))
         flops += sum(_tile_flops(w, i) for i in tiles)
     return tasks, flops
 
@@ -194,30 +194,31 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def _capture(workload: str, pv: str = "fp16"):
+def _capture(workload: str, mode: str = "default"):
     """The committed ncu capture of one fused-kernel launch, if it was taken
-    on this workload and P.V mode with the current kernel source (else None)."""
+    on this workload and kernel mode with the current kernel source (else
+    None)."""
     path = os.path.join(ROOT, "profiles", "lamp_fwd_traffic.json")
     if not os.path.exists(path):
         return None
     d = json.load(open(path))
-    if d.get("workload") != workload or d.get("source_sha") != kernel_source_sha() or d.get("pv", "fp16") != pv:
+    if d.get("workload") != workload or d.get("source_sha") != kernel_source_sha() or d.get("mode", "default") != mode:
         return None
     return d
 
 
-def _traffic(workload: str, pv: str = "fp16"):
+def _traffic(workload: str, mode: str = "default"):
     """DRAM bytes per launch of the fused kernel (committed capture)."""
-    d = _capture(workload, pv)
+    d = _capture(workload, mode)
     return None if d is None else float(d["dram_bytes_read"]) + float(d["dram_bytes_write"])
 
 
-def _issue_roofline(workload: str, ms_main: float, sm_mhz, pv: str = "fp16"):
+def _issue_roofline(workload: str, ms_main: float, sm_mhz, mode: str = "default"):
     """The fused kernel is bound by instruction issue in its softmax warps:
     the floor its warp-instruction count (committed capture) allows at one
     instruction per clock on each of the 4 schedulers of every SM, at the
     SM clock sampled in the timed region, against the measured time."""
-    d = _capture(workload, pv)
+    d = _capture(workload, mode)
     if d is None or "warp_instructions" not in d or not sm_mhz:
         return None
     import torch
@@ -269,6 +270,8 @@ def main():
                     help="input generator in place of the workload's own (same shape)")
     ap.add_argument("--pv", default="fp16", choices=["fp16", "fp8"],
                     help="P.V precision of unflagged sub-blocks (fp8: the optional FP8 P.V mode)")
+    ap.add_argument("--qk", default="exact", choices=["exact", "chunk32"],
+                    help="8-bit logit accumulation (chunk32: rounded after every 32-element chunk of d)")
     ap.add_argument("--parity-tiles", type=int, default=64,
                     help="query tiles of the timed inputs checked against the oracle (0: none)")
     args = ap.parse_args()
@@ -283,7 +286,7 @@ def main():
     config = {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "heads_q": w.heads_q,
               "heads_kv": w.heads_kv, "head_dim": w.head_dim, "mask": w.mask, "window": w.window,
               "in_dtype": w.dtype, "tau": args.tau, "delta": args.delta,
-              "generator": w.gen, "seed": args.seed, "pv": args.pv}
+              "generator": w.gen, "seed": args.seed, "pv": args.pv, "qk": args.qk}
 
     if args.impl == "reference" and rank != 0:
         return  # the oracle arm runs on rank 0 only
@@ -308,7 +311,7 @@ def main():
         # (the pool's transfers roughly double the estimate)
         tasks, sflops = cpu_sample_tasks(w, q, k, v, args.delta, args.tau,
                                          args.cpu_seconds * 4 / max(1, args.steps + args.warmup), ncores,
-                                         pv=args.pv)
+                                         pv=args.pv, qk=args.qk)
         for _ in range(args.warmup):
             run_cpu_oracle(pool, tasks)
         times = [run_cpu_oracle(pool, tasks) for _ in range(args.steps)]
@@ -339,13 +342,13 @@ def main():
     out = torch.empty_like(qd)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
     mbytes, cnt = lamp.new_stats(B, Hq, N, device=dev)
-    ws = torch.empty(lamp.workspace_bytes(qd, kd, vd, out, pv=args.pv), dtype=torch.uint8, device=dev)
+    ws = torch.empty(lamp.workspace_bytes(qd, kd, vd, out, pv=args.pv, qk=args.qk), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step(evs=None, o=out, l=lse, qq=qd, kk=kd, vv=vd):
         lamp.lamp_attn_fwd(qq, kk, vv, mask=w.mask, window=w.window, delta=args.delta, tau=args.tau,
                            out=o, lse=l, mask_bytes=mbytes, counters=cnt, workspace=ws, stage_events=evs,
-                           pv=args.pv)
+                           pv=args.pv, qk=args.qk)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -399,14 +402,16 @@ def main():
     qh, kh, vh = (x.cpu().pin_memory() for x in (qd, kd, vd))
     oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    hbuf = torch.empty(lamp.host_buffer_bytes(qh, kh, vh, oh, pv=args.pv), dtype=torch.uint8, device=dev)
+    hbuf = torch.empty(lamp.host_buffer_bytes(qh, kh, vh, oh, pv=args.pv, qk=args.qk), dtype=torch.uint8,
+                       device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = []
     for i in range(max(3, K // 2) + 2):
         torch.cuda.synchronize()
         e0.record()
         lamp.lamp_attn_fwd_host(qh, kh, vh, mask=w.mask, window=w.window, delta=args.delta, tau=args.tau,
-                                out=oh, lse=lh, mask_bytes=mbytes, counters=cnt, dev_buffer=hbuf, pv=args.pv)
+                                out=oh, lse=lh, mask_bytes=mbytes, counters=cnt, dev_buffer=hbuf, pv=args.pv,
+                                qk=args.qk)
         e1.record()
         torch.cuda.synchronize()
         if i >= 2:
@@ -434,6 +439,8 @@ def main():
     e2e_step, _ = reduce_over_ranks(statistics.mean(e2e_ms), [0], world, dev)  # slowest rank
     sw_hist = sw_hist.cpu().numpy()
 
+    # the kernel mode a committed capture must match
+    kmode = "pv_fp8" if args.pv == "fp8" else ("qk_chunk32" if args.qk == "chunk32" else "default")
     bf16_peak, bf16_sus, peak_src = _peaks()
     fp8_peak = 2.0 * bf16_peak  # nominal dense FP8 : BF16 ratio of the part
     achieved = flops / (ms_main * 1e-3) / 1e12
@@ -467,11 +474,11 @@ def main():
         "config": {**config, "l2": "flushed between steps (256 MB write), per-step CUDA events"},
         "fp8_peak_frac": flops / (ms * 1e-3) / 1e12 / fp8_peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": achieved / fp8_peak, "traffic": _traffic(w.name, args.pv),
+                     "frac": achieved / fp8_peak, "traffic": _traffic(w.name, kmode),
                      "kernel": "lamp_fwd_kernel", "peak_basis": f"2 x {peak_src} bf16 burst {bf16_peak} (dense FP8:BF16 = 2)",
                      "mixed_tc_time_frac": t_tc / (ms_main * 1e-3),
                      "ceiling_fp8_frac": flops / t_tc / 1e12 / fp8_peak,
-                     "issue": _issue_roofline(w.name, ms_main, (clocks or {}).get("sm_mhz"), args.pv)},
+                     "issue": _issue_roofline(w.name, ms_main, (clocks or {}).get("sm_mhz"), kmode)},
         "ms_main_kernel": ms_main, "ms_prepass": statistics.mean(t_prep), "wall_s": t_wall,
         "ms_per_step_p10_p50_p90": pct, "ms_per_step_l2_warm": warm_ms,
         "stats": {n: int(c[i]) for i, n in enumerate(lamp.COUNTER_NAMES)},
@@ -489,7 +496,8 @@ def main():
         "clocks": clocks,
     }
     if want_cpu:
-        tasks, sflops = cpu_sample_tasks(w, q, k, v, args.delta, args.tau, args.cpu_seconds, ncores, pv=args.pv)
+        tasks, sflops = cpu_sample_tasks(w, q, k, v, args.delta, args.tau, args.cpu_seconds, ncores, pv=args.pv,
+                                         qk=args.qk)
         tcpu = run_cpu_oracle(pool, tasks)
         res["cpu_baseline"] = {"value": sflops / tcpu / 1e12, "unit": "TFLOP/s", "cores": ncores, "kind": "oracle",
                                "sample": f"{sum(len(x[3]) for x in tasks)} query tiles of {w.name}, {tcpu:.1f} s"}
@@ -498,7 +506,7 @@ def main():
         tiles = sp.sample_tiles(w.batch, w.heads_q, w.seqlen, args.parity_tiles, seed=args.seed)
         ptasks, pkeys = sp.make_tasks(q, k, v, tiles, bf16=w.dtype == "bf16", heads_q=w.heads_q,
                                       heads_kv=w.heads_kv, mask=w.mask, window=w.window, delta=args.delta,
-                                      tau=args.tau, out_dtype=w.dtype, pv=args.pv)
+                                      tau=args.tau, out_dtype=w.dtype, pv=args.pv, qk=args.qk)
         presults = pool.map(sp.oracle_task, ptasks)
         par = sp.compare(presults, pkeys, out_h, lse_h, mask_h, w.dtype, w.seqlen, w.mask, w.window)
         par["sample"] = (f"{par['tiles']} query tiles (64 rows, all their keys) of the last timed step's "

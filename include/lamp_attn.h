@@ -81,6 +81,19 @@ typedef enum {
                         128 (LAMP_ERR_UNSUPPORTED for 256) */
 } lamp_pv_mode;
 
+/* How the 8-bit key-query products accumulate into an 8-bit logit (the
+ * abstract of the same paper: "accumulated ... in 8-bit formats"). */
+typedef enum {
+  LAMP_QK_EXACT = 0,   /* exact sum of the products, one E4M3 rounding:
+                          S8 = fl8(sigma * sum_i fl8(q_i) fl8(k_i)) */
+  LAMP_QK_CHUNK32 = 1  /* the running logit rounded to E4M3 after every
+                          32-element chunk of d, in ascending order:
+                          a_c = fl8(a_{c-1} + sigma * A_c) (product and sum in
+                          double), S8 = the last a_c.  head_dim 64 or 128
+                          (LAMP_ERR_UNSUPPORTED for 256); not together with
+                          LAMP_PV_FP8 (LAMP_ERR_UNSUPPORTED) */
+} lamp_qk_accum;
+
 /* Counter slots of lamp_stats.counters (uint64 each). */
 enum {
   LAMP_CNT_TILES = 0,       /* visited 64x64 tiles (>= 1 visible entry) */
@@ -132,6 +145,7 @@ typedef struct {
                             the fused kernel (per-stage timing); NULL = none */
   int32_t pv_mode;       /* lamp_pv_mode; 0 = LAMP_PV_FP16 (zero-initialised
                             shapes keep the FP16 path) */
+  int32_t qk_accum;      /* lamp_qk_accum; 0 = LAMP_QK_EXACT */
 } lamp_shapes;
 
 typedef struct {
@@ -264,7 +278,8 @@ size_t lamp_attn_host_buffer_bytes(const lamp_shapes* shapes);
  *             ones (HIST0..2, FLAGGED, RECOMP_STEPS, SPEC_WASTE, RECOMP_LATE
  *             stay 0);
  *             stats->mask is not written.
- * shapes->pv_mode is not used (the pass computes no P.V).
+ * shapes->pv_mode is not used (the pass computes no P.V); shapes->qk_accum
+ * must be LAMP_QK_EXACT (LAMP_ERR_UNSUPPORTED otherwise).
  * Asynchronous on shapes->stream; errors as lamp_attn_fwd.
  */
 int lamp_attn_tau_sweep(const void* q, const void* k, const lamp_shapes* shapes,

@@ -14,7 +14,7 @@
 
 namespace lamp {
 cudaError_t launch_prep(const PrepParams& p, int d, cudaStream_t st);
-cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st, bool sweep, bool pv8);
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st, bool sweep, int opt);
 cudaError_t launch_v8t(const void* v, const int64_t* vs, bool in_f32, uint8_t* v8t, int B, int N, int Hkv, int D,
                        cudaStream_t st);
 cudaError_t launch_sweep_hist(const uint32_t* rec, long long n, const SweepCodes& tcode, int ntau,
@@ -110,6 +110,7 @@ bool shapes_ok(const lamp_shapes* s) {
   if (s->out_dtype != LAMP_DT_BF16 && s->out_dtype != LAMP_DT_FP32) return false;
   if (s->force < LAMP_FORCE_OFF || s->force > LAMP_FORCE_ALL8) return false;
   if (s->pv_mode != LAMP_PV_FP16 && s->pv_mode != LAMP_PV_FP8) return false;
+  if (s->qk_accum != LAMP_QK_EXACT && s->qk_accum != LAMP_QK_CHUNK32) return false;
   if (!(s->softmax_scale >= 0.0f) || std::isinf(s->softmax_scale)) return false;
   return true;
 }
@@ -155,7 +156,10 @@ void lamp_exp8_table(uint8_t out[256]) {
 size_t lamp_attn_workspace_bytes(const lamp_shapes* shapes) {
   if (!shapes_ok(shapes)) return 0;
   if (shapes->head_dim != 64 && shapes->head_dim != 128 && shapes->head_dim != 256) return 0;
-  if (shapes->pv_mode == LAMP_PV_FP8 && shapes->head_dim == 256) return 0;  // no FP8 P.V at d = 256
+  // the optional modes: d <= 128, one at a time
+  const bool opt = shapes->pv_mode == LAMP_PV_FP8 || shapes->qk_accum == LAMP_QK_CHUNK32;
+  if (opt && shapes->head_dim == 256) return 0;
+  if (shapes->pv_mode == LAMP_PV_FP8 && shapes->qk_accum == LAMP_QK_CHUNK32) return 0;
   return ws_layout(*shapes).total;
 }
 
@@ -175,9 +179,14 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   const int D = s.head_dim;
   if (D != 64 && D != 128 && D != 256) return LAMP_ERR_UNSUPPORTED;
   // FP8 P.V: the kernel's shared memory holds the extra P8 and V8 tiles only
-  // at d <= 128 (the tau sweep computes no P.V and ignores the mode)
+  // at d <= 128 (the tau sweep computes no P.V and ignores the mode);
+  // chunked logits: TMEM holds the per-chunk accumulators only at d <= 128,
+  // and the tau sweep takes one rounding of the whole dot product
   const bool pv8 = !sweep && s.pv_mode == LAMP_PV_FP8;
-  if (pv8 && D == 256) return LAMP_ERR_UNSUPPORTED;
+  const bool chunk = s.qk_accum == LAMP_QK_CHUNK32;
+  if ((pv8 || chunk) && D == 256) return LAMP_ERR_UNSUPPORTED;
+  if ((pv8 && chunk) || (sweep && chunk)) return LAMP_ERR_UNSUPPORTED;
+  const int opt = pv8 ? 1 : (chunk ? 2 : 0);  // the kernel's optional-mode bits
   if (mask_kind < LAMP_MASK_NONE || mask_kind > LAMP_MASK_SLIDING) return LAMP_ERR_INVALID_ARG;
   if (mask_kind == LAMP_MASK_SLIDING && s.window < 1) return LAMP_ERR_INVALID_ARG;
   if (!(delta >= 0.0f) || std::isnan(tau)) return LAMP_ERR_INVALID_ARG;
@@ -304,7 +313,7 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
     return fail(LAMP_ERR_CUDA);
   if (!mark(1)) return fail(LAMP_ERR_CUDA);
 
-  if (launch_fwd(fp, D, stream, sweep, pv8) != cudaSuccess) return fail(LAMP_ERR_CUDA);
+  if (launch_fwd(fp, D, stream, sweep, opt) != cudaSuccess) return fail(LAMP_ERR_CUDA);
   if (!mark(2)) return fail(LAMP_ERR_CUDA);
   if (own_ws && cudaFreeAsync(ws, stream) != cudaSuccess) return LAMP_ERR_CUDA;
   return LAMP_OK;

@@ -102,6 +102,19 @@ __device__ __forceinline__ uint32_t exp8_f16x2(uint32_t x8) {
   return e4m3x2_to_f16x2((uint16_t)exp8_code2(x8));
 }
 
+// E4M3 value, as f16 bits, of prev + A sigma (chunked logits): A = acc *
+// 2^-18 is a chunk's exact dot product, prev the running 8-bit value.  The
+// product and the sum are taken in double (the reading's definition; sig18
+// = sigma * 2^-18 exactly, so acc * sig18 is the double product A * sigma),
+// then rounded to float to odd and to E4M3 (float keeps 24 >= 4 + 2 bits:
+// the second rounding is the correctly rounded E4M3 value of the double).
+__device__ __forceinline__ uint32_t e4m3_f16_of_chunk_sum(float prev, long long acc, double sig18) {
+  const double y = (double)prev + (double)acc * sig18;
+  float f = __double2float_rz(y);
+  if ((double)f != y) f = __uint_as_float(__float_as_uint(f) | 1u);
+  return e4m3x2_to_f16x2(cvt_e4m3x2(0.0f, f)) & 0xFFFFu;
+}
+
 // Exact product of two E4M3 codes, times 2^18 (an integer below 2^36): every
 // finite code is (significand <= 15) * 2^(shift - 9) with shift in 0..14.
 __device__ __forceinline__ long long e4m3_prod_2p18(uint32_t a, uint32_t b) {
@@ -223,6 +236,21 @@ struct Mma {
       const uint64_t ad = make_sdesc(q8 + col * 128 * 128 + off, 16, sbo, layout);
       const uint64_t bd = make_sdesc(k8 + col * 64 * 128 + off, 16, sbo, layout);
       mma_f8(tmem_d, ad, bd, idesc, kk > 0);
+    }
+  }
+  // Chunked 8-bit logits: S[c][128 x 64] = Q8_c . K8_c^T for each 32-element
+  // chunk c of d (one K = 32 instruction each), into its own accumulator 64
+  // TMEM columns after the previous one, not summed
+  static __device__ __forceinline__ void qk8_chunks(uint32_t tmem_d, uint32_t q8, uint32_t k8) {
+    constexpr uint32_t idesc = make_idesc(0, 0, 0, 128, 64);
+    const uint32_t layout = (F8_ROW == 64) ? kLayoutSW64 : kLayoutSW128;
+    const uint32_t sbo = (F8_ROW == 64) ? 512u : 1024u;
+#pragma unroll
+    for (int kk = 0; kk < D / 32; ++kk) {
+      const int col = (kk * 32) / F8_ROW, off = (kk * 32) % F8_ROW;
+      const uint64_t ad = make_sdesc(q8 + col * 128 * 128 + off, 16, sbo, layout);
+      const uint64_t bd = make_sdesc(k8 + col * 64 * 128 + off, 16, sbo, layout);
+      mma_f8(tmem_d + (uint32_t)(kk * 64), ad, bd, idesc, 0u);
     }
   }
   // S16[128 x 64] = Q16[128 x D] . K16[64 x D]^T (BF16)

@@ -40,11 +40,18 @@
 
 namespace lamp {
 
-template <int D, bool PV8 = false>
+// Optional modes of the forward pass (template bits).
+constexpr int kOptPV8 = 1;    // FP8 P.V for rows of unflagged sub-blocks
+constexpr int kOptChunk = 2;  // 8-bit logits rounded after every 32-element chunk of d
+
+template <int D, int OPT = 0>
 struct Cfg {
-  // query tiles of 128 rows per CTA: one at d = 256, and at d = 128 with the
-  // FP8 P.V (whose P8 and V8 tiles leave no room for a second tile)
-  static constexpr int NT = (D == 256 || (PV8 && D == 128)) ? 1 : 2;
+  static constexpr bool PV8 = (OPT & kOptPV8) != 0;
+  static constexpr bool CHUNK = (OPT & kOptChunk) != 0;
+  // query tiles of 128 rows per CTA: one at d = 256, and at d = 128 in an
+  // optional mode (the FP8 P.V's P8 and V8 tiles leave no room in shared
+  // memory for a second tile, the chunked logits' accumulators none in TMEM)
+  static constexpr int NT = (D == 256 || (OPT != 0 && D == 128)) ? 1 : 2;
   static constexpr int NS = (D == 256) ? 1 : 2;  // K/V stages
   static constexpr int SM_THREADS = 256;                // softmax threads per tile (2 per row)
   static constexpr int THREADS = 32 * (8 * NT + 1 + NT);
@@ -58,7 +65,8 @@ struct Cfg {
   static constexpr int V_BYTES = (D / 64) * kBN * 128;
   // FP8 P.V: V8t [D rows x 64 keys] E4M3 after V16 in the stage, and the P8
   // tile [128 rows x 64 keys] after the P16 tile (both 64-byte swizzled)
-  static_assert(!(PV8 && D == 256), "no FP8 P.V at d = 256");
+  static_assert(!(OPT != 0 && D == 256), "no optional mode at d = 256");
+  static_assert(!(PV8 && CHUNK), "one optional mode at a time");
   static constexpr int V8_BYTES = PV8 ? kBN * D : 0;
   static constexpr int OFF_V8 = K8_BYTES + K16_BYTES + V_BYTES;  // inside a stage
   static constexpr int STAGE_BYTES = K8_BYTES + K16_BYTES + V_BYTES + V8_BYTES;
@@ -74,16 +82,18 @@ struct Cfg {
   static constexpr int CH = D / 32;  // 32-element chunks of d (one FP8 MMA instruction each)
   static constexpr int MISC_BYTES = 9216 + 2 * NT * kBM * CH * 4;
   static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
-  // TMEM columns per tile (fp32): O (d values), the 64-column S8 buffer and
-  // the 64-column S16 buffer.  QK16 of a step is computed ahead, while the
-  // softmax still works on S8, so the recompute never waits for it.
+  // TMEM columns per tile (fp32): O (d values), the 64-column S8 buffer
+  // (one per 32-element chunk of d with chunked logits) and the 64-column
+  // S16 buffer.  QK16 of a step is computed ahead, while the softmax still
+  // works on S8, so the recompute never waits for it.
   static constexpr int O_COLS = D;
+  static constexpr int S8_BUFS = CHUNK ? D / 32 : 1;
   static constexpr int S8_OFF = D;
-  static constexpr int S16_OFF = D + kBN;
+  static constexpr int S16_OFF = D + S8_BUFS * kBN;
   // one K/V stage (d = 256, one tile): two S16 buffers, so QK16 of a step
   // can be issued while the softmax may still read the previous step's S16
   static constexpr int S16_BUFS = (NS == 1) ? 2 : 1;
-  static constexpr int TILE_COLS = D + (1 + S16_BUFS) * kBN;
+  static constexpr int TILE_COLS = D + (S8_BUFS + S16_BUFS) * kBN;
   static constexpr int TMEM_COLS = 512;
   static_assert(NT * TILE_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -230,6 +240,19 @@ __device__ __forceinline__ long long exact_dot(const uint8_t* sQ8, const uint8_t
   return (long long)hi * 16777216ll + (long long)lo;
 }
 
+// The same for chunk ch of d only (32 elements: lane L takes element
+// 32 ch + L; 32 products below 2^36 each, split at bit 24 as above).
+template <int D>
+__device__ __forceinline__ long long exact_dot_chunk(const uint8_t* sQ8, const uint8_t* sK8, int r, int c, int ch,
+                                                     int lane) {
+  constexpr int RB = (Cfg<D>::F8_SWZ_ROW == 64) ? 64 : D;
+  const int x = ch * 32 + lane;
+  const long long acc = e4m3_prod_2p18(sQ8[swz_offset(r, x, kBM, RB)], sK8[swz_offset(c, x, kBN, RB)]);
+  const int hi = __reduce_add_sync(0xffffffffu, (int)(acc >> 24));
+  const unsigned lo = __reduce_add_sync(0xffffffffu, (unsigned)(acc & 0xFFFFFF));
+  return (long long)hi * 16777216ll + (long long)lo;
+}
+
 }  // namespace lamp
 
 namespace lamp {
@@ -280,12 +303,14 @@ __device__ __noinline__ float q8_from_q16(uint8_t* q8w, int t, int hf, uint32_t 
   return ss;
 }
 
-template <int D, int kMode, bool kPV8>
-__global__ void __launch_bounds__(Cfg<D, kPV8>::THREADS, 1) lamp_fwd_kernel(const __grid_constant__ FwdParams p) {
+template <int D, int kMode, int kOpt>
+__global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(const __grid_constant__ FwdParams p) {
   constexpr bool kSweep = kMode == 2;
   constexpr bool kNoStage1 = kMode == 1;
-  static_assert(!(kSweep && kPV8), "the sweep pass computes no P.V");
-  using C = Cfg<D, kPV8>;
+  constexpr bool kPV8 = (kOpt & kOptPV8) != 0;
+  constexpr bool kChunk = (kOpt & kOptChunk) != 0;
+  static_assert(!(kSweep && kOpt != 0), "the sweep pass has no optional mode");
+  using C = Cfg<D, kOpt>;
   extern __shared__ uint8_t smem_raw[];
   // align by pointer arithmetic on the __shared__ array so that every access
   // through `smem` stays a shared-memory access
@@ -612,7 +637,10 @@ __global__ void __launch_bounds__(Cfg<D, kPV8>::THREADS, 1) lamp_fwd_kernel(cons
         if (ok) ok = wait_bar(cx, bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1);
         if (!ok) break;
         tc_fence_after();
-        Mma<D>::qk8(tm + C::S8_OFF, qbase, kv(j));
+        if constexpr (kChunk)
+          Mma<D>::qk8_chunks(tm + C::S8_OFF, qbase, kv(j));
+        else
+          Mma<D>::qk8(tm + C::S8_OFF, qbase, kv(j));
         mma_commit(bar(M_S_FULL + 8 * t));
         if (i > 0) {
           // the decision of step i - 1, read once QK8(i) is on its way
@@ -717,7 +745,10 @@ __global__ void __launch_bounds__(Cfg<D, kPV8>::THREADS, 1) lamp_fwd_kernel(cons
     // y = A_tc sigma, y -+ G and of this sum); qg holds
     // 40 * 2^-25 (C - c) sigma (||q8_c|| + 2^-6), the pre-pass the key side.
 #pragma unroll
-    for (int c = 0; c < C::CH; ++c) qg[c] = (qg[c] + 0x1p-6f) * (40.0f * 0x1p-25f * (float)(C::CH - c)) * p.sigma_f;
+    // (chunked logits: each chunk is one instruction with a zero
+    // accumulator, its own bound without the chain factor C - c)
+    for (int c = 0; c < C::CH; ++c)
+      qg[c] = (qg[c] + 0x1p-6f) * (40.0f * 0x1p-25f * (kChunk ? 1.0f : (float)(C::CH - c))) * p.sigma_f;
     const float satq = p.sigma_f * nq * (1.0f + p.guard);
     uint32_t c_h0 = 0, c_h1 = 0, c_h2 = 0, c_strips = 0, c_st1 = 0, c_fl = 0, c_sat = 0, c_fix = 0,
              c_res = 0, c_fmax = 0;  // per-thread counts (a CTA sees at most 2^21 logits per thread slot)
@@ -761,7 +792,7 @@ __global__ void __launch_bounds__(Cfg<D, kPV8>::THREADS, 1) lamp_fwd_kernel(cons
       // bound on |A_tc sigma - A sigma| for this row and tile (see qg)
       float G = 0.0f;
 #pragma unroll
-      for (int c = 0; c < C::CH; c += (C::CH >= 4 ? 4 : 2)) {
+      for (int c = 0; c < (kChunk ? 0 : C::CH); c += (C::CH >= 4 ? 4 : 2)) {
         if constexpr (C::CH >= 4) {
           const float4 kb = *reinterpret_cast<const float4*>(nkcrow + (size_t)jt * C::CH + c);
           const float4 qw = *reinterpret_cast<const float4*>(qg + c);
@@ -772,11 +803,97 @@ __global__ void __launch_bounds__(Cfg<D, kPV8>::THREADS, 1) lamp_fwd_kernel(cons
           G = fmaf(qw.x, kb.x, fmaf(qw.y, kb.y, G));
         }
       }
-      const bool satp = satq * nk >= 400.0f;  // can a logit of this tile reach the 8-bit limit?
+      // can a logit of this tile reach the 8-bit limit?  (chunked: each of
+      // the C roundings may add 1/16, (1 + 1/16)^4 < 1.3)
+      const bool satp = satq * nk * (kChunk ? 1.3f : 1.0f) >= 400.0f;
 
       // ---- S = Q8 K8^T (fp32, TMEM) -> 8-bit logits
-      uint32_t a32[NC];
+      uint32_t s8h[NC / 2];  // S8 pairs as f16x2 (exact values; cl until resolved)
+      uint32_t gmx[NC / 8];  // per group of 8: max of the pairs (f16x2)
+      uint32_t unc = 0u;     // visible logits whose candidates differ and that may matter
+      uint32_t hmx = 0xFC00FC00u;  // f16x2 max of their high candidates ch (-inf: none)
+      const float2 gp = make_float2(G, G);
       if (!fail) fail = !wait_bar_warp(cx, bar(M_S_FULL + 8 * tt), jj & 1);
+      if constexpr (kChunk) {
+        // Chunked logits: a_c = fl8(a_{c-1} + A_c sigma), chunk by chunk.
+        // The tensor core's A_c (one K = 32 instruction, zero accumulator)
+        // errs by less than 37 * 2^-25 x_c (x_c bounds |A_c| and each
+        // product); with sigma's float rounding and the roundings of y and
+        // y -+ g, g = qg[c] nkc + 2^-22 |y| bounds |y - (a_{c-1} + A_c sigma)|.
+        // Where fl8(y - g) and fl8(y + g) differ, the logit's chunk is
+        // re-derived exactly (integer dot product) before the next chunk.
+        const uint8_t* sK8c = smem + C::OFF_ST + ((jt - J0) % C::NS) * C::STAGE_BYTES;
+#pragma unroll
+        for (int i = 0; i < NC / 2; ++i) s8h[i] = 0u;
+#pragma unroll 1
+        for (int c = 0; c < C::CH; ++c) {
+          uint32_t a32[NC];
+          if (!fail) {
+            tc_fence_after();
+            tmem_ld32(lane_base + C::S8_OFF + c * kBN + col0, a32);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < NC; ++e) a32[e] = 0u;
+          }
+          const float gc = qg[c] * nkcrow[(size_t)jt * C::CH + c];
+          uint32_t ucm = 0u;  // logits whose rounding of this chunk is uncertain
+#pragma unroll
+          for (int i = 0; i < NC / 2; ++i) {
+            const __half2 ph = as_half2(s8h[i]);
+            const float2 av = make_float2(__uint_as_float(a32[2 * i]), __uint_as_float(a32[2 * i + 1]));
+            const float2 y = __ffma2_rn(av, sig2, make_float2(__low2float(ph), __high2float(ph)));
+            const float g0 = fmaf(fabsf(y.x), 0x1p-22f, gc), g1 = fmaf(fabsf(y.y), 0x1p-22f, gc);
+            const uint16_t cl = cvt_e4m3x2(y.y - g1, y.x - g0), ch = cvt_e4m3x2(y.y + g1, y.x + g0);
+            const uint32_t dd = (uint32_t)(cl ^ ch);
+            const uint32_t um = ((dd & 0xFFu) ? 0x0000FFFFu : 0u) | ((dd >> 8) ? 0xFFFF0000u : 0u);
+            s8h[i] = (e4m3x2_to_f16x2(cl) & ~um) | (s8h[i] & um);  // uncertain: keep a_{c-1}
+            ucm |= ((uint32_t)((dd & 0xFFu) != 0u) << (2 * i)) | ((uint32_t)((dd >> 8) != 0u) << (2 * i + 1));
+          }
+          if (!all_full) ucm &= vm;  // hidden keys take -inf below
+          if (fail) ucm = 0u;
+          for (;;) {  // one uncertain logit at a time over the warp
+            const unsigned who = __ballot_sync(0xffffffffu, ucm != 0u);
+            if (!who) break;
+            const int src = __ffs(who) - 1;
+            const int cb = __shfl_sync(0xffffffffu, ucm ? (__ffs(ucm) - 1) : 0, src);
+            const long long acc = exact_dot_chunk<D>(sQ8, sK8c, rw * 32 + src, col0 + cb, c, lane);
+            if (lane == src) {
+              static_assert(NC == 32, "the switches below list 16 pairs");
+              uint32_t w = 0u;
+              switch (cb >> 1) {
+#define LAMP_GET_CASE(i) case i: w = s8h[i]; break;
+                LAMP_GET_CASE(0) LAMP_GET_CASE(1) LAMP_GET_CASE(2) LAMP_GET_CASE(3)
+                LAMP_GET_CASE(4) LAMP_GET_CASE(5) LAMP_GET_CASE(6) LAMP_GET_CASE(7)
+                LAMP_GET_CASE(8) LAMP_GET_CASE(9) LAMP_GET_CASE(10) LAMP_GET_CASE(11)
+                LAMP_GET_CASE(12) LAMP_GET_CASE(13) LAMP_GET_CASE(14) LAMP_GET_CASE(15)
+#undef LAMP_GET_CASE
+                default: break;
+              }
+              const __half2 wh = as_half2(w);
+              const uint32_t hv = e4m3_f16_of_chunk_sum((cb & 1) ? __high2float(wh) : __low2float(wh), acc, p.sig18);
+              const uint32_t keep = (cb & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+              const uint32_t put = (hv * 0x00010001u) & ~keep;
+              switch (cb >> 1) {
+#define LAMP_PUT_CASE(i) case i: s8h[i] = (s8h[i] & keep) | put; break;
+                LAMP_PUT_CASE(0) LAMP_PUT_CASE(1) LAMP_PUT_CASE(2) LAMP_PUT_CASE(3)
+                LAMP_PUT_CASE(4) LAMP_PUT_CASE(5) LAMP_PUT_CASE(6) LAMP_PUT_CASE(7)
+                LAMP_PUT_CASE(8) LAMP_PUT_CASE(9) LAMP_PUT_CASE(10) LAMP_PUT_CASE(11)
+                LAMP_PUT_CASE(12) LAMP_PUT_CASE(13) LAMP_PUT_CASE(14) LAMP_PUT_CASE(15)
+#undef LAMP_PUT_CASE
+                default: break;
+              }
+              ucm &= ucm - 1u;
+            }
+            if (lane == 0) ++c_fix;
+          }
+        }
+#pragma unroll
+        for (int g4 = 0; g4 < NC / 8; ++g4)
+          gmx[g4] = as_u32(__hmax2(__hmax2(as_half2(s8h[4 * g4]), as_half2(s8h[4 * g4 + 1])),
+                                   __hmax2(as_half2(s8h[4 * g4 + 2]), as_half2(s8h[4 * g4 + 3]))));
+      } else {
+      uint32_t a32[NC];
       if (!fail) {
         tc_fence_after();
         tmem_ld32(lane_base + C::S8_OFF + col0, a32);
@@ -800,11 +917,6 @@ __global__ void __launch_bounds__(Cfg<D, kPV8>::THREADS, 1) lamp_fwd_kernel(cons
       // adds at most |.|/16 + 2^-10, so the exact values are at most
       // cl + 0.13 |cl| + 2.2 G + 2^-8: below m - 6.75 nothing in it counts.
       // Those uncertain logits are resolved once the tile maximum is known.
-      uint32_t s8h[NC / 2];  // S8 pairs as f16x2 (exact values; cl until resolved)
-      uint32_t gmx[NC / 8];  // per group of 8: max of the pairs (f16x2)
-      uint32_t unc = 0u;     // visible logits whose candidates differ and that may matter
-      uint32_t hmx = 0xFC00FC00u;  // f16x2 max of their high candidates ch (-inf: none)
-      const float2 gp = make_float2(G, G);
       {
         // delta = 0 (first stage off): stage 1 holds for every visible entry,
         // so besides the logits near m only those whose candidates lie on
@@ -860,6 +972,7 @@ __global__ void __launch_bounds__(Cfg<D, kPV8>::THREADS, 1) lamp_fwd_kernel(cons
           }
         }
       }
+      }  // one rounding of the whole dot product
       if (fail) unc = 0u;
       // hidden keys take -inf: they are never the max and x8 saturates to -448 (P8 = 0)
       if (!all_full) {
@@ -1323,35 +1436,40 @@ __global__ void __launch_bounds__(Cfg<D, kPV8>::THREADS, 1) lamp_fwd_kernel(cons
 }
 
 // ---------------------------------------------------------------- launcher
-template <int D, int kMode, bool kPV8>
+template <int D, int kMode, int kOpt>
 static cudaError_t launch_fwd_d(FwdParams p, cudaStream_t st) {
-  using C = Cfg<D, kPV8>;
+  using C = Cfg<D, kOpt>;
   cudaError_t e =
-      cudaFuncSetAttribute(lamp_fwd_kernel<D, kMode, kPV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      cudaFuncSetAttribute(lamp_fwd_kernel<D, kMode, kOpt>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   p.nqb = (p.N + kBM * C::NT - 1) / (kBM * C::NT);
   const unsigned grid = (unsigned)p.nqb * (unsigned)p.B * (unsigned)p.Hq;
   if (grid == 0) return cudaSuccess;
-  lamp_fwd_kernel<D, kMode, kPV8><<<grid, C::THREADS, C::SMEM, st>>>(p);
+  lamp_fwd_kernel<D, kMode, kOpt><<<grid, C::THREADS, C::SMEM, st>>>(p);
   return cudaGetLastError();
 }
 
-template <int D>
-static cudaError_t launch_fwd_mode(const FwdParams& p, cudaStream_t st, bool sweep, bool pv8) {
-  if (sweep) return launch_fwd_d<D, 2, false>(p, st);
-  if constexpr (D != 256) {
-    if (pv8) return p.delta_code == 0u ? launch_fwd_d<D, 1, true>(p, st) : launch_fwd_d<D, 0, true>(p, st);
-  } else {
-    if (pv8) return cudaErrorInvalidValue;
-  }
-  return p.delta_code == 0u ? launch_fwd_d<D, 1, false>(p, st) : launch_fwd_d<D, 0, false>(p, st);
+template <int D, int kOpt>
+static cudaError_t launch_fwd_opt(const FwdParams& p, cudaStream_t st) {
+  return p.delta_code == 0u ? launch_fwd_d<D, 1, kOpt>(p, st) : launch_fwd_d<D, 0, kOpt>(p, st);
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st, bool sweep, bool pv8) {
+template <int D>
+static cudaError_t launch_fwd_mode(const FwdParams& p, cudaStream_t st, bool sweep, int opt) {
+  if (sweep) return opt == 0 ? launch_fwd_d<D, 2, 0>(p, st) : cudaErrorInvalidValue;
+  if constexpr (D != 256) {
+    if (opt == kOptPV8) return launch_fwd_opt<D, kOptPV8>(p, st);
+    if (opt == kOptChunk) return launch_fwd_opt<D, kOptChunk>(p, st);
+  }
+  return opt == 0 ? launch_fwd_opt<D, 0>(p, st) : cudaErrorInvalidValue;
+}
+
+// opt: 0, or one of the optional modes (FP8 P.V, chunked logits; d <= 128)
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st, bool sweep, int opt) {
   switch (d) {
-    case 64: return launch_fwd_mode<64>(p, st, sweep, pv8);
-    case 128: return launch_fwd_mode<128>(p, st, sweep, pv8);
-    case 256: return launch_fwd_mode<256>(p, st, sweep, pv8);
+    case 64: return launch_fwd_mode<64>(p, st, sweep, opt);
+    case 128: return launch_fwd_mode<128>(p, st, sweep, opt);
+    case 256: return launch_fwd_mode<256>(p, st, sweep, opt);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -20,6 +20,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 MASK = {"none": 0, "causal": 1, "sliding": 2}
 FORCE = {"off": 0, "all16": 1, "all8": 2}
 PV = {"fp16": 0, "fp8": 1}
+QK = {"exact": 0, "chunk32": 1}
 DT = {torch.bfloat16: 0, torch.float32: 1}
 NUM_COUNTERS = 16
 COUNTER_NAMES = ["tiles", "hist0", "hist1", "hist2p", "strips", "stage1", "flagged",
@@ -40,7 +41,7 @@ class LampShapes(ctypes.Structure):
         ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32), ("force", ctypes.c_int32),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("stream", ctypes.c_void_p), ("stage_events", ctypes.c_void_p * 3),
-        ("pv_mode", ctypes.c_int32),
+        ("pv_mode", ctypes.c_int32), ("qk_accum", ctypes.c_int32),
     ]
 
 
@@ -104,7 +105,7 @@ def _check(code: int):
 
 
 def make_shapes(q, k, v, out, *, window=0, scale=0.0, force="off", workspace=None, stream=None,
-                stage_events=None, pv="fp16"):
+                stage_events=None, pv="fp16", qk="exact"):
     B, N, Hq, d = q.shape
     sh = LampShapes()
     sh.batch, sh.seqlen, sh.heads_q, sh.heads_kv, sh.head_dim = B, N, Hq, k.shape[2], d
@@ -119,6 +120,7 @@ def make_shapes(q, k, v, out, *, window=0, scale=0.0, force="off", workspace=Non
     sh.out_dtype = DT[out.dtype]
     sh.force = FORCE[force]
     sh.pv_mode = PV[pv]
+    sh.qk_accum = QK[qk]
     if workspace is not None:
         sh.workspace = workspace.data_ptr()
         sh.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -137,13 +139,14 @@ def workspace_bytes(q, k, v, out=None, **kw) -> int:
 
 def lamp_attn_fwd(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -8, tau=2.0 ** -1,
                   force="off", out=None, out_dtype=None, lse=None, want_lse=True, mask_bytes=None,
-                  counters=None, workspace=None, stream=None, stage_events=None, pv="fp16"):
+                  counters=None, workspace=None, stream=None, stage_events=None, pv="fp16", qk="exact"):
     """Forward pass.  q [B, N, Hq, d], k/v [B, N, Hkv, d] CUDA tensors (bf16
     or fp32, d contiguous).  Returns (out, lse, mask_bytes, counters); the
     last three may be None when not requested.  Asynchronous on ``stream``
     (default: torch's current stream).  ``stage_events``: three
     torch.cuda.Event recorded around the pre-pass and the fused kernel.
-    ``pv``: "fp16" or "fp8", the P.V precision of unflagged sub-blocks."""
+    ``pv``: "fp16" or "fp8", the P.V precision of unflagged sub-blocks.
+    ``qk``: "exact" or "chunk32", how the 8-bit logits accumulate."""
     lib = load()
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
         raise LampError("q, k, v must be CUDA tensors")
@@ -155,7 +158,7 @@ def lamp_attn_fwd(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, N), device=q.device, dtype=torch.float32)
     sh = make_shapes(q, k, v, out, window=window, scale=scale, force=force, workspace=workspace,
-                     stream=stream, stage_events=stage_events, pv=pv)
+                     stream=stream, stage_events=stage_events, pv=pv, qk=qk)
     stats = LampStats()
     stats.mask = mask_bytes.data_ptr() if mask_bytes is not None else None
     stats.counters = counters.data_ptr() if counters is not None else None
@@ -172,7 +175,8 @@ def host_buffer_bytes(q, k, v, out=None, **kw) -> int:
     return int(load().lamp_attn_host_buffer_bytes(ctypes.byref(_host_shapes(q, k, v, out, **kw))))
 
 
-def _host_shapes(q, k, v, out, *, window=0, scale=0.0, force="off", stream=None, device=None, pv="fp16"):
+def _host_shapes(q, k, v, out, *, window=0, scale=0.0, force="off", stream=None, device=None, pv="fp16",
+                 qk="exact"):
     dev = torch.device("cuda") if device is None else torch.device(device)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     B, N, Hq, d = q.shape
@@ -189,13 +193,14 @@ def _host_shapes(q, k, v, out, *, window=0, scale=0.0, force="off", stream=None,
     sh.out_dtype = DT[out.dtype]
     sh.force = FORCE[force]
     sh.pv_mode = PV[pv]
+    sh.qk_accum = QK[qk]
     sh.stream = s.cuda_stream
     return sh
 
 
 def lamp_attn_fwd_host(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -8, tau=2.0 ** -1,
                        force="off", out=None, out_dtype=None, lse=None, want_lse=True, mask_bytes=None,
-                       counters=None, dev_buffer=None, stream=None, device=None, pv="fp16"):
+                       counters=None, dev_buffer=None, stream=None, device=None, pv="fp16", qk="exact"):
     """Forward pass on HOST tensors (CPU, page-locked for full speed): the
     copies to and from the GPU are pipelined against the computation inside
     the library.  Returns (out, lse, mask_bytes, counters) with out / lse on
@@ -211,7 +216,8 @@ def lamp_attn_fwd_host(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0
         out = torch.empty((B, N, Hq, d), dtype=out_dtype or q.dtype).pin_memory()
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, N), dtype=torch.float32).pin_memory()
-    sh = _host_shapes(q, k, v, out, window=window, scale=scale, force=force, stream=stream, device=device, pv=pv)
+    sh = _host_shapes(q, k, v, out, window=window, scale=scale, force=force, stream=stream, device=device, pv=pv,
+                      qk=qk)
     stats = LampStats()
     stats.mask = mask_bytes.data_ptr() if mask_bytes is not None else None
     stats.counters = counters.data_ptr() if counters is not None else None

@@ -21,12 +21,12 @@ def values(t):
 
 
 def run_gpu(qd, kd, vd, *, mask="causal", window=0, delta=2.0 ** -8, tau=0.5, force="off",
-            out_dtype=None, scale=0.0, pv="fp16"):
+            out_dtype=None, scale=0.0, pv="fp16", qk="exact"):
     B, N, Hq, d = qd.shape
     mbytes, cnt = lamp.new_stats(B, Hq, N)
     out, lse, _, _ = lamp.lamp_attn_fwd(qd, kd, vd, mask=mask, window=window, delta=delta, tau=tau,
                                         force=force, out_dtype=out_dtype, mask_bytes=mbytes,
-                                        counters=cnt, scale=scale, pv=pv)
+                                        counters=cnt, scale=scale, pv=pv, qk=qk)
     torch.cuda.synchronize()
     return (out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
             mbytes.cpu().numpy(), cnt.cpu().numpy())
@@ -54,6 +54,7 @@ def assert_close(gpu_out, gpu_lse, ref, out_dtype, rows=None):
         gpu_out = gpu_out[rows["o"]]
         gpu_lse = gpu_lse[rows["l"]]
     err, bound = out_errors(gpu_out, o_ref, out_dtype)
+    bound = np.broadcast_to(bound, err.shape)
     worst = np.unravel_index(np.argmax(err - bound), err.shape)
     assert np.all(err <= bound), f"out error {err[worst]} > {bound[worst]} at {worst}"
     fin = np.isfinite(l_ref)

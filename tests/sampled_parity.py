@@ -57,17 +57,17 @@ def sample_tiles(batch, heads_q, seqlen, n, seed=0):
 
 def oracle_task(args):
     """One head's sampled query tiles through the oracle and FP64 attention.
-    args = (q, k, v, tiles, mask, window, delta, tau, force, out_dtype, pv):
+    args = (q, k, v, tiles, mask, window, delta, tau, force, out_dtype, pv, qk):
     q, k, v float64 [1, N, 1, d] values of one (b, h) and its kv head;
     tiles: query-tile indices.  Returns (tiles, mask rows [n, T], out
     [n, 64, d] (before output rounding), lse [n, 64], fp64 out, fp64 lse,
     seconds in the oracle)."""
     import oracle
-    q, k, v, tiles, mask, window, delta, tau, force, out_dtype, pv = args
+    q, k, v, tiles, mask, window, delta, tau, force, out_dtype, pv, qk = args
     n = q.shape[1]
     t0 = time.perf_counter()
     r = oracle.lamp_forward(q, k, v, mask=mask, window=window, delta=delta, tau=tau, force=force,
-                            out_dtype=out_dtype, tiles=[(0, 0, i) for i in tiles], pv=pv)
+                            out_dtype=out_dtype, tiles=[(0, 0, i) for i in tiles], pv=pv, qk=qk)
     secs = time.perf_counter() - t0
     d = q.shape[3]
     mrows, outs, lses, o64s, l64s = [], [], [], [], []
@@ -91,7 +91,7 @@ def oracle_task(args):
 
 
 def make_tasks(q, k, v, tiles, *, bf16, heads_q, heads_kv, mask, window, delta, tau, force="off",
-               out_dtype="bf16", pv="fp16"):
+               out_dtype="bf16", pv="fp16", qk="exact"):
     """Group the sampled tiles by head into oracle_task arguments."""
     grp = heads_q // heads_kv
     by_head = {}
@@ -101,7 +101,7 @@ def make_tasks(q, k, v, tiles, *, bf16, heads_q, heads_kv, mask, window, delta, 
     for (b, h), il in sorted(by_head.items()):
         g = h // grp
         tasks.append((head_values(q, b, h, bf16), head_values(k, b, g, bf16), head_values(v, b, g, bf16),
-                      sorted(il), mask, window, delta, tau, force, out_dtype, pv))
+                      sorted(il), mask, window, delta, tau, force, out_dtype, pv, qk))
         keys.append((b, h))
     return tasks, keys
 

@@ -72,16 +72,31 @@ def test_workspace_bytes(lib):
     sh.pv_mode = 2
     sh.head_dim = 128
     assert lib.lamp_attn_workspace_bytes(ctypes.byref(sh)) == 0
+    # chunked 8-bit logits: no extra workspace; not at d = 256, not with FP8 P.V
+    sh = _shapes()
+    sh.qk_accum = 1
+    assert lib.lamp_attn_workspace_bytes(ctypes.byref(sh)) == n
+    sh.pv_mode = 1
+    assert lib.lamp_attn_workspace_bytes(ctypes.byref(sh)) == 0
+    sh = _shapes(d=256)
+    sh.qk_accum = 1
+    assert lib.lamp_attn_workspace_bytes(ctypes.byref(sh)) == 0
+    sh.qk_accum = 2
+    sh.head_dim = 128
+    assert lib.lamp_attn_workspace_bytes(ctypes.byref(sh)) == 0
 
 
 def test_shapes_struct_matches_the_header():
-    """The ctypes mirror ends with the same field as the C struct, at the
-    offset the C layout gives it (pv_mode after the three event handles)."""
-    assert lamp.LampShapes._fields_[-1][0] == "pv_mode"
+    """The ctypes mirror ends with the same fields as the C struct, at the
+    offsets the C layout gives them (pv_mode and qk_accum after the three
+    event handles)."""
+    assert [f[0] for f in lamp.LampShapes._fields_[-2:]] == ["pv_mode", "qk_accum"]
     assert lamp.LampShapes.pv_mode.offset == lamp.LampShapes.stage_events.offset + 3 * ctypes.sizeof(ctypes.c_void_p)
+    assert lamp.LampShapes.qk_accum.offset == lamp.LampShapes.pv_mode.offset + 4
     src = open(os.path.join(ROOT, "include", "lamp_attn.h")).read()
     body = src[src.index("typedef struct {\n  int32_t batch"):src.index("} lamp_shapes;")]
-    assert body.rstrip().splitlines()[-2].strip().startswith("int32_t pv_mode;")
+    fields = [ln.strip() for ln in body.splitlines() if ln.strip().startswith(("int32_t", "void*", "size_t"))]
+    assert fields[-2].startswith("int32_t pv_mode;") and fields[-1].startswith("int32_t qk_accum;")
 
 
 def _call(lib, sh, ptrs=(16, 32, 48, 64), mask=1, delta=2 ** -8, tau=0.5):
@@ -111,6 +126,12 @@ def test_argument_errors_before_launch(lib):
     sh = _shapes()
     sh.pv_mode = 3
     assert _call(lib, sh) == lamp.LAMP_ERR_INVALID_ARG
+    sh = _shapes(d=256)
+    sh.qk_accum = 1  # no chunked logits at d = 256
+    assert _call(lib, sh) == lamp.LAMP_ERR_UNSUPPORTED
+    sh = _shapes()
+    sh.qk_accum, sh.pv_mode = 1, 1  # one optional mode at a time
+    assert _call(lib, sh) == lamp.LAMP_ERR_UNSUPPORTED
 
 
 def test_no_device_is_an_error_not_a_fallback(lib):
