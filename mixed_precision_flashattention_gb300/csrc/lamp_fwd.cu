@@ -5,19 +5,20 @@
 // in ascending key order (the running maximum of the method is defined
 // over that order).  The tiles share the K/V stages and ping-pong: while
 // the softmax warps of one tile work, the tensor core serves the other.
-// Warp roles:
-//   warps 8t..8t+7  softmax of tile t: two threads per query row (warps
-//              8t+w and 8t+4+w hold TMEM lanes 32w.. for key columns 0-31
-//              and 32-63 of each step).  Per step: 8-bit logits S8 (with an
+// Warp roles (TPR softmax threads per query row: 2, and 4 at d = 256, so
+// that its one tile per CTA still has 16 softmax warps):
+//   warps 4 TPR t .. 4 TPR t + 4 TPR - 1  softmax of tile t: warps
+//              4 TPR t + 4 j + w (j < TPR) hold TMEM lanes 32w.. for key
+//              columns 64 j / TPR .. of each step.  Per step: 8-bit logits S8 (with an
 //              exactness guard: two candidate roundings per logit, settled
 //              by a cheap check or an exact integer re-derivation), running
 //              max, the two-stage detector, sub-block flags, mask byte +
 //              histogram, FP16 P (P8 = fl8(e^x8) computed with an fp32 ex2
 //              and one E4M3 rounding, or P16 for the rows of flagged
 //              sub-blocks), O rescale in TMEM, the row sum l in registers.
-//   warp 8*NT  TMA producer: Q (Q16, and Q8 for fp32 q) of every tile once,
+//   warp 4 TPR NT  TMA producer: Q (Q16, and Q8 for fp32 q) of every tile once,
 //              then K8/K16/V16 per step into a ring of stages.
-//   warp 8*NT+1+t  MMA issuer of tile t (the first one also owns TMEM):
+//   warp 4 TPR NT + 1 + t  MMA issuer of tile t (the first one also owns TMEM):
 //              S = Q8 K8^T (kind::f8f6f4) into the S8 buffer; S16 = Q16 K16^T
 //              (kind::f16, BF16) into its own S16 buffer, only for steps with
 //              a flagged sub-block -- issued ahead of the decision for the
@@ -53,9 +54,15 @@ struct Cfg {
   // memory for a second tile, the chunked logits' accumulators none in TMEM)
   static constexpr int NT = (D == 256 || (OPT != 0 && D == 128)) ? 1 : 2;
   static constexpr int NS = (D == 256) ? 1 : 2;  // K/V stages
-  static constexpr int SM_THREADS = 256;                // softmax threads per tile (2 per row)
-  static constexpr int THREADS = 32 * (8 * NT + 1 + NT);
-  static constexpr int PRODUCER_WARP = 8 * NT, MMA_WARP = 8 * NT + 1;  // + t: MMA warp of tile t
+  // softmax threads per query row: two, each with 32 of a step's 64 keys;
+  // four at d = 256 (16 keys each), so that its one query tile per CTA still
+  // has 16 softmax warps to hide latency with
+  static constexpr int TPR = (D == 256) ? 4 : 2;
+  static constexpr int NC = kBN / TPR;                  // logits per softmax thread per step
+  static constexpr int SM_THREADS = kBM * TPR;          // softmax threads per tile
+  static constexpr int SM_WARPS = NT * SM_THREADS / 32;
+  static constexpr int THREADS = 32 * (SM_WARPS + 1 + NT);
+  static constexpr int PRODUCER_WARP = SM_WARPS, MMA_WARP = SM_WARPS + 1;  // + t: MMA warp of tile t
   static constexpr int F8_SWZ_ROW = (D == 64) ? 64 : 128;  // swizzle row width of 8-bit tiles
   static constexpr int Q8_BYTES = kBM * D;
   static constexpr int Q16_BYTES = kBM * D * 2;
@@ -264,19 +271,21 @@ namespace lamp {
 // the largest half-ulp8 of its stage-1 entries (the flag at any tau follows
 // from it); no 16-bit recompute, no P.V, no output.
 
-// bf16 q: a softmax thread rounds its half (hf) of row t of the Q16 tile to
-// E4M3 (the rounding the pre-pass applies to fp32 values; bf16 -> fp32 is
-// exact), writes the codes into the Q8 tile for the tensor core, arrives on
-// `rdy` and returns the sum of squares of their values.  Not inlined: kept
-// out of the step loop's code, which runs measurably slower otherwise.
-template <int D>
+// bf16 q: a softmax thread rounds its part hf (of TPR) of row t of the Q16
+// tile to E4M3 (the rounding the pre-pass applies to fp32 values; bf16 ->
+// fp32 is exact), writes the codes into the Q8 tile for the tensor core,
+// arrives on `rdy` and returns the sum of squares of their values; the sum
+// of each 32-element chunk goes to qg_own[chunk] and qg_other[chunk].  Not
+// inlined: kept out of the step loop's code, which runs measurably slower
+// otherwise.
+template <int D, int TPR>
 __device__ __noinline__ float q8_from_q16(uint8_t* q8w, int t, int hf, uint32_t rdy, float* qg_own, float* qg_other) {
   using C = Cfg<D>;
   float ss = 0.0f, sc = 0.0f;
   const uint8_t* q16 = q8w + C::Q8_BYTES;
 #pragma unroll
-  for (int u = 0; u < D / 32; ++u) {
-    const int cb = hf * (D / 2) + 16 * u;  // first of the 16 columns
+  for (int u = 0; u < D / (16 * TPR); ++u) {
+    const int cb = hf * (D / TPR) + 16 * u;  // first of the 16 columns
     const uint4 w0 = *reinterpret_cast<const uint4*>(q16 + swz_offset(t, 2 * cb, kBM, 2 * D));
     const uint4 w1 = *reinterpret_cast<const uint4*>(q16 + swz_offset(t, 2 * cb + 16, kBM, 2 * D));
     const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -291,7 +300,7 @@ __device__ __noinline__ float q8_from_q16(uint8_t* q8w, int t, int hf, uint32_t 
     }
     *reinterpret_cast<uint4*>(q8w + swz_offset(t, cb, kBM, D)) = make_uint4(o[0], o[1], o[2], o[3]);
     if (u & 1) {  // a 32-element chunk done: its sum of squares for both threads of the row
-      const int ch = hf * (D / 64) + (u >> 1);
+      const int ch = hf * (D / (32 * TPR)) + (u >> 1);
       qg_own[ch] = sc;
       qg_other[ch] = sc;
       ss += sc;
@@ -680,28 +689,32 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // Two threads per query row: warps 8tt+rw and 8tt+4+rw hold TMEM lanes
-    // 32rw.. of tile tt, the first for key columns 0..31 of each step, the
-    // second for 32..63.  Every softmax thread of a tile runs every step of
+    // TPR threads per query row: warps 4 TPR tt + 4 hf + rw (hf < TPR) hold
+    // TMEM lanes 32rw.. of tile tt, each for key columns hf NC .. hf NC +
+    // NC - 1 of every step; row values are exchanged through shared memory
+    // behind a named barrier of the TPR warps.  Every softmax thread of a tile runs every step of
     // the tile, also after a failed wait (its later waits and TMEM accesses
     // are then skipped), so named barriers never miss a participant; waits
     // are warp-uniform so the .sync.aligned TMEM accesses stay converged.
-    constexpr int NC = kNC;               // logits per thread per step
-    const int tt = warp >> 3;             // query tile
-    const int hf = (warp >> 2) & 1;       // column half
+    constexpr int NC = C::NC;             // logits per thread per step
+    constexpr int TPR = C::TPR;           // threads per row
+    constexpr uint32_t kAll = NC == 32 ? 0xFFFFFFFFu : ((1u << NC) - 1u);  // all NC columns visible
+    const int tt = warp / (4 * TPR);      // query tile
+    const int hf = (warp >> 2) % TPR;     // column part: keys hf NC .. hf NC + NC - 1 of a step
     const int rw = warp & 3;              // 32-row group of the tile
     const int t = rw * 32 + lane;         // row within the tile == TMEM lane
     const int col0 = hf * NC;
     const int R = q0 + tt * kBM + t;
     const int jlo_t = JLO(tt), nsteps = JHI(tt) - JLO(tt);
-    const uint32_t tile_bar = 1 + tt;             // the tile's 256 softmax threads
-    const uint32_t pair_bar = 3 + 4 * tt + rw;    // the two warps of these 32 rows
+    const uint32_t tile_bar = 1 + tt;             // the tile's softmax threads
+    const uint32_t pair_bar = 3 + 4 * tt + rw;    // the TPR warps of these 32 rows
+    constexpr int kPairThreads = 32 * TPR;
     const uint32_t lane_base = tmem + tt * C::TILE_COLS + ((uint32_t)(rw * 32) << 16);
     const uint8_t* sQ8 = smem + C::OFF_Q + tt * C::QT_BYTES;
     uint8_t* sP = smem + C::OFF_P + tt * C::P_BYTES;
     const uint8_t* tab = misc + M_EXP8;
-    float* xch = (float*)(misc + M_XCH) + tt * 2 * kBM;
-    uint32_t* xb = (uint32_t*)(misc + M_XB) + tt * 2 * kBM;
+    float* xch = (float*)(misc + M_XCH) + tt * TPR * kBM;
+    uint32_t* xb = (uint32_t*)(misc + M_XB) + tt * TPR * kBM;
     int lo, hi;
     row_range(p, R, lo, hi);
     // key tiles the row sees whole: [jf0, jf1] (empty for a row past the end)
@@ -710,26 +723,36 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
     float l = 0.0f;  // this half's running sum of the (rounded) P values fed to P.V
     bool fail = !(nsteps > 0 && wait_bar_warp(cx, bar(M_Q_FULL), 0));
     float nq = 0.0f;
-    // this thread's copy of the row's weights of the exactness bound (below)
-    float* qg = (float*)(misc + M_QG) + ((hf * C::NT + tt) * kBM + t) * C::CH;
+    // The row's weights of the exactness bound (below): two threads a row
+    // keep a copy each in shared memory; four (d = 256) keep them in
+    // registers, the shared array then holding the row's chunk sums once.
+    float* qg = (float*)(misc + M_QG) + (((TPR == 2 ? hf : 0) * C::NT + tt) * kBM + t) * C::CH;
+    float qgr[TPR == 2 ? 1 : C::CH];
+    auto QG = [&](int c) -> float& {
+      if constexpr (TPR == 2) return qg[c]; else return qgr[c];
+    };
     if (!kSweep && p.q8_in_cta) {
-      // bf16 q: Q8 and this half's sums of squares from the Q16 tile, per
-      // 32-element chunk into both threads' copies; the row's two halves
-      // are added for ||fl8(q_r)||
+      // bf16 q: Q8 and this part's sums of squares from the Q16 tile, per
+      // 32-element chunk (into both threads' copies with two threads a
+      // row); the row's parts are added for ||fl8(q_r)||
       float ss = 0.0f;
-      float* qg_other = (float*)(misc + M_QG) + (((1 - hf) * C::NT + tt) * kBM + t) * C::CH;
-      if (!fail) ss = q8_from_q16<D>(smem + C::OFF_Q + tt * C::QT_BYTES, t, hf, bar(M_Q8_READY + 8 * tt), qg, qg_other);
+      float* qg_other = (float*)(misc + M_QG) + (((TPR == 2 ? 1 - hf : 0) * C::NT + tt) * kBM + t) * C::CH;
+      if (!fail)
+        ss = q8_from_q16<D, TPR>(smem + C::OFF_Q + tt * C::QT_BYTES, t, hf, bar(M_Q8_READY + 8 * tt), qg, qg_other);
       xb[hf * kBM + t] = __float_as_uint(ss);
-      bar_sync(pair_bar, 64);
+      bar_sync(pair_bar, kPairThreads);
       // upper bounds of the norms: the float sums of squares are rounded up
-      if (R < p.N) nq = sqrtf(__uint_as_float(xb[t]) + __uint_as_float(xb[kBM + t])) * (1.0f + 0x1p-16f);
+      float sst = 0.0f;
 #pragma unroll
-      for (int c = 0; c < C::CH; ++c) qg[c] = sqrtf(qg[c]) * (1.0f + 0x1p-16f);
+      for (int p2 = 0; p2 < TPR; ++p2) sst += __uint_as_float(xb[p2 * kBM + t]);
+      if (R < p.N) nq = sqrtf(sst) * (1.0f + 0x1p-16f);
+#pragma unroll
+      for (int c = 0; c < C::CH; ++c) QG(c) = sqrtf(qg[c]) * (1.0f + 0x1p-16f);
     } else {
       const size_t row = ((size_t)b * p.Hq + h) * p.N + R;
       if (R < p.N) nq = p.nq[row];
 #pragma unroll
-      for (int c = 0; c < C::CH; ++c) qg[c] = R < p.N ? p.nqc[row * C::CH + c] : 0.0f;
+      for (int c = 0; c < C::CH; ++c) QG(c) = R < p.N ? p.nqc[row * C::CH + c] : 0.0f;
     }
     // Exactness guard: |A_tc - A| sigma <= G.  Instruction c of the FP8
     // tensor-core chain (K = 32: chunk c of d) aligns the accumulator D_c and
@@ -748,7 +771,7 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
     // (chunked logits: each chunk is one instruction with a zero
     // accumulator, its own bound without the chain factor C - c)
     for (int c = 0; c < C::CH; ++c)
-      qg[c] = (qg[c] + 0x1p-6f) * (40.0f * 0x1p-25f * (kChunk ? 1.0f : (float)(C::CH - c))) * p.sigma_f;
+      QG(c) = (QG(c) + 0x1p-6f) * (40.0f * 0x1p-25f * (kChunk ? 1.0f : (float)(C::CH - c))) * p.sigma_f;
     const float satq = p.sigma_f * nq * (1.0f + p.guard);
     uint32_t c_h0 = 0, c_h1 = 0, c_h2 = 0, c_strips = 0, c_st1 = 0, c_fl = 0, c_sat = 0, c_fix = 0,
              c_res = 0, c_fmax = 0;  // per-thread counts (a CTA sees at most 2^21 logits per thread slot)
@@ -780,7 +803,7 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
       const float nk = nk_next;  // loaded one step ahead
       if (jj + 1 < nsteps) nk_next = nkrow[jt + 1];
       bool rowvis = true;
-      uint32_t vm = 0xFFFFFFFFu;  // visible columns of this half (bit c = key k0 + col0 + c)
+      uint32_t vm = kAll;  // visible columns of this part (bit c = key k0 + col0 + c)
       if (jt < jf0 || jt > jf1) {  // the row does not see the whole tile
         const int k0 = jt * kBN;
         const int clo = imax(k0, lo), chi = imin(k0 + kBN - 1, hi);
@@ -788,14 +811,18 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
         const int a = imax(clo - (k0 + col0), 0), z = imin(chi - (k0 + col0), NC - 1);
         vm = (rowvis && a <= z) ? ((z == 31 ? 0xFFFFFFFFu : ((1u << (z + 1)) - 1u)) & ~((1u << a) - 1u)) : 0u;
       }
-      const bool all_full = __all_sync(0xffffffffu, vm == 0xFFFFFFFFu);
+      const bool all_full = __all_sync(0xffffffffu, vm == kAll);
       // bound on |A_tc sigma - A sigma| for this row and tile (see qg)
       float G = 0.0f;
 #pragma unroll
       for (int c = 0; c < (kChunk ? 0 : C::CH); c += (C::CH >= 4 ? 4 : 2)) {
         if constexpr (C::CH >= 4) {
           const float4 kb = *reinterpret_cast<const float4*>(nkcrow + (size_t)jt * C::CH + c);
-          const float4 qw = *reinterpret_cast<const float4*>(qg + c);
+          float4 qw;
+          if constexpr (TPR == 2)
+            qw = *reinterpret_cast<const float4*>(qg + c);
+          else
+            qw = make_float4(QG(c), QG(c + 1), QG(c + 2), QG(c + 3));
           G = fmaf(qw.x, kb.x, fmaf(qw.y, kb.y, fmaf(qw.z, kb.z, fmaf(qw.w, kb.w, G))));
         } else {
           const float2 kb = *reinterpret_cast<const float2*>(nkcrow + (size_t)jt * C::CH + c);
@@ -830,13 +857,13 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
           uint32_t a32[NC];
           if (!fail) {
             tc_fence_after();
-            tmem_ld32(lane_base + C::S8_OFF + c * kBN + col0, a32);
+            tmem_ld_n(lane_base + C::S8_OFF + c * kBN + col0, a32);
             tmem_wait_ld();
           } else {
 #pragma unroll
             for (int e = 0; e < NC; ++e) a32[e] = 0u;
           }
-          const float gc = qg[c] * nkcrow[(size_t)jt * C::CH + c];
+          const float gc = QG(c) * nkcrow[(size_t)jt * C::CH + c];
           uint32_t ucm = 0u;  // logits whose rounding of this chunk is uncertain
 #pragma unroll
           for (int i = 0; i < NC / 2; ++i) {
@@ -896,7 +923,7 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
       uint32_t a32[NC];
       if (!fail) {
         tc_fence_after();
-        tmem_ld32(lane_base + C::S8_OFF + col0, a32);
+        tmem_ld_n(lane_base + C::S8_OFF + col0, a32);
         tmem_wait_ld();
       } else {
 #pragma unroll
@@ -986,12 +1013,14 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
       // ---- tile max over both halves.  The largest cl is a lower bound of
       // it and the largest ch of the uncertain logits an upper bound; they
       // agree unless an uncertain logit may be the maximum (rare).
-      float2* xlh = (float2*)(misc + M_XLH) + tt * 2 * kBM;
+      float2* xlh = (float2*)(misc + M_XLH) + tt * TPR * kBM;
       float lo_row, hi_row;
       {
         __half2 mx;
         if (all_full) {
-          mx = __hmax2(__hmax2(as_half2(gmx[0]), as_half2(gmx[1])), __hmax2(as_half2(gmx[2]), as_half2(gmx[3])));
+          mx = as_half2(gmx[0]);
+#pragma unroll
+          for (int g8 = 1; g8 < NC / 8; ++g8) mx = __hmax2(mx, as_half2(gmx[g8]));
         } else {
           mx = as_half2(s8h[0]);
 #pragma unroll
@@ -1001,10 +1030,16 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
         const __half2 hx = as_half2(hmx);
         const float hi = fmaxf(lo, fmaxf(__low2float(hx), __high2float(hx)));
         xlh[hf * kBM + t] = make_float2(lo, hi);
-        bar_sync(pair_bar, 64);
-        const float2 o = xlh[(1 - hf) * kBM + t];
-        lo_row = fmaxf(lo, o.x);
-        hi_row = fmaxf(hi, o.y);
+        bar_sync(pair_bar, kPairThreads);
+        lo_row = lo;
+        hi_row = hi;
+#pragma unroll
+        for (int p2 = 0; p2 < TPR; ++p2) {
+          if (p2 == hf) continue;
+          const float2 o = xlh[p2 * kBM + t];
+          lo_row = fmaxf(lo_row, o.x);
+          hi_row = fmaxf(hi_row, o.y);
+        }
       }
       // Uncertain logits are settled in up to two passes.  Pass 0 (only if
       // an uncertain logit may be a row's maximum; the same decision in both
@@ -1096,11 +1131,14 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
               const uint32_t hv = e4m3_f16_of_product(acc, p.sig18);
               // replace half (cb & 1) of pair cb >> 1: a switch with constant
               // indices keeps s8h in registers
-              static_assert(NC == 32, "the switch below lists 16 pairs");
+              static_assert(NC == 32 || NC == 16, "the switch below lists up to 16 pairs");
               const uint32_t keep = (cb & 1) ? 0x0000FFFFu : 0xFFFF0000u;
               const uint32_t put = (hv * 0x00010001u) & ~keep;
               switch (cb >> 1) {
-#define LAMP_FIX_CASE(i) case i: s8h[i] = (s8h[i] & keep) | put; break;
+#define LAMP_FIX_CASE(i) \
+  case i:                  \
+    if constexpr (i < NC / 2) s8h[i] = (s8h[i] & keep) | put; \
+    break;
                 LAMP_FIX_CASE(0) LAMP_FIX_CASE(1) LAMP_FIX_CASE(2) LAMP_FIX_CASE(3)
                 LAMP_FIX_CASE(4) LAMP_FIX_CASE(5) LAMP_FIX_CASE(6) LAMP_FIX_CASE(7)
                 LAMP_FIX_CASE(8) LAMP_FIX_CASE(9) LAMP_FIX_CASE(10) LAMP_FIX_CASE(11)
@@ -1119,8 +1157,11 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
           for (int i = 1; i < NC / 2; ++i) mx = __hmax2(mx, as_half2(s8h[i]));
           const float mine = fmaxf(__low2float(mx), __high2float(mx));
           xch[hf * kBM + t] = mine;
-          bar_sync(pair_bar, 64);
-          m_tile = fmaxf(mine, xch[(1 - hf) * kBM + t]);
+          bar_sync(pair_bar, kPairThreads);
+          m_tile = mine;
+#pragma unroll
+          for (int p2 = 0; p2 < TPR; ++p2)
+            if (p2 != hf) m_tile = fmaxf(m_tile, xch[p2 * kBM + t]);
         }
       }
       const float m_new = rowvis ? fmaxf(m, m_tile) : m;
@@ -1158,8 +1199,12 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
           }
           const float mine = fminf(__low2float(mn), __high2float(mn));
           xb[hf * kBM + t] = __float_as_uint(mine);
-          bar_sync(pair_bar, 64);
-          if (scan) A = fmaxf(A, -fminf(mine, __uint_as_float(xb[(1 - hf) * kBM + t])));
+          bar_sync(pair_bar, kPairThreads);
+          float mn_row = mine;
+#pragma unroll
+          for (int p2 = 0; p2 < TPR; ++p2)
+            if (p2 != hf) mn_row = fminf(mn_row, __uint_as_float(xb[p2 * kBM + t]));
+          if (scan) A = fmaxf(A, -mn_row);
         }
         if (rowvis && st1) {
           const int e = (int)((__float_as_uint(A) >> 23) & 0xFFu) - 127;  // floor(log2 A), A >= 2^-6
@@ -1183,8 +1228,12 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
           }
         }
         xb[hf * kBM + t] = mine;
-        bar_sync(pair_bar, 64);
-        if (maybe_neg) flg = (mine | xb[(1 - hf) * kBM + t]) != 0u;
+        bar_sync(pair_bar, kPairThreads);
+        uint32_t any_neg = mine;
+#pragma unroll
+        for (int p2 = 0; p2 < TPR; ++p2)
+          if (p2 != hf) any_neg |= xb[p2 * kBM + t];
+        if (maybe_neg) flg = any_neg != 0u;
       }
       if (__any_sync(0xffffffffu, rowvis && satp)) {  // warp-uniform: rare
 #pragma unroll
@@ -1274,9 +1323,9 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
       const float alpha = (m_new == m) ? 1.0f : (m == -INFINITY ? 0.0f : ex2_approx((m - m_new) * kLog2e));
       if (!fail && jj > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
         tc_fence_after();
-        // this half rescales O columns [hf D/2, (hf+1) D/2)
+        // this part rescales O columns [hf D/TPR, (hf+1) D/TPR)
 #pragma unroll 1
-        for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+        for (int c0 = hf * (D / TPR); c0 < (hf + 1) * (D / TPR); c0 += 32) {
           uint32_t o[32];
           tmem_ld32(lane_base + c0, o);
           tmem_wait_ld();
@@ -1304,7 +1353,7 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
       if (any && !fail) {
         tc_fence_after();
         uint32_t r16[NC];
-        tmem_ld32(lane_base + C::S16_OFF + (C::S16_BUFS == 2 ? (jj & 1) * kBN : 0) + col0, r16);
+        tmem_ld_n(lane_base + C::S16_OFF + (C::S16_BUFS == 2 ? (jj & 1) * kBN : 0) + col0, r16);
         tmem_wait_ld();
         if (my_flag && rowvis) {
           const float sl2 = sig * kLog2e, ml = m_new * kLog2e;
@@ -1338,22 +1387,22 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
           // tile with P16 in those rows and 0 in the others
 #pragma unroll
           for (int k = 0; k < 2; ++k)
-            *reinterpret_cast<uint4*>(sP + C::P16_BYTES + swz_offset(t, hf * 32 + 16 * k, kBM, 64)) =
+            *reinterpret_cast<uint4*>(sP + C::P16_BYTES + swz_offset(t, col0 + 16 * k, kBM, 64)) =
                 make_uint4(pc[4 * k], pc[4 * k + 1], pc[4 * k + 2], pc[4 * k + 3]);
           if (any) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < NC / 8; ++k) {
               const uint4 v4 = my_flag ? make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3])
                                        : make_uint4(0u, 0u, 0u, 0u);
-              *reinterpret_cast<uint4*>(sP + swz_offset(t, (4 * hf + k) * 16, kBM, 128)) = v4;
+              *reinterpret_cast<uint4*>(sP + swz_offset(t, 2 * col0 + 16 * k, kBM, 128)) = v4;
             }
           }
         } else {
-          // P row half -> shared memory (K-major, 128-byte swizzle)
+          // this part of the P row -> shared memory (K-major, 128-byte swizzle)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < NC / 8; ++k) {
             const uint4 v4 = make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
-            *reinterpret_cast<uint4*>(sP + swz_offset(t, (4 * hf + k) * 16, kBM, 128)) = v4;
+            *reinterpret_cast<uint4*>(sP + swz_offset(t, 2 * col0 + 16 * k, kBM, 128)) = v4;
           }
         }
         fence_proxy_async_smem();
@@ -1367,8 +1416,10 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
 
     // ---- epilogue: l of the row = sum of both halves; out = O / l, LSE = m + ln l
     xch[hf * kBM + t] = l;
-    bar_sync(pair_bar, 64);
-    const float lrow = l + xch[(1 - hf) * kBM + t];
+    bar_sync(pair_bar, kPairThreads);
+    float lrow = 0.0f;  // the parts in a fixed order: the same sum in every thread of the row
+#pragma unroll
+    for (int p2 = 0; p2 < TPR; ++p2) lrow += xch[p2 * kBM + t];
     if (kSweep) done_ok = false;  // no output
     if (done_ok) done_ok = wait_bar_warp(cx, bar(M_PV_DONE + 8 * tt), (nsteps - 1) & 1);
     if (done_ok) {
@@ -1380,7 +1431,7 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
       char* orow = (char*)p.out + ((size_t)b * p.o_stride[0] + (size_t)R * p.o_stride[1] +
                                    (size_t)h * p.o_stride[2]) * (p.out_f32 ? 4 : 2);
 #pragma unroll 1
-      for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 16) {
+      for (int c0 = hf * (D / TPR); c0 < (hf + 1) * (D / TPR); c0 += 16) {
         uint32_t o[16];
         tmem_ld16(lane_base + c0, o);
         tmem_wait_ld();

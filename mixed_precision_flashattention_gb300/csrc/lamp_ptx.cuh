@@ -186,6 +186,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
+// 32 or 16 consecutive columns of the warp's 32 lanes, by the array's size
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 32 || N == 16, "32 or 16 columns");
+  if constexpr (N == 32)
+    tmem_ld32(taddr, r);
+  else
+    tmem_ld16(taddr, r);
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
