@@ -55,9 +55,10 @@ struct Cfg {
   static constexpr int NT = (D == 256 || (OPT != 0 && D == 128)) ? 1 : 2;
   static constexpr int NS = (D == 256) ? 1 : 2;  // K/V stages
   // softmax threads per query row: two, each with 32 of a step's 64 keys;
-  // four at d = 256 (16 keys each), so that its one query tile per CTA still
-  // has 16 softmax warps to hide latency with
-  static constexpr int TPR = (D == 256) ? 4 : 2;
+  // four (16 keys each) with one query tile per CTA (d = 256, and the
+  // optional modes at d = 128), so that the tile still has 16 softmax warps
+  // to hide latency with
+  static constexpr int TPR = (NT == 1) ? 4 : 2;
   static constexpr int NC = kBN / TPR;                  // logits per softmax thread per step
   static constexpr int SM_THREADS = kBM * TPR;          // softmax threads per tile
   static constexpr int SM_WARPS = NT * SM_THREADS / 32;
@@ -863,7 +864,11 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
 #pragma unroll
             for (int e = 0; e < NC; ++e) a32[e] = 0u;
           }
-          const float gc = QG(c) * nkcrow[(size_t)jt * C::CH + c];
+          float qw = 0.0f;  // QG(c) with constant indices (no local memory)
+#pragma unroll
+          for (int cc = 0; cc < C::CH; ++cc)
+            if (cc == c) qw = QG(cc);
+          const float gc = qw * nkcrow[(size_t)jt * C::CH + c];
           uint32_t ucm = 0u;  // logits whose rounding of this chunk is uncertain
 #pragma unroll
           for (int i = 0; i < NC / 2; ++i) {
@@ -886,10 +891,13 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
             const int cb = __shfl_sync(0xffffffffu, ucm ? (__ffs(ucm) - 1) : 0, src);
             const long long acc = exact_dot_chunk<D>(sQ8, sK8c, rw * 32 + src, col0 + cb, c, lane);
             if (lane == src) {
-              static_assert(NC == 32, "the switches below list 16 pairs");
+              static_assert(NC == 32 || NC == 16, "the switches below list up to 16 pairs");
               uint32_t w = 0u;
               switch (cb >> 1) {
-#define LAMP_GET_CASE(i) case i: w = s8h[i]; break;
+#define LAMP_GET_CASE(i) \
+  case i:                \
+    if constexpr (i < NC / 2) w = s8h[i]; \
+    break;
                 LAMP_GET_CASE(0) LAMP_GET_CASE(1) LAMP_GET_CASE(2) LAMP_GET_CASE(3)
                 LAMP_GET_CASE(4) LAMP_GET_CASE(5) LAMP_GET_CASE(6) LAMP_GET_CASE(7)
                 LAMP_GET_CASE(8) LAMP_GET_CASE(9) LAMP_GET_CASE(10) LAMP_GET_CASE(11)
@@ -902,7 +910,10 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
               const uint32_t keep = (cb & 1) ? 0x0000FFFFu : 0xFFFF0000u;
               const uint32_t put = (hv * 0x00010001u) & ~keep;
               switch (cb >> 1) {
-#define LAMP_PUT_CASE(i) case i: s8h[i] = (s8h[i] & keep) | put; break;
+#define LAMP_PUT_CASE(i) \
+  case i:                \
+    if constexpr (i < NC / 2) s8h[i] = (s8h[i] & keep) | put; \
+    break;
                 LAMP_PUT_CASE(0) LAMP_PUT_CASE(1) LAMP_PUT_CASE(2) LAMP_PUT_CASE(3)
                 LAMP_PUT_CASE(4) LAMP_PUT_CASE(5) LAMP_PUT_CASE(6) LAMP_PUT_CASE(7)
                 LAMP_PUT_CASE(8) LAMP_PUT_CASE(9) LAMP_PUT_CASE(10) LAMP_PUT_CASE(11)
@@ -1386,7 +1397,7 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
           // sub-blocks) and, when the step has a flagged sub-block, the P16
           // tile with P16 in those rows and 0 in the others
 #pragma unroll
-          for (int k = 0; k < 2; ++k)
+          for (int k = 0; k < NC / 16; ++k)
             *reinterpret_cast<uint4*>(sP + C::P16_BYTES + swz_offset(t, col0 + 16 * k, kBM, 64)) =
                 make_uint4(pc[4 * k], pc[4 * k + 1], pc[4 * k + 2], pc[4 * k + 3]);
           if (any) {
