@@ -1066,6 +1066,23 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
 #pragma unroll 1
       for (int pass = max_unc ? 0 : (__any_sync(0xffffffffu, unc != 0u) ? 1 : 2); pass < 2; ++pass) {
         uint32_t ex = 0u;  // logits to re-derive exactly in this pass
+        if (!kSweep && pass == 1) {
+          // With the row maximum exact, a row whose own maximum flags it
+          // (P8 of the maximum >= delta and the maximum >= tau_abs: a flagged
+          // entry) flags its sub-block.  Every row of a sub-block flagged
+          // this way takes P16 (from the 16-bit products and the exact m),
+          // the sub-block's stage-1 bit comes from the row maxima, and the
+          // flag is set whatever its other logits are: their uncertain ones
+          // can change nothing except the saturation count (kept when the
+          // tile can saturate) and are left unresolved.
+          const float mnr = rowvis ? fmaxf(m, m_tile) : m;
+          const bool st1m = rowvis && tab[cvt_e4m3x2(0.0f, m_tile - mnr) & 0xFFu] >= dcode;
+          const bool rowflag =
+              rowvis && (p.force == 1 || (p.force == 0 && st1m && (T <= 0.0f || m_tile >= T)));
+          const unsigned bfc = __ballot_sync(0xffffffffu, rowflag);
+          const bool sb_flagged = ((lane >> 4) ? (bfc >> 16) : (bfc & 0xFFFFu)) != 0u;
+          if (sb_flagged && !satp) unc = 0u;
+        }
         if constexpr (kNoStage1) {
           // first stage off: most uncertain logits straddle +-tau_abs, where
           // the comparison of the candidates cannot settle them (measured:
