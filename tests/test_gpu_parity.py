@@ -151,3 +151,16 @@ def test_small_logits_negative_maxima(t):
     negative logits decide the flags."""
     q, k, v = synth.gen_iid(1, 320, 2, 1, 128, seed=62, scale=0.35)
     _compare(q, k, v, "bf16", tau=2.0 ** -t, mask="sliding", window=150)
+
+
+def test_saturating_logits_in_flagged_sub_blocks():
+    """8-bit logits at the 448 limit inside flagged sub-blocks: the
+    saturation count stays exact there (uncertain logits of sub-blocks a
+    row maximum already flags are otherwise left unresolved).  The 16-bit
+    logits of the large keys exceed 448 too, so no row's P16 falls into
+    fp16's subnormal range (reading R13's extreme case)."""
+    q, k, v = synth.gen_iid(1, 256, 2, 1, 64, seed=63)
+    q[0, :, :, 0] = np.linspace(80, 120, 256)[:, None]
+    k[0, [5, 70, 71, 130], 0, 0] = [46.0, 47.0, 45.0, 48.0]
+    gc, ref = _compare(q, k, v, "fp32", tau=0.5)
+    assert ref.counters[7] > 0 and ref.counters[6] > 0
