@@ -1,12 +1,17 @@
 // lamp_fwd.cu -- fused LampAttention forward kernel for sm_103a.
 //
 // One CTA computes NT query tiles of 128 rows (NT = 2 for d <= 128, 1 for
-// d = 256) of one (batch, query head) against their visible 64-key tiles,
-// in ascending key order (the running maximum of the method is defined
-// over that order).  The tiles share the K/V stages and ping-pong: while
-// the softmax warps of one tile work, the tensor core serves the other.
-// Warp roles (TPR softmax threads per query row: 2, and 4 at d = 256, so
-// that its one tile per CTA still has 16 softmax warps):
+// d = 256 and for the optional modes at d = 128) of one (batch, query
+// head) against their visible 64-key tiles, in ascending key order (the
+// running maximum of the method is defined over that order).  The tiles
+// share the K/V stages and ping-pong: while the softmax warps of one tile
+// work, the tensor core serves the other.  Optional modes (template bits):
+// FP8 P.V for the rows of unflagged sub-blocks (P8 . V8, V8 = fl8(v)
+// transposed by the pre-pass; P16 . V16 only for steps with a flagged
+// sub-block), and 8-bit logits rounded after every 32-element chunk of d
+// (one accumulator per chunk, combined on the CUDA cores).
+// Warp roles (TPR softmax threads per query row: 2, and 4 with one tile per
+// CTA, so that the tile still has 16 softmax warps):
 //   warps 4 TPR t .. 4 TPR t + 4 TPR - 1  softmax of tile t: warps
 //              4 TPR t + 4 j + w (j < TPR) hold TMEM lanes 32w.. for key
 //              columns 64 j / TPR .. of each step.  Per step: 8-bit logits S8 (with an
@@ -23,7 +28,9 @@
 //              (kind::f16, BF16) into its own S16 buffer, only for steps with
 //              a flagged sub-block -- issued ahead of the decision for the
 //              first step and after a flagged step, else once the decision
-//              is published; O += P V16 (kind::f16, V MN-major).
+//              is published; O += P V16 (kind::f16, V MN-major), or in the
+//              FP8 P.V mode O += P8 V8 (kind::f8f6f4, both K-major) and,
+//              for steps with a flagged sub-block, O += P16 V16.
 //
 // The method follows "LampAttention: Look-Ahead Mixed-Precision
 // FlashAttention for Dedicated Accelerators" (abstract: 8-bit key-query
