@@ -270,6 +270,9 @@ def main():
                     help="input generator in place of the workload's own (same shape)")
     ap.add_argument("--pv", default="fp16", choices=["fp16", "fp8"],
                     help="P.V precision of unflagged sub-blocks (fp8: the optional FP8 P.V mode)")
+    ap.add_argument("--kv-prepared", action="store_true",
+                    help="keys and values prepared once (lamp_kv_prepare) before the timed steps: "
+                         "each step is the forward call on the prepared K/V cache")
     ap.add_argument("--qk", default="exact", choices=["exact", "chunk32"],
                     help="8-bit logit accumulation (chunk32: rounded after every 32-element chunk of d)")
     ap.add_argument("--parity-tiles", type=int, default=64,
@@ -286,7 +289,8 @@ def main():
     config = {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "heads_q": w.heads_q,
               "heads_kv": w.heads_kv, "head_dim": w.head_dim, "mask": w.mask, "window": w.window,
               "in_dtype": w.dtype, "tau": args.tau, "delta": args.delta,
-              "generator": w.gen, "seed": args.seed, "pv": args.pv, "qk": args.qk}
+              "generator": w.gen, "seed": args.seed, "pv": args.pv, "qk": args.qk,
+              "kv_prepared": bool(args.kv_prepared)}
 
     if args.impl == "reference" and rank != 0:
         return  # the oracle arm runs on rank 0 only
@@ -345,10 +349,13 @@ def main():
     ws = torch.empty(lamp.workspace_bytes(qd, kd, vd, out, pv=args.pv, qk=args.qk), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    if args.kv_prepared:  # the K/V cache, once, outside the timed region
+        lamp.kv_prepare(kd, vd, ws, pv=args.pv, qk=args.qk)
+
     def step(evs=None, o=out, l=lse, qq=qd, kk=kd, vv=vd):
         lamp.lamp_attn_fwd(qq, kk, vv, mask=w.mask, window=w.window, delta=args.delta, tau=args.tau,
                            out=o, lse=l, mask_bytes=mbytes, counters=cnt, workspace=ws, stage_events=evs,
-                           pv=args.pv, qk=args.qk)
+                           pv=args.pv, qk=args.qk, kv_prepared=args.kv_prepared)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -491,8 +498,10 @@ def main():
         "tau_sweep": {"taus": sweep_taus, "ms": sweep_ms, "forward_ms": ms, "speedup_vs_forward_per_tau":
                       len(sweep_taus) * ms / sweep_ms,
                       "tiles_0_1_2plus": [[float(x) / max(1, hrow[0]) for x in hrow[1:]] for hrow in sw_hist]},
-        # pre-pass (+ the V8 copy for the FP8 P.V) + fused kernel per step and rank
-        "gpu_launches": (3 if args.pv == "fp8" else 2) * K * world,
+        # pre-pass (+ the V8 copy for the FP8 P.V) + fused kernel per step and rank; with a
+        # prepared K/V cache and bf16 q the pre-pass has no work and is not launched
+        "gpu_launches": (1 if (args.kv_prepared and w.dtype == "bf16") else
+                         (2 if args.kv_prepared else (3 if args.pv == "fp8" else 2))) * K * world,
         "clocks": clocks,
     }
     if want_cpu:

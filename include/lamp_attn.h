@@ -146,6 +146,10 @@ typedef struct {
   int32_t pv_mode;       /* lamp_pv_mode; 0 = LAMP_PV_FP16 (zero-initialised
                             shapes keep the FP16 path) */
   int32_t qk_accum;      /* lamp_qk_accum; 0 = LAMP_QK_EXACT */
+  int32_t kv_prepared;   /* 1: `workspace` already holds this k / v's 8-bit and
+                            16-bit copies and key-tile norms, written by
+                            lamp_kv_prepare with the same shapes (the forward
+                            call then skips that work); 0: the call writes them */
 } lamp_shapes;
 
 typedef struct {
@@ -179,6 +183,29 @@ typedef struct {
 int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out,
                   float* lse, const lamp_shapes* shapes, int mask_kind,
                   float delta, float tau, lamp_stats* stats);
+
+/*
+ * lamp_kv_prepare: the key/value half of lamp_attn_fwd's pre-pass on its
+ * own: writes into shapes->workspace the E4M3 copy of k, the fp16 copy of v
+ * (and, for fp32 inputs, the bf16 copy of k; for LAMP_PV_FP8 the
+ * transposed E4M3 copy of v) and the per-key-tile norms that size the
+ * exactness guard.  A K/V cache in the attention's own formats: any number
+ * of lamp_attn_fwd calls with shapes->kv_prepared = 1, the same workspace,
+ * the same k and v (unchanged since) and the same batch, seqlen, heads_kv,
+ * head_dim, in_dtype, k / v strides and modes then skip that work and give
+ * bit-identical results; their heads_q (any multiple of heads_kv), q, out
+ * and strides may differ (the keys' and values' place in the workspace does
+ * not depend on them).
+ *   k, v      DEVICE, as for lamp_attn_fwd.
+ *   shapes    workspace must be given (>= lamp_attn_workspace_bytes() of
+ *             these shapes; the later calls check their own size);
+ *             kv_prepared is ignored; q_stride / o_stride are not used.
+ * Asynchronous on shapes->stream; LAMP_ERR_INVALID_ARG for a missing
+ * workspace, otherwise errors as lamp_attn_fwd.  Not for
+ * lamp_attn_fwd_host / lamp_attn_fwd_noalloc (their scratch is their own:
+ * they return LAMP_ERR_INVALID_ARG for kv_prepared = 1).
+ */
+int lamp_kv_prepare(const void* k, const void* v, const lamp_shapes* shapes);
 
 /* Bytes of device workspace lamp_attn_fwd needs for these shapes (E4M3
  * copies of q and k, an fp16 copy of v, bf16 copies of fp32 inputs,

@@ -83,21 +83,25 @@ WsLayout ws_layout(const lamp_shapes& s) {
   const size_t T = (N + kBN - 1) / kBN;
   WsLayout w{};
   size_t o = 0;
-  w.q8 = o; o = align256(o + B * Hq * N * D);
+  // keys and values first: their place does not depend on the query heads,
+  // so one lamp_kv_prepare serves calls with any number of them
   w.k8 = o; o = align256(o + B * Hkv * N * D);
   w.v16 = o; o = align256(o + B * Hkv * N * D * 2);
   if (s.in_dtype == LAMP_DT_FP32) {
-    w.q16 = o; o = align256(o + B * Hq * N * D * 2);
     w.k16 = o; o = align256(o + B * Hkv * N * D * 2);
   }
   if (s.pv_mode == LAMP_PV_FP8) {  // [B, Hkv, D, T * 64]: keys contiguous
     w.v8t = o; o = align256(o + B * Hkv * D * T * kBN);
   }
-  w.nq = o; o = align256(o + B * Hq * N * 4);
-  w.nqc = o; o = align256(o + B * Hq * N * (D / 32) * 4);
   w.nk = o; o = align256(o + B * Hkv * T * 4);   // nk, nkc and abort are zeroed by one memset
   w.nkc = o; o = align256(o + B * Hkv * T * (D / 32) * 4);
   w.abort = o; o = align256(o + 4);
+  w.q8 = o; o = align256(o + B * Hq * N * D);
+  if (s.in_dtype == LAMP_DT_FP32) {
+    w.q16 = o; o = align256(o + B * Hq * N * D * 2);
+  }
+  w.nq = o; o = align256(o + B * Hq * N * 4);
+  w.nqc = o; o = align256(o + B * Hq * N * (D / 32) * 4);
   w.total = o;
   return w;
 }
@@ -187,6 +191,9 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   if ((pv8 || chunk) && D == 256) return LAMP_ERR_UNSUPPORTED;
   if ((pv8 && chunk) || (sweep && chunk)) return LAMP_ERR_UNSUPPORTED;
   const int opt = pv8 ? 1 : (chunk ? 2 : 0);  // the kernel's optional-mode bits
+  // keys and values prepared by lamp_kv_prepare in the caller's workspace
+  const bool prepared = s.kv_prepared != 0;
+  if (prepared && !s.workspace) return LAMP_ERR_INVALID_ARG;
   if (mask_kind < LAMP_MASK_NONE || mask_kind > LAMP_MASK_SLIDING) return LAMP_ERR_INVALID_ARG;
   if (mask_kind == LAMP_MASK_SLIDING && s.window < 1) return LAMP_ERR_INVALID_ARG;
   if (!(delta >= 0.0f) || std::isnan(tau)) return LAMP_ERR_INVALID_ARG;
@@ -291,12 +298,15 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   if (sweep && cudaMemsetAsync(records, 0, (size_t)B * Hq * T * T * 4, stream) != cudaSuccess)
     return fail(LAMP_ERR_CUDA);
   // norms of the key tiles (whole and per chunk) and the abort word are
-  // contiguous: one memset
-  if (cudaMemsetAsync(ws + w.nk, 0, w.total - w.nk, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
+  // contiguous: one memset (prepared keys keep their norms: the abort word
+  // alone)
+  const size_t z0 = prepared ? w.abort : w.nk;
+  if (cudaMemsetAsync(ws + z0, 0, w.abort + 4 - z0, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
 
   PrepParams pp{};
   pp.q = q; pp.k = k; pp.v = sweep ? nullptr : v;  // the sweep needs no V
   pp.skip_q = fp.q8_in_cta;
+  pp.skip_kv = prepared;  // with bf16 q as well, nothing is left for the pre-pass
   for (int i = 0; i < 3; ++i) { pp.qs[i] = s.q_stride[i]; pp.ks[i] = s.k_stride[i]; pp.vs[i] = s.v_stride[i]; }
   pp.q8 = ws + w.q8; pp.k8 = ws + w.k8; pp.v16 = ws + w.v16;
   pp.q16 = s.in_dtype == LAMP_DT_FP32 ? (void*)(ws + w.q16) : nullptr;
@@ -309,7 +319,8 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   };
   if (!mark(0)) return fail(LAMP_ERR_CUDA);
   if (launch_prep(pp, D, stream) != cudaSuccess) return fail(LAMP_ERR_CUDA);
-  if (pv8 && launch_v8t(v, s.v_stride, s.in_dtype == LAMP_DT_FP32, ws + w.v8t, B, N, Hkv, D, stream) != cudaSuccess)
+  if (pv8 && !prepared &&
+      launch_v8t(v, s.v_stride, s.in_dtype == LAMP_DT_FP32, ws + w.v8t, B, N, Hkv, D, stream) != cudaSuccess)
     return fail(LAMP_ERR_CUDA);
   if (!mark(1)) return fail(LAMP_ERR_CUDA);
 
@@ -319,10 +330,53 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   return LAMP_OK;
 }
 
+// The key/value half of the pre-pass into the caller's workspace (a K/V
+// cache in the attention's own formats; see lamp_kv_prepare).
+int kv_prepare(const void* k, const void* v, const lamp_shapes* shapes) {
+  if (!k || !v || !shapes_ok(shapes)) return LAMP_ERR_INVALID_ARG;
+  const lamp_shapes& s = *shapes;
+  const int D = s.head_dim;
+  if (D != 64 && D != 128 && D != 256) return LAMP_ERR_UNSUPPORTED;
+  const bool pv8 = s.pv_mode == LAMP_PV_FP8;
+  if ((pv8 || s.qk_accum == LAMP_QK_CHUNK32) && D == 256) return LAMP_ERR_UNSUPPORTED;
+  if (pv8 && s.qk_accum == LAMP_QK_CHUNK32) return LAMP_ERR_UNSUPPORTED;
+  const int es_in = s.in_dtype == LAMP_DT_FP32 ? 4 : 2;
+  const int64_t* strides[2] = {s.k_stride, s.v_stride};
+  for (int t = 0; t < 2; ++t)
+    for (int i = 0; i < 3; ++i)
+      if (strides[t][i] < D || (strides[t][i] * es_in) % 16) return LAMP_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v)) return LAMP_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(s);
+  uint8_t* ws = (uint8_t*)s.workspace;
+  if (!ws) return LAMP_ERR_INVALID_ARG;
+  if (s.workspace_bytes < w.total || !aligned16(ws)) return LAMP_ERR_WORKSPACE;
+  int st = device_check();
+  if (st != LAMP_OK) return st;
+  cudaStream_t stream = (cudaStream_t)s.stream;
+  const int B = s.batch, N = s.seqlen, Hq = s.heads_q, Hkv = s.heads_kv;
+  const int T = (N + kBN - 1) / kBN;
+  if (cudaMemsetAsync(ws + w.nk, 0, w.abort + 4 - w.nk, stream) != cudaSuccess) return LAMP_ERR_CUDA;
+  PrepParams pp{};
+  pp.q = nullptr; pp.k = k; pp.v = v;
+  pp.skip_q = 1;
+  for (int i = 0; i < 3; ++i) { pp.qs[i] = s.k_stride[i]; pp.ks[i] = s.k_stride[i]; pp.vs[i] = s.v_stride[i]; }
+  pp.q8 = ws + w.q8; pp.k8 = ws + w.k8; pp.v16 = ws + w.v16;
+  pp.k16 = s.in_dtype == LAMP_DT_FP32 ? (void*)(ws + w.k16) : nullptr;
+  pp.nq = (float*)(ws + w.nq); pp.nkmax = (float*)(ws + w.nk);
+  pp.nqc = (float*)(ws + w.nqc); pp.nkc = (float*)(ws + w.nkc);
+  pp.B = B; pp.N = N; pp.Hq = Hq; pp.Hkv = Hkv; pp.T = T; pp.in_f32 = s.in_dtype == LAMP_DT_FP32;
+  if (launch_prep(pp, D, stream) != cudaSuccess) return LAMP_ERR_CUDA;
+  if (pv8 && launch_v8t(v, s.v_stride, s.in_dtype == LAMP_DT_FP32, ws + w.v8t, B, N, Hkv, D, stream) != cudaSuccess)
+    return LAMP_ERR_CUDA;
+  return LAMP_OK;
+}
+
 }  // namespace
 }  // namespace lamp
 
 extern "C" {
+
+int lamp_kv_prepare(const void* k, const void* v, const lamp_shapes* shapes) { return kv_prepare(k, v, shapes); }
 
 int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const lamp_shapes* shapes,
                   int mask_kind, float delta, float tau, lamp_stats* stats) {

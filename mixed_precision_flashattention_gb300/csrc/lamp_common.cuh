@@ -62,7 +62,8 @@ struct PrepParams {
   float* nqc;                     // [B, Hq, N, D/32] chunk norms
   float* nkc;                     // [B, Hkv, T, D/32] max chunk norms + 2^-6 (zeroed before the launch)
   int B, N, Hq, Hkv, T, in_f32;
-  int skip_q;  // the fused kernel makes Q8 and the q norms itself
+  int skip_q;   // the fused kernel makes Q8 and the q norms itself
+  int skip_kv;  // k / v already prepared (a K/V cache): q rows only
   // division by Hq, Hkv and N as multiply and shift (set by the launcher)
   uint32_t mul_hq, mul_hkv, mul_n;
   int shr_hq, shr_hkv, shr_n;

@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(256) lamp_prep_kernel(const PrepParams p) {
   constexpr int NI = kPrepRows<D> / RPI;  // instructions per group
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, col = (lane % LPR) * 8;
-  const long long nQ = p.skip_q ? 0LL : (long long)p.B * p.N * p.Hq, nK = (long long)p.B * p.N * p.Hkv;
+  const long long nQ = p.skip_q ? 0LL : (long long)p.B * p.N * p.Hq;
+  const long long nK = p.skip_kv ? 0LL : (long long)p.B * p.N * p.Hkv;
   const long long nrows = nQ + (p.v ? 2 : 1) * nK;
   const long long ngroups = (nrows + kPrepRows<D> - 1) / kPrepRows<D>;
   const long long stride = (long long)gridDim.x * 8;
@@ -239,7 +240,9 @@ static long long max_offset(const long long* st, int B, int N, int H, int D) {
 template <int D>
 static cudaError_t launch_prep_d(const PrepParams& p0, cudaStream_t st) {
   PrepParams p = p0;
-  const long long rows = (long long)p.B * p.N * ((p.skip_q ? 0LL : p.Hq) + (p.v ? 2LL : 1LL) * p.Hkv);  // no V rows without v
+  // no V rows without v, no K or V rows for prepared keys and values
+  const long long rows =
+      (long long)p.B * p.N * ((p.skip_q ? 0LL : p.Hq) + (p.skip_kv ? 0LL : (p.v ? 2LL : 1LL) * p.Hkv));
   const long long ngroups = (rows + kPrepRows<D> - 1) / kPrepRows<D>;
   if (ngroups == 0) return cudaSuccess;
   inv_divisor(p.Hq, p.mul_hq, p.shr_hq);

@@ -26,7 +26,7 @@ NUM_COUNTERS = 16
 COUNTER_NAMES = ["tiles", "hist0", "hist1", "hist2p", "strips", "stage1", "flagged",
                  "s8_saturated", "fixups", "status", "recompute_steps", "spec_waste", "recompute_late",
                  "guard_resolved", "fixups_max"]
-EXPORTS = ["lamp_attn_fwd", "lamp_attn_fwd_noalloc", "lamp_attn_workspace_bytes", "lamp_strerror",
+EXPORTS = ["lamp_attn_fwd", "lamp_attn_fwd_noalloc", "lamp_kv_prepare", "lamp_attn_workspace_bytes", "lamp_strerror",
            "lamp_version", "lamp_exp8_table", "lamp_selftest", "lamp_attn_fwd_host",
            "lamp_attn_host_buffer_bytes", "lamp_attn_tau_sweep"]
 
@@ -41,7 +41,7 @@ class LampShapes(ctypes.Structure):
         ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32), ("force", ctypes.c_int32),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("stream", ctypes.c_void_p), ("stage_events", ctypes.c_void_p * 3),
-        ("pv_mode", ctypes.c_int32), ("qk_accum", ctypes.c_int32),
+        ("pv_mode", ctypes.c_int32), ("qk_accum", ctypes.c_int32), ("kv_prepared", ctypes.c_int32),
     ]
 
 
@@ -77,6 +77,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         ctypes.POINTER(LampStats)]
     lib.lamp_attn_fwd_noalloc.restype = ctypes.c_int
     lib.lamp_attn_fwd_noalloc.argtypes = lib.lamp_attn_fwd.argtypes
+    lib.lamp_kv_prepare.restype = ctypes.c_int
+    lib.lamp_kv_prepare.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(LampShapes)]
     lib.lamp_attn_workspace_bytes.restype = ctypes.c_size_t
     lib.lamp_attn_workspace_bytes.argtypes = [ctypes.POINTER(LampShapes)]
     lib.lamp_strerror.restype = ctypes.c_char_p
@@ -105,7 +107,7 @@ def _check(code: int):
 
 
 def make_shapes(q, k, v, out, *, window=0, scale=0.0, force="off", workspace=None, stream=None,
-                stage_events=None, pv="fp16", qk="exact"):
+                stage_events=None, pv="fp16", qk="exact", kv_prepared=False):
     B, N, Hq, d = q.shape
     sh = LampShapes()
     sh.batch, sh.seqlen, sh.heads_q, sh.heads_kv, sh.head_dim = B, N, Hq, k.shape[2], d
@@ -121,6 +123,7 @@ def make_shapes(q, k, v, out, *, window=0, scale=0.0, force="off", workspace=Non
     sh.force = FORCE[force]
     sh.pv_mode = PV[pv]
     sh.qk_accum = QK[qk]
+    sh.kv_prepared = int(bool(kv_prepared))
     if workspace is not None:
         sh.workspace = workspace.data_ptr()
         sh.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -139,14 +142,16 @@ def workspace_bytes(q, k, v, out=None, **kw) -> int:
 
 def lamp_attn_fwd(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -8, tau=2.0 ** -1,
                   force="off", out=None, out_dtype=None, lse=None, want_lse=True, mask_bytes=None,
-                  counters=None, workspace=None, stream=None, stage_events=None, pv="fp16", qk="exact"):
+                  counters=None, workspace=None, stream=None, stage_events=None, pv="fp16", qk="exact",
+                  kv_prepared=False):
     """Forward pass.  q [B, N, Hq, d], k/v [B, N, Hkv, d] CUDA tensors (bf16
     or fp32, d contiguous).  Returns (out, lse, mask_bytes, counters); the
     last three may be None when not requested.  Asynchronous on ``stream``
     (default: torch's current stream).  ``stage_events``: three
     torch.cuda.Event recorded around the pre-pass and the fused kernel.
     ``pv``: "fp16" or "fp8", the P.V precision of unflagged sub-blocks.
-    ``qk``: "exact" or "chunk32", how the 8-bit logits accumulate."""
+    ``qk``: "exact" or "chunk32", how the 8-bit logits accumulate.
+    ``kv_prepared``: ``workspace`` holds this k / v prepared by kv_prepare."""
     lib = load()
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
         raise LampError("q, k, v must be CUDA tensors")
@@ -158,7 +163,7 @@ def lamp_attn_fwd(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, N), device=q.device, dtype=torch.float32)
     sh = make_shapes(q, k, v, out, window=window, scale=scale, force=force, workspace=workspace,
-                     stream=stream, stage_events=stage_events, pv=pv, qk=qk)
+                     stream=stream, stage_events=stage_events, pv=pv, qk=qk, kv_prepared=kv_prepared)
     stats = LampStats()
     stats.mask = mask_bytes.data_ptr() if mask_bytes is not None else None
     stats.counters = counters.data_ptr() if counters is not None else None
@@ -167,6 +172,16 @@ def lamp_attn_fwd(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -
                              MASK[mask], float(delta), float(tau), ctypes.byref(stats))
     _check(code)
     return out, lse, mask_bytes, counters
+
+
+def kv_prepare(k, v, workspace, *, pv="fp16", qk="exact", stream=None):
+    """The key/value half of the pre-pass into ``workspace`` (a K/V cache in
+    the attention's own formats): later lamp_attn_fwd calls with the same k,
+    v, workspace and modes and ``kv_prepared=True`` skip it (any number of
+    query heads that is a multiple of k's)."""
+    lib = load()
+    sh = make_shapes(k, k, v, k, workspace=workspace, stream=stream, pv=pv, qk=qk)
+    _check(lib.lamp_kv_prepare(k.data_ptr(), v.data_ptr(), ctypes.byref(sh)))
 
 
 def host_buffer_bytes(q, k, v, out=None, **kw) -> int:

@@ -88,15 +88,16 @@ def test_workspace_bytes(lib):
 
 def test_shapes_struct_matches_the_header():
     """The ctypes mirror ends with the same fields as the C struct, at the
-    offsets the C layout gives them (pv_mode and qk_accum after the three
-    event handles)."""
-    assert [f[0] for f in lamp.LampShapes._fields_[-2:]] == ["pv_mode", "qk_accum"]
+    offsets the C layout gives them (pv_mode, qk_accum and kv_prepared after
+    the three event handles)."""
+    assert [f[0] for f in lamp.LampShapes._fields_[-3:]] == ["pv_mode", "qk_accum", "kv_prepared"]
     assert lamp.LampShapes.pv_mode.offset == lamp.LampShapes.stage_events.offset + 3 * ctypes.sizeof(ctypes.c_void_p)
     assert lamp.LampShapes.qk_accum.offset == lamp.LampShapes.pv_mode.offset + 4
+    assert lamp.LampShapes.kv_prepared.offset == lamp.LampShapes.qk_accum.offset + 4
     src = open(os.path.join(ROOT, "include", "lamp_attn.h")).read()
     body = src[src.index("typedef struct {\n  int32_t batch"):src.index("} lamp_shapes;")]
     fields = [ln.strip() for ln in body.splitlines() if ln.strip().startswith(("int32_t", "void*", "size_t"))]
-    assert fields[-2].startswith("int32_t pv_mode;") and fields[-1].startswith("int32_t qk_accum;")
+    assert [f.split()[1].rstrip(";") for f in fields[-3:]] == ["pv_mode", "qk_accum", "kv_prepared"]
 
 
 def _call(lib, sh, ptrs=(16, 32, 48, 64), mask=1, delta=2 ** -8, tau=0.5):
@@ -132,6 +133,17 @@ def test_argument_errors_before_launch(lib):
     sh = _shapes()
     sh.qk_accum, sh.pv_mode = 1, 1  # one optional mode at a time
     assert _call(lib, sh) == lamp.LAMP_ERR_UNSUPPORTED
+    sh = _shapes()
+    sh.kv_prepared = 1  # prepared keys live in a caller workspace: none given
+    assert _call(lib, sh) == lamp.LAMP_ERR_INVALID_ARG
+    st = lamp.LampStats()
+    assert lib.lamp_attn_fwd_noalloc(16, 32, 48, 64, None, ctypes.byref(sh), 1, 2 ** -8, 0.5,
+                                     ctypes.byref(st)) == lamp.LAMP_ERR_INVALID_ARG
+    assert lib.lamp_attn_fwd_host(16, 32, 48, 64, None, ctypes.byref(sh), 1, 2 ** -8, 0.5, ctypes.byref(st),
+                                  None, 0) == lamp.LAMP_ERR_INVALID_ARG
+    # lamp_kv_prepare: a workspace is required
+    assert lib.lamp_kv_prepare(32, 48, ctypes.byref(_shapes())) == lamp.LAMP_ERR_INVALID_ARG
+    assert lib.lamp_kv_prepare(None, 48, ctypes.byref(_shapes())) == lamp.LAMP_ERR_INVALID_ARG
 
 
 def test_no_device_is_an_error_not_a_fallback(lib):
