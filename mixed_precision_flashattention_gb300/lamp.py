@@ -246,12 +246,13 @@ def lamp_attn_fwd_host(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0
 
 
 def lamp_tau_sweep(q, k, taus, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -8, records=None,
-                   counters=None, stream=None):
+                   counters=None, stream=None, workspace=None, kv_prepared=False):
     """Histograms of 16-bit sub-blocks per tile for up to 8 tau values from
     one pass.  q [B, N, Hq, d], k [B, N, Hkv, d] CUDA tensors.  Returns
     (hist [ntau, 4] int64 CUDA tensor: visited tiles, tiles with 0 / 1 / 2+
     flagged sub-blocks; records [B, Hq, T, T] int32 CUDA tensor of the tile
-    records).  Asynchronous on ``stream``."""
+    records).  Asynchronous on ``stream``.  ``workspace`` / ``kv_prepared``: as
+    for lamp_attn_fwd (keys prepared by kv_prepare, whose v is then unused)."""
     lib = load()
     if not (q.is_cuda and k.is_cuda):
         raise LampError("q, k must be CUDA tensors")
@@ -263,7 +264,8 @@ def lamp_tau_sweep(q, k, taus, *, mask="causal", window=0, scale=0.0, delta=2.0 
     if records is None:
         records = torch.empty((B, Hq, T, T), dtype=torch.int32, device=q.device)
     hist = torch.zeros((max(1, len(taus)), 4), dtype=torch.int64, device=q.device)
-    sh = make_shapes(q, k, k, q, window=window, scale=scale, stream=stream)
+    sh = make_shapes(q, k, k, q, window=window, scale=scale, stream=stream, workspace=workspace,
+                     kv_prepared=kv_prepared)
     stats = LampStats()
     stats.mask = None
     stats.counters = counters.data_ptr() if counters is not None else None

@@ -88,3 +88,17 @@ def test_prepared_call_launches_no_pre_pass():
         torch.cuda.synchronize()
         times.append(ev[0].elapsed_time(ev[1]))
     assert min(times) < 0.02  # ms: no kernel between the first two events
+
+
+def test_prepared_keys_serve_the_tau_sweep():
+    """The tau-sweep pass reads the prepared 8-bit keys and their norms:
+    the same records and histograms as a sweep that prepares them."""
+    q, k, v = synth.gen_outlier_sink(1, 320, 4, 2, 128, seed=74)
+    qd, kd, vd = to_device(q, k, v, "bf16")
+    taus = [2.0 ** -i for i in range(6)]
+    h_ref, r_ref = lamp.lamp_tau_sweep(qd, kd, taus)
+    ws = torch.empty(lamp.workspace_bytes(qd, kd, vd), dtype=torch.uint8, device="cuda")
+    lamp.kv_prepare(kd, vd, ws)
+    h, r = lamp.lamp_tau_sweep(qd, kd, taus, workspace=ws, kv_prepared=True)
+    torch.cuda.synchronize()
+    assert torch.equal(h.cpu(), h_ref.cpu()) and torch.equal(r.cpu(), r_ref.cpu())
