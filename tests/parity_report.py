@@ -34,13 +34,16 @@ from mixed_precision_flashattention_gb300 import synth  # noqa: E402
 from tests import sampled_parity as sp  # noqa: E402
 
 TAUS = [2.0 ** -i for i in range(6)]
-RUNS = (  # (workload, tau, delta)
+RUNS = (  # (workload, tau, delta[, P.V mode, 8-bit accumulation])
     [("tiny", 0.5, 2.0 ** -8)]
     + [("qwen3_8b", t, 2.0 ** -8) for t in TAUS]
     + [("gemma3_12b", 0.5, 2.0 ** -8), ("gemma3_12b", 0.5, 2.0 ** -4),
        ("gemma3_12b_sw1024", 0.5, 2.0 ** -8), ("gemma3_12b_sw1024", 0.5, 2.0 ** -4)]
     + [("qwen3_32b", 0.5, 2.0 ** -8), ("qwen3_32b", 0.5, 0.0)]
     + [("gemma3_27b_stress", t, 2.0 ** -8) for t in TAUS]
+    # the optional modes against the oracle's own modes
+    + [("tiny", 0.5, 2.0 ** -8, "fp8", "exact"), ("tiny", 0.5, 2.0 ** -8, "fp16", "chunk32"),
+       ("qwen3_8b", 0.5, 2.0 ** -8, "fp8", "exact"), ("qwen3_8b", 0.5, 2.0 ** -8, "fp16", "chunk32")]
 )
 
 
@@ -69,7 +72,9 @@ def main():
     rows = []
     ok_all = True
     made = {}
-    for wname, tau, delta in runs:
+    for run in runs:
+        wname, tau, delta = run[:3]
+        pv, qk = run[3:] if len(run) > 3 else ("fp16", "exact")
         w = synth.WORKLOADS[wname]
         if wname not in made:
             made.clear()
@@ -82,7 +87,7 @@ def main():
         mb, cnt = lamp.new_stats(B, Hq, N)
         t0 = time.time()
         out, lse, _, _ = lamp.lamp_attn_fwd(qd, kd, vd, mask=w.mask, window=w.window, delta=delta, tau=tau,
-                                            mask_bytes=mb, counters=cnt)
+                                            mask_bytes=mb, counters=cnt, pv=pv, qk=qk)
         torch.cuda.synchronize()
         c = cnt.cpu().numpy()
         if c[9] != 0:
@@ -94,14 +99,16 @@ def main():
         n_tiles = B * Hq * T if wname == "tiny" else args.tiles
         tiles = sp.sample_tiles(B, Hq, N, n_tiles, seed=7)
         tasks, keys = sp.make_tasks(q, k, v, tiles, bf16=w.dtype == "bf16", heads_q=Hq, heads_kv=w.heads_kv,
-                                    mask=w.mask, window=w.window, delta=delta, tau=tau, out_dtype=w.dtype)
+                                    mask=w.mask, window=w.window, delta=delta, tau=tau, out_dtype=w.dtype,
+                                    pv=pv, qk=qk)
         res = pool.map(sp.oracle_task, tasks)
         par = sp.compare(res, keys, out_h, lse_h, mask_h, w.dtype, N, w.mask, w.window)
         ok = par["mask_bitexact"] and par["hist_bitexact_on_sample"] and par["out_within_tol"] and \
             par["lse_within_tol"]
         ok_all &= ok
-        rows.append((wname, tau, delta, par, c, ok, time.time() - t0))
-        print(f"{wname} tau={tau} delta={delta}: {'ok' if ok else 'FAIL'} {par}", flush=True)
+        mode = "default" if (pv, qk) == ("fp16", "exact") else ("FP8 P.V" if pv == "fp8" else "chunked")
+        rows.append((wname, mode, tau, delta, par, c, ok, time.time() - t0))
+        print(f"{wname} {mode} tau={tau} delta={delta}: {'ok' if ok else 'FAIL'} {par}", flush=True)
         del out, lse, mb, cnt
         torch.cuda.empty_cache()
     pool.close()
@@ -117,20 +124,22 @@ def main():
         "query tile.  Bounds (asserted): out 2e-3 + half a bf16 ulp, LSE 1e-3 against",
         "the oracle.  The FP64 columns are reported, not bounded: the 8-bit logits are",
         "by design further than 2e-3 from FP64 attention (forced-16-bit runs are",
-        "bounded against FP64 in `tests/test_gpu_parity.py`).",
+        "bounded against FP64 in `tests/test_gpu_parity.py`).  The optional modes",
+        "(FP8 P.V, chunked 8-bit accumulation) are checked against the oracle's",
+        "same modes.",
         "",
         "Command: `python tests/parity_report.py --tiles "
         f"{args.tiles}`" + (f" `--only {args.only}`" if args.only else ""),
         "",
-        "| workload | tau | delta | sampled tiles | mask bytes bit-exact | histogram (sample) equal "
+        "| workload | mode | tau | delta | sampled tiles | mask bytes bit-exact | histogram (sample) equal "
         "| out err vs oracle | LSE err vs oracle | out err vs FP64 | LSE err vs FP64 | full-size 0/1/2+ tiles "
         "| flagged sub-blocks | pass |",
-        "|---|---|---|---|---|---|---|---|---|---|---|---|---|",
+        "|---|---|---|---|---|---|---|---|---|---|---|---|---|---|",
     ]
-    for wname, tau, delta, par, c, ok, _ in rows:
+    for wname, mode, tau, delta, par, c, ok, _ in rows:
         tiles = max(1, int(c[0]))
         lines.append(
-            f"| {wname} | {_fmt_pow2(tau)} | {_fmt_pow2(delta)} | {par['tiles']} | "
+            f"| {wname} | {mode} | {_fmt_pow2(tau)} | {_fmt_pow2(delta)} | {par['tiles']} | "
             f"{'yes' if par['mask_bitexact'] else 'NO'} ({par['mask_bytes_checked']}) | "
             f"{'yes' if par['hist_bitexact_on_sample'] else 'NO'} {par['hist_on_sample']} | "
             f"{par['out_err_vs_oracle']:.2e} | {par['lse_err_vs_oracle']:.2e} | "
