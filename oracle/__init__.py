@@ -17,4 +17,5 @@ flags in tau and delta, closed forms, and a hand-derived detector example
 """
 from .formats import bf16_round, f16_round, e4m3_decode, e4m3_encode, e4m3_round, exp8, half_ulp_e4m3  # noqa: F401
 from .lamp_oracle import LampResult, lamp_forward  # noqa: F401
+from .projection import qkv_projection  # noqa: F401
 from .reference_attn import bf16_attention, fp64_attention, fp64_attention_rows, lamp8_rowloop  # noqa: F401

@@ -363,3 +363,25 @@ def test_fp64_attention_rows_equals_full():
         o, l = oracle.fp64_attention_rows(q, k, v, rows, b=1, h=3, mask=mask, window=window)
         assert np.allclose(o, out[1, rows, 3], atol=1e-13, rtol=0)
         assert np.allclose(l, lse[1, 3, rows], atol=1e-13, rtol=0)
+
+
+def test_qkv_projection_against_a_scalar_loop():
+    """Reading R16 (the projection upstream of the attention): the exact
+    products of small integers summed by a Python loop, one BF16 rounding,
+    columns split query heads / key heads / value heads."""
+    rng = np.random.default_rng(17)
+    B, N, Hq, Hkv, d, hidden = 2, 3, 2, 1, 4, 5
+    x = rng.integers(-40, 40, size=(B * N, hidden)).astype(np.float64)
+    w = rng.integers(-40, 40, size=((Hq + 2 * Hkv) * d, hidden)).astype(np.float64)
+    q, k, v = oracle.qkv_projection(x, w, batch=B, heads_q=Hq, heads_kv=Hkv, head_dim=d)
+    for t in range(B * N):
+        b, n = divmod(t, N)
+        for col in range((Hq + 2 * Hkv) * d):
+            exact = sum(int(x[t, i]) * int(w[col, i]) for i in range(hidden))
+            want = float(F.bf16_round(float(exact)))
+            h, e = divmod(col, d)
+            got = q[b, n, h, e] if h < Hq else (k[b, n, h - Hq, e] if h < Hq + Hkv else v[b, n, h - Hq - Hkv, e])
+            assert got == want, (t, col)
+    # 257 = 1 0000 0001b needs 9 significant bits: BF16 keeps 8 and the tie
+    # goes to the even neighbour, 256
+    assert float(F.bf16_round(257.0)) == 256.0 and float(F.bf16_round(259.0)) == 260.0
