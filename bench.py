@@ -237,6 +237,60 @@ def _peaks():
     return 1900.0, 1700.0, "fallback"
 
 
+def qkv_fusion_leg(args, w, lamp, torch, dev, flush, bf16_peak):
+    """The QKV projection upstream of the attention, two ways, each step from
+    the layer input x [B N, hidden] (seeded, synthetic) to out: (a) cuBLAS
+    (torch.matmul) writes y = x W^T, q / k / v are strided views of y, and
+    the attention runs with its pre-pass; (b) lamp_qkv_project writes q, k,
+    v and the K/V cache, and the attention runs on the cache."""
+    hidden = args.qkv_fusion
+    B, N, Hq, Hkv, d = w.batch, w.seqlen, w.heads_q, w.heads_kv, w.head_dim
+    g = torch.Generator(device=dev).manual_seed(args.seed + 11)
+    x = (torch.randn(B * N, hidden, device=dev, generator=g) * 0.5).to(torch.bfloat16)
+    wt = (torch.randn((Hq + 2 * Hkv) * d, hidden, device=dev, generator=g) / hidden ** 0.5).to(torch.bfloat16)
+    probe = torch.empty((B, N, Hq, d), device=dev, dtype=torch.bfloat16)
+    kp = torch.empty((B, N, Hkv, d), device=dev, dtype=torch.bfloat16)
+    ws = torch.empty(lamp.workspace_bytes(probe, kp, kp), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(probe)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+
+    def unfused():
+        y = torch.matmul(x, wt.t()).view(B, N, Hq + 2 * Hkv, d)
+        lamp.lamp_attn_fwd(y[:, :, :Hq], y[:, :, Hq:Hq + Hkv], y[:, :, Hq + Hkv:], mask=w.mask, window=w.window,
+                           delta=args.delta, tau=args.tau, out=out, lse=lse, workspace=ws)
+
+    def fused():
+        q, k, v = lamp.qkv_project(x, wt, batch=B, heads_q=Hq, heads_kv=Hkv, head_dim=d, workspace=ws)
+        lamp.lamp_attn_fwd(q, k, v, mask=w.mask, window=w.window, delta=args.delta, tau=args.tau, out=out,
+                           lse=lse, workspace=ws, kv_prepared=True)
+
+    def proj_only_cublas():
+        torch.matmul(x, wt.t())
+
+    def proj_only_fused():
+        lamp.qkv_project(x, wt, batch=B, heads_q=Hq, heads_kv=Hkv, head_dim=d, workspace=ws)
+
+    def timed(fn, n=10):
+        ts = []
+        for i in range(n + 3):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    proj_flop = 2.0 * B * N * hidden * (Hq + 2 * Hkv) * d
+    t_pc, t_pf = timed(proj_only_cublas), timed(proj_only_fused)
+    return {"hidden": hidden, "ms_cublas_prepass_attention": timed(unfused), "ms_fused_projection_attention": timed(fused),
+            "ms_projection_cublas": t_pc, "ms_projection_fused": t_pf,
+            "projection_tflops_cublas": proj_flop / t_pc / 1e9, "projection_tflops_fused": proj_flop / t_pf / 1e9,
+            "projection_fused_frac_of_bf16_peak": proj_flop / t_pf / 1e9 / bf16_peak}
+
+
 def reduce_over_ranks(ms: float, counters, world: int, device=None):
     """Whole-job figures of a multi-rank run: the slowest rank's step time
     and the counters summed over ranks (every rank holds its own shard).
@@ -270,6 +324,10 @@ def main():
                     help="input generator in place of the workload's own (same shape)")
     ap.add_argument("--pv", default="fp16", choices=["fp16", "fp8"],
                     help="P.V precision of unflagged sub-blocks (fp8: the optional FP8 P.V mode)")
+    ap.add_argument("--qkv-fusion", type=int, default=0, metavar="HIDDEN",
+                    help="also time the QKV projection upstream of the attention (hidden size HIDDEN, bf16): "
+                         "cuBLAS GEMM + pre-pass + attention against lamp_qkv_project + attention on its "
+                         "K/V cache (an extra 'qkv_fusion' object)")
     ap.add_argument("--kv-prepared", action="store_true",
                     help="keys and values prepared once (lamp_kv_prepare) before the timed steps: "
                          "each step is the forward call on the prepared K/V cache")
@@ -504,6 +562,8 @@ def main():
                          (2 if args.kv_prepared else (3 if args.pv == "fp8" else 2))) * K * world,
         "clocks": clocks,
     }
+    if args.qkv_fusion and w.dtype == "bf16":
+        res["qkv_fusion"] = qkv_fusion_leg(args, w, lamp, torch, dev, flush, bf16_peak)
     if want_cpu:
         tasks, sflops = cpu_sample_tasks(w, q, k, v, args.delta, args.tau, args.cpu_seconds, ncores, pv=args.pv,
                                          qk=args.qk)

@@ -207,6 +207,34 @@ int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out,
  */
 int lamp_kv_prepare(const void* k, const void* v, const lamp_shapes* shapes);
 
+/*
+ * lamp_qkv_project: the QKV projection upstream of the attention, with the
+ * attention's key/value cache written by its epilogue.  y = x W^T (BF16
+ * operands, FP32 tensor-core accumulation, one rounding to BF16), its
+ * columns split into q, k and v; for the key and value columns it also
+ * writes what lamp_kv_prepare writes (the E4M3 copy of k, the fp16 copy of
+ * v and the key-tile norms) into shapes->workspace, so that lamp_attn_fwd
+ * on these q, k, v with shapes->kv_prepared = 1 and the same workspace runs
+ * without a pre-pass.
+ *   x        DEVICE bf16 [batch * seqlen, hidden], row-major (token-major).
+ *   w        DEVICE bf16 [(heads_q + 2 heads_kv) * head_dim, hidden],
+ *            row-major: the query heads' rows, then the key heads', then
+ *            the value heads' (the layout of a linear layer's weight).
+ *   hidden   a multiple of 64.
+ *   q, k, v  DEVICE bf16 outputs, dense BSHD: q [B, N, Hq, d], k and v
+ *            [B, N, Hkv, d].
+ *   shapes   batch, seqlen, heads_q, heads_kv, head_dim; in_dtype bf16;
+ *            q/k/v strides, if non-zero, must be the dense ones; workspace
+ *            given (>= lamp_attn_workspace_bytes()); pv_mode FP16 or FP8
+ *            (FP8: the transposed E4M3 copy of v is written too).
+ *   stats    optional: counters[LAMP_CNT_STATUS] receives the device status.
+ * Asynchronous on shapes->stream.  Errors as lamp_attn_fwd
+ * (LAMP_ERR_INVALID_ARG for a missing workspace, an fp32 in_dtype, a hidden
+ * size that is not a positive multiple of 64, or non-dense strides).
+ */
+int lamp_qkv_project(const void* x, const void* w, int hidden, void* q, void* k, void* v,
+                     const lamp_shapes* shapes, lamp_stats* stats);
+
 /* Bytes of device workspace lamp_attn_fwd needs for these shapes (E4M3
  * copies of q and k, an fp16 copy of v, bf16 copies of fp32 inputs,
  * per-row norms and, for LAMP_PV_FP8, an E4M3 copy of v).  0 on invalid

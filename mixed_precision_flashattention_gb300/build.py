@@ -11,7 +11,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "liblamp_attn.so")
-SOURCES = ["lamp_api.cu", "lamp_prep.cu", "lamp_fwd.cu", "lamp_selftest.cu", "lamp_noalloc.cu", "lamp_host.cu"]
+SOURCES = ["lamp_api.cu", "lamp_prep.cu", "lamp_fwd.cu", "lamp_selftest.cu", "lamp_noalloc.cu", "lamp_host.cu",
+           "lamp_qkv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

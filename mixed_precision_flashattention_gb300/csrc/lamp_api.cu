@@ -17,6 +17,7 @@ cudaError_t launch_prep(const PrepParams& p, int d, cudaStream_t st);
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t st, bool sweep, int opt);
 cudaError_t launch_v8t(const void* v, const int64_t* vs, bool in_f32, uint8_t* v8t, int B, int N, int Hkv, int D,
                        cudaStream_t st);
+cudaError_t launch_qkv(const QkvParams& p, cudaStream_t st);
 cudaError_t launch_sweep_hist(const uint32_t* rec, long long n, const SweepCodes& tcode, int ntau,
                               unsigned long long* hist, cudaStream_t st);
 
@@ -371,10 +372,73 @@ int kv_prepare(const void* k, const void* v, const lamp_shapes* shapes) {
   return LAMP_OK;
 }
 
+// The QKV projection with the K/V cache in its epilogue (see lamp_qkv_project).
+int qkv_project(const void* x, const void* w, int hidden, void* q, void* k, void* v, const lamp_shapes* shapes,
+                lamp_stats* stats) {
+  if (!x || !w || !q || !k || !v || !shapes_ok(shapes)) return LAMP_ERR_INVALID_ARG;
+  const lamp_shapes& s = *shapes;
+  const int D = s.head_dim;
+  if (D != 64 && D != 128 && D != 256) return LAMP_ERR_UNSUPPORTED;
+  const bool pv8 = s.pv_mode == LAMP_PV_FP8;
+  if ((pv8 || s.qk_accum == LAMP_QK_CHUNK32) && D == 256) return LAMP_ERR_UNSUPPORTED;
+  if (pv8 && s.qk_accum == LAMP_QK_CHUNK32) return LAMP_ERR_UNSUPPORTED;
+  if (s.in_dtype != LAMP_DT_BF16 || hidden < 64 || hidden % 64) return LAMP_ERR_INVALID_ARG;
+  const int B = s.batch, N = s.seqlen, Hq = s.heads_q, Hkv = s.heads_kv;
+  // outputs are dense BSHD: strides either not given (0) or the dense ones
+  auto dense = [&](const int64_t* st, int H) {
+    return (st[0] == 0 && st[1] == 0 && st[2] == 0) ||
+           (st[0] == (int64_t)N * H * D && st[1] == (int64_t)H * D && st[2] == D);
+  };
+  if (!dense(s.q_stride, Hq) || !dense(s.k_stride, Hkv) || !dense(s.v_stride, Hkv)) return LAMP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return LAMP_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(s);
+  uint8_t* ws = (uint8_t*)s.workspace;
+  if (!ws) return LAMP_ERR_INVALID_ARG;
+  if (s.workspace_bytes < wl.total || !aligned16(ws)) return LAMP_ERR_WORKSPACE;
+  int st = device_check();
+  if (st != LAMP_OK) return st;
+  cudaStream_t stream = (cudaStream_t)s.stream;
+  const long long T = (long long)B * N, ncols = (long long)(Hq + 2 * Hkv) * D;
+  if (T >= (1LL << 31) || ncols >= (1LL << 31)) return LAMP_ERR_INVALID_ARG;
+  QkvParams p;
+  memset(&p, 0, sizeof(p));
+  bool ok = true;
+  // x and W as 4-D maps (hidden, rows, 1, 1): 64-element K blocks of 128 x rows / 256 W rows
+  ok &= make_map(&p.tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, hidden, (int)T, 1, 1, hidden, T * hidden, T * hidden,
+                 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok &= make_map(&p.tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, hidden, (int)ncols, 1, 1, hidden, ncols * hidden,
+                 ncols * hidden, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return LAMP_ERR_CUDA;
+  p.q = (uint16_t*)q; p.k = (uint16_t*)k; p.v = (uint16_t*)v;
+  p.k8 = ws + wl.k8; p.v16 = (uint16_t*)(ws + wl.v16);
+  p.nk = (float*)(ws + wl.nk); p.nkc = (float*)(ws + wl.nkc);
+  p.abort = (unsigned int*)(ws + wl.abort);
+  p.counters = stats ? (unsigned long long*)stats->counters : nullptr;
+  p.timeout_ns = kTimeoutNs;
+  if (const char* e = getenv("LAMP_WAIT_TIMEOUT_NS")) p.timeout_ns = strtoull(e, nullptr, 10);
+  p.B = B; p.N = N; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.T = (int)T; p.hidden = hidden; p.ncols = (int)ncols;
+  if (stats && stats->counters &&
+      cudaMemsetAsync(stats->counters, 0, LAMP_NUM_COUNTERS * sizeof(uint64_t), stream) != cudaSuccess)
+    return LAMP_ERR_CUDA;
+  // the key-tile norms (atomic maxima) and the abort word start at 0
+  if (cudaMemsetAsync(ws + wl.nk, 0, wl.abort + 4 - wl.nk, stream) != cudaSuccess) return LAMP_ERR_CUDA;
+  if (launch_qkv(p, stream) != cudaSuccess) return LAMP_ERR_CUDA;
+  if (pv8) {
+    const int64_t vs[3] = {(int64_t)N * Hkv * D, (int64_t)Hkv * D, D};
+    if (launch_v8t(v, vs, false, ws + wl.v8t, B, N, Hkv, D, stream) != cudaSuccess) return LAMP_ERR_CUDA;
+  }
+  return LAMP_OK;
+}
+
 }  // namespace
 }  // namespace lamp
 
 extern "C" {
+
+int lamp_qkv_project(const void* x, const void* w, int hidden, void* q, void* k, void* v, const lamp_shapes* shapes,
+                     lamp_stats* stats) {
+  return qkv_project(x, w, hidden, q, k, v, shapes, stats);
+}
 
 int lamp_kv_prepare(const void* k, const void* v, const lamp_shapes* shapes) { return kv_prepare(k, v, shapes); }
 

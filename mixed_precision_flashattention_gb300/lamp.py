@@ -26,7 +26,8 @@ NUM_COUNTERS = 16
 COUNTER_NAMES = ["tiles", "hist0", "hist1", "hist2p", "strips", "stage1", "flagged",
                  "s8_saturated", "fixups", "status", "recompute_steps", "spec_waste", "recompute_late",
                  "guard_resolved", "fixups_max"]
-EXPORTS = ["lamp_attn_fwd", "lamp_attn_fwd_noalloc", "lamp_kv_prepare", "lamp_attn_workspace_bytes", "lamp_strerror",
+EXPORTS = ["lamp_attn_fwd", "lamp_attn_fwd_noalloc", "lamp_kv_prepare", "lamp_qkv_project", "lamp_attn_workspace_bytes",
+           "lamp_strerror",
            "lamp_version", "lamp_exp8_table", "lamp_selftest", "lamp_attn_fwd_host",
            "lamp_attn_host_buffer_bytes", "lamp_attn_tau_sweep"]
 
@@ -77,6 +78,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         ctypes.POINTER(LampStats)]
     lib.lamp_attn_fwd_noalloc.restype = ctypes.c_int
     lib.lamp_attn_fwd_noalloc.argtypes = lib.lamp_attn_fwd.argtypes
+    lib.lamp_qkv_project.restype = ctypes.c_int
+    lib.lamp_qkv_project.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p, ctypes.POINTER(LampShapes), ctypes.POINTER(LampStats)]
     lib.lamp_kv_prepare.restype = ctypes.c_int
     lib.lamp_kv_prepare.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(LampShapes)]
     lib.lamp_attn_workspace_bytes.restype = ctypes.c_size_t
@@ -182,6 +186,30 @@ def kv_prepare(k, v, workspace, *, pv="fp16", qk="exact", stream=None):
     lib = load()
     sh = make_shapes(k, k, v, k, workspace=workspace, stream=stream, pv=pv, qk=qk)
     _check(lib.lamp_kv_prepare(k.data_ptr(), v.data_ptr(), ctypes.byref(sh)))
+
+
+def qkv_project(x, w, *, batch, heads_q, heads_kv, head_dim, workspace, pv="fp16", counters=None, stream=None):
+    """The QKV projection with the attention's K/V cache in its epilogue:
+    x [batch * N, hidden] and w [(heads_q + 2 heads_kv) head_dim, hidden]
+    bf16 CUDA tensors.  Returns dense q [B, N, Hq, d], k and v [B, N, Hkv, d]
+    (bf16); ``workspace`` then holds their prepared keys and values, for
+    lamp_attn_fwd(..., workspace=workspace, kv_prepared=True)."""
+    lib = load()
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16 or not (x.is_cuda and w.is_cuda):
+        raise LampError("x and w must be bf16 CUDA tensors")
+    tokens, hidden = x.shape
+    n = tokens // batch
+    dev = x.device
+    q = torch.empty((batch, n, heads_q, head_dim), device=dev, dtype=torch.bfloat16)
+    k = torch.empty((batch, n, heads_kv, head_dim), device=dev, dtype=torch.bfloat16)
+    v = torch.empty_like(k)
+    sh = make_shapes(q, k, v, q, workspace=workspace, stream=stream, pv=pv)
+    stats = LampStats()
+    stats.mask = None
+    stats.counters = counters.data_ptr() if counters is not None else None
+    _check(lib.lamp_qkv_project(x.data_ptr(), w.data_ptr(), int(hidden), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                ctypes.byref(sh), ctypes.byref(stats)))
+    return q, k, v
 
 
 def host_buffer_bytes(q, k, v, out=None, **kw) -> int:
