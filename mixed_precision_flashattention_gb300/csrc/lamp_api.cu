@@ -11,6 +11,7 @@
 
 #include "../../include/lamp_attn.h"
 #include "lamp_common.cuh"
+#include "lamp_qkv.cuh"
 
 namespace lamp {
 cudaError_t launch_prep(const PrepParams& p, int d, cudaStream_t st);

@@ -69,22 +69,6 @@ struct PrepParams {
   int shr_hq, shr_hkv, shr_n;
 };
 
-// QKV projection parameters (see lamp_qkv.cu).
-struct QkvParams {
-  CUtensorMap tmX, tmW;          // x [T, hidden], W [ncols, hidden]: BF16, K-major
-  uint16_t* q;                   // [B, N, Hq, D]  BF16
-  uint16_t* k;                   // [B, N, Hkv, D] BF16
-  uint16_t* v;                   // [B, N, Hkv, D] BF16
-  uint8_t* k8;                   // workspace [B, Hkv, N, D] E4M3
-  uint16_t* v16;                 // workspace [B, Hkv, N, D] fp16
-  float* nk;                     // workspace [B, Hkv, T_k] (zeroed before the launch)
-  float* nkc;                    // workspace [B, Hkv, T_k, D/32] (zeroed before the launch)
-  unsigned int* abort;           // grid abort word (zeroed before the launch)
-  unsigned long long* counters;  // optional: status slot 9 on a timed-out wait
-  unsigned long long timeout_ns;
-  int B, N, Hq, Hkv, D, T, hidden, ncols;  // T = B N tokens, ncols = (Hq + 2 Hkv) D
-};
-
 // Byte offset of byte `x` (0 <= x < row_bytes) of row `r` in a K-major
 // tile whose rows are `row_bytes` long, stored as 128-byte (or 64-byte when
 // row_bytes == 64) swizzled atoms: 8 rows per atom, atoms stacked along the

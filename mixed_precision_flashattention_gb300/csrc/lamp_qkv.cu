@@ -24,6 +24,7 @@
 #include <cstdint>
 
 #include "lamp_common.cuh"
+#include "lamp_qkv.cuh"
 
 namespace lamp {
 
