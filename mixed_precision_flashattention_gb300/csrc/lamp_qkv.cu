@@ -10,11 +10,13 @@
 // attention's pre-pass (lamp_prep.cu) writes, so the attention call that
 // follows runs with kv_prepared = 1 and no pre-pass.
 //
-// One CTA per 128-token x 256-column tile (two heads at d = 128): a TMA
-// producer warp fills a ring of 4 stages of 64-element K blocks (x 16 KB,
-// W 32 KB, 128-byte swizzle), one thread of the MMA warp issues four
-// 128 x 256 x 16 kind::f16 MMAs per block into a 256-column TMEM
-// accumulator, and four epilogue warps read it back, one token row per
+// Tiles of 128 tokens x 256 columns (two heads at d = 128), the column
+// tiles of a token tile one after the other, over a persistent grid of one
+// CTA per SM: a TMA producer warp fills a ring of 4 stages of 64-element K
+// blocks (x 16 KB, W 32 KB, 128-byte swizzle), one thread of the MMA warp
+// issues four 128 x 256 x 16 kind::f16 MMAs per block into one of two
+// 256-column TMEM accumulators (a tile's epilogue overlaps the next tile's
+// main loop), and four epilogue warps read them back, one token row per
 // thread.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -69,10 +71,17 @@ __global__ void __launch_bounds__(kQThreads, 1) lamp_qkv_kernel(const __grid_con
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t full = sbase + kQBar, empty = full + 8 * kQST, accf = empty + 8 * kQST;
-  uint32_t* tslot = (uint32_t*)(smem + kQBar + 8 * (2 * kQST + 1));
+  // barriers: full / empty per stage, and per accumulator: full (MMA ->
+  // epilogue) and empty (epilogue -> MMA)
+  const uint32_t full = sbase + kQBar, empty = full + 8 * kQST, accf = empty + 8 * kQST, acce = accf + 16;
+  uint32_t* tslot = (uint32_t*)(smem + kQBar + 8 * (2 * kQST + 4));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kQBM, n0 = blockIdx.y * kQBN;
+  // Persistent: CTA c takes tiles c, c + grid, ...  Tile id -> (token tile,
+  // column tile) with the column tiles of a token tile consecutive, so the
+  // tiles in flight share a few x tiles and all of W, which stay in L2
+  // (with the token tiles fastest, every column tile re-read x from DRAM).
+  const int ntn = (p.ncols + kQBN - 1) / kQBN;
+  const int ntiles = ((p.T + kQBM - 1) / kQBM) * ntn;
   const int nkb = p.hidden / kQBK;
 
   if (threadIdx.x == 0) {
@@ -80,142 +89,177 @@ __global__ void __launch_bounds__(kQThreads, 1) lamp_qkv_kernel(const __grid_con
       mbar_init(full + 8 * s, 1);
       mbar_init(empty + 8 * s, 1);
     }
-    mbar_init(accf, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf + 8 * a, 1);
+      mbar_init(acce + 8 * a, 128);  // every epilogue thread, after its last load of the accumulator
+    }
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tslot), kQBN);
+  if (warp == 1) tmem_alloc(smem_u32(tslot), 2 * kQBN);  // two 256-column accumulators
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *(volatile uint32_t*)tslot;
 
   if (warp == 0) {
-    // ---- TMA producer
+    // ---- TMA producer: the K blocks of this CTA's tiles, one ring
     if (lane == 0) {
       prefetch_tmap(&p.tmX);
       prefetch_tmap(&p.tmW);
-      int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kQST, u = kb / kQST;
-        if (u > 0 && !qkv_wait(empty + 8 * s, (u - 1) & 1, p)) break;
-        const uint32_t st = sbase + s * kQStage;
-        mbar_expect_tx(full + 8 * s, kQStage);
-        tma_load_4d(st, &p.tmX, full + 8 * s, kb * kQBK, m0, 0, 0);
-        tma_load_4d(st + kQA, &p.tmW, full + 8 * s, kb * kQBK, n0, 0, 0);
-        issued = kb + 1;
+      int it = 0;  // K blocks issued so far (over all tiles)
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int m0 = (tile / ntn) * kQBM, n0 = (tile % ntn) * kQBN;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kQST, u = it / kQST;
+          if (u > 0 && !qkv_wait(empty + 8 * s, (u - 1) & 1, p)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = sbase + s * kQStage;
+          mbar_expect_tx(full + 8 * s, kQStage);
+          tma_load_4d(st, &p.tmX, full + 8 * s, kb * kQBK, m0, 0, 0);
+          tma_load_4d(st + kQA, &p.tmW, full + 8 * s, kb * kQBK, n0, 0, 0);
+        }
       }
       // after a failure, let the copies in flight land before the CTA exits
-      for (int kb = (issued > kQST ? issued - kQST : 0); kb < issued; ++kb) {
-        const int s = kb % kQST, u = kb / kQST;
-        for (int it = 0; it < 100000 && !mbar_try_wait(full + 8 * s, u & 1); ++it) {
+      for (int i = (it > kQST ? it - kQST : 0); i < it; ++i) {
+        const int s = i % kQST, u = i / kQST;
+        for (int n = 0; n < 100000 && !mbar_try_wait(full + 8 * s, u & 1); ++n) {
         }
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer: D[128 x 256] (+)= X[128 x 64] . W[256 x 64]^T per block
+    // ---- MMA issuer: D[128 x 256] (+)= X[128 x 64] . W[256 x 64]^T per block,
+    // tile lt of this CTA into accumulator lt & 1
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc(1, 1, 0, kQBM, kQBN);
       bool ok = true;
-      for (int kb = 0; kb < nkb && ok; ++kb) {
-        const int s = kb % kQST, u = kb / kQST;
-        ok = qkv_wait(full + 8 * s, u & 1, p);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t st = sbase + s * kQStage;
-#pragma unroll
-        for (int kk = 0; kk < kQBK / 16; ++kk) {
-          const uint64_t ad = make_sdesc(st + kk * 32, 16, 1024, kLayoutSW128);
-          const uint64_t bd = make_sdesc(st + kQA + kk * 32, 16, 1024, kLayoutSW128);
-          mma_f16(tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+      int it = 0, lt = 0;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++lt) {
+        const int a = lt & 1;
+        // the epilogue has read this accumulator's previous tile
+        if (lt >= 2 && !qkv_wait(acce + 8 * a, ((lt >> 1) - 1) & 1, p)) {
+          ok = false;
+          break;
         }
-        mma_commit(empty + 8 * s);
+        tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)(a * kQBN);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kQST, u = it / kQST;
+          if (!qkv_wait(full + 8 * s, u & 1, p)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = sbase + s * kQStage;
+#pragma unroll
+          for (int kk = 0; kk < kQBK / 16; ++kk) {
+            const uint64_t ad = make_sdesc(st + kk * 32, 16, 1024, kLayoutSW128);
+            const uint64_t bd = make_sdesc(st + kQA + kk * 32, 16, 1024, kLayoutSW128);
+            mma_f16(acc, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(empty + 8 * s);
+        }
+        mma_commit(accf + 8 * a);  // also after a failure: the epilogue must not wait forever
       }
-      mma_commit(accf);  // also after a failure: the epilogue must not wait forever
-      // the accumulator is released below only once these MMAs are done
-      for (int it = 0; it < 1000000 && !mbar_try_wait(accf, 0); ++it) {
+      // the accumulators are released below only once the last MMAs are done
+      if (lt > 0) {
+        const int a = (lt - 1) & 1;
+        for (int n = 0; n < 1000000 && !mbar_try_wait(accf + 8 * a, ((lt - 1) >> 1) & 1); ++n) {
+        }
       }
     }
   } else {
     // ---- epilogue: one token row per thread
     const int quad = warp & 3;  // TMEM lanes 32 quad .. (warp w reads lanes of w % 4)
     const int r = quad * 32 + lane;
-    const int t = m0 + r;
-    const bool live_row = t < p.T;
-    const int b = live_row ? t / p.N : 0, n = live_row ? t - b * p.N : 0;
     const int D = p.D, CH = D / 32, TT = (p.N + kBN - 1) / kBN;
-    bool ok = qkv_wait(accf, 0, p);
-    ok = __all_sync(0xffffffffu, ok);  // warp-uniform: TMEM loads and shuffles below
-    if (ok) tc_fence_after();
-    float ssum = 0.0f;  // sum of squares of the E4M3 key row of the current head
+    bool ok = true;
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++lt) {
+      const int a = lt & 1;
+      const int m0 = (tile / ntn) * kQBM, n0 = (tile % ntn) * kQBN;
+      const int t = m0 + r;
+      const bool live_row = t < p.T;
+      const int b = live_row ? t / p.N : 0, n = live_row ? t - b * p.N : 0;
+      ok = qkv_wait(accf + 8 * a, (lt >> 1) & 1, p);
+      ok = __all_sync(0xffffffffu, ok);  // warp-uniform: TMEM loads and shuffles below
+      if (!ok) break;
+      tc_fence_after();
+      float ssum = 0.0f;  // sum of squares of the E4M3 key row of the current head
 #pragma unroll 1
-    for (int c0 = 0; c0 < kQBN; c0 += 32) {
-      uint32_t acc[32];
-      if (ok) {
-        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + c0, acc);
+      for (int c0 = 0; c0 < kQBN; c0 += 32) {
+        uint32_t acc[32];
+        tmem_ld32(tmem + (uint32_t)(a * kQBN) + ((uint32_t)(quad * 32) << 16) + c0, acc);
         tmem_wait_ld();
-      }
-      const int col = n0 + c0;
-      if (!ok || col >= p.ncols) continue;  // warp-uniform
-      const int head = col / D, e = col - head * D;
-      // round once to BF16 (RNE): the projection's output values
-      uint32_t hb[16];
-      float vals[32];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
-        memcpy(&hb[i], &h2, 4);
-        vals[2 * i] = __low2float(h2);
-        vals[2 * i + 1] = __high2float(h2);
-      }
-      if (head < p.Hq) {
-        if (live_row) {
-          uint4* dst = reinterpret_cast<uint4*>(p.q + (((size_t)b * p.N + n) * p.Hq + head) * D + e);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
+        if (c0 + 32 == kQBN) {  // the accumulator is read: the MMA warp may reuse it
+          tc_fence_before();
+          mbar_arrive(acce + 8 * a);
         }
-      } else if (head < p.Hq + p.Hkv) {
-        const int g = head - p.Hq;
-        const size_t krow = ((size_t)b * p.Hkv + g) * p.N + n;  // row of the [B, Hkv, N, D] copies
-        uint32_t c8[8];
-        float ss = 0.0f;
+        const int col = n0 + c0;
+        if (col >= p.ncols) continue;  // warp-uniform
+        const int head = col / D, e = col - head * D;
+        // round once to BF16 (RNE): the projection's output values
+        uint32_t hb[16];
+        float vals[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint16_t c = cvt_e4m3x2(vals[2 * i + 1], vals[2 * i]);
-          const uint32_t hv = e4m3x2_to_f16x2(c);
-          __half2 h2;
-          memcpy(&h2, &hv, 4);
-          const float a0 = __low2float(h2), a1 = __high2float(h2);
-          ss = fmaf(a0, a0, fmaf(a1, a1, ss));
-          if (i & 1) c8[i >> 1] |= (uint32_t)c << 16; else c8[i >> 1] = c;
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
+          memcpy(&hb[i], &h2, 4);
+          vals[2 * i] = __low2float(h2);
+          vals[2 * i + 1] = __high2float(h2);
         }
-        if (live_row) {
-          uint4* dst = reinterpret_cast<uint4*>(p.k + (((size_t)b * p.N + n) * p.Hkv + g) * D + e);
+        if (head < p.Hq) {
+          if (live_row) {
+            uint4* dst = reinterpret_cast<uint4*>(p.q + (((size_t)b * p.N + n) * p.Hq + head) * D + e);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
-          uint4* d8 = reinterpret_cast<uint4*>(p.k8 + krow * D + e);
-          d8[0] = make_uint4(c8[0], c8[1], c8[2], c8[3]);
-          d8[1] = make_uint4(c8[4], c8[5], c8[6], c8[7]);
-        }
-        // upper bounds of the norms: the float sums of squares rounded up
-        const long long tile = ((long long)b * p.Hkv + g) * TT + n / kBN;
-        qkv_atomic_max(p.nkc, tile * CH + e / 32, sqrtf(ss) * (1.0f + 0x1p-16f) + 0x1p-6f, live_row);
-        ssum += ss;
-        if (e + 32 == D) {  // the head's last chunk: the whole row
-          qkv_atomic_max(p.nk, tile, sqrtf(ssum) * (1.0f + 0x1p-16f), live_row);
-          ssum = 0.0f;
-        }
-      } else {
-        const int g = head - p.Hq - p.Hkv;
-        if (live_row) {
-          uint4* dst = reinterpret_cast<uint4*>(p.v + (((size_t)b * p.N + n) * p.Hkv + g) * D + e);
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
+          }
+        } else if (head < p.Hq + p.Hkv) {
+          const int g = head - p.Hq;
+          const size_t krow = ((size_t)b * p.Hkv + g) * p.N + n;  // row of the [B, Hkv, N, D] copies
+          uint32_t c8[8];
+          float ss = 0.0f;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
-          uint32_t h16[16];
+          for (int i = 0; i < 16; ++i) {
+            const uint16_t c = cvt_e4m3x2(vals[2 * i + 1], vals[2 * i]);
+            const uint32_t hv = e4m3x2_to_f16x2(c);
+            __half2 h2;
+            memcpy(&h2, &hv, 4);
+            const float a0 = __low2float(h2), a1 = __high2float(h2);
+            ss = fmaf(a0, a0, fmaf(a1, a1, ss));
+            if (i & 1) c8[i >> 1] |= (uint32_t)c << 16; else c8[i >> 1] = c;
+          }
+          if (live_row) {
+            uint4* dst = reinterpret_cast<uint4*>(p.k + (((size_t)b * p.N + n) * p.Hkv + g) * D + e);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) h16[i] = cvt_f16x2_sat(vals[2 * i + 1], vals[2 * i]);
-          uint4* d16 = reinterpret_cast<uint4*>(p.v16 + (((size_t)b * p.Hkv + g) * p.N + n) * D + e);
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
+            uint4* d8 = reinterpret_cast<uint4*>(p.k8 + krow * D + e);
+            d8[0] = make_uint4(c8[0], c8[1], c8[2], c8[3]);
+            d8[1] = make_uint4(c8[4], c8[5], c8[6], c8[7]);
+          }
+          // upper bounds of the norms: the float sums of squares rounded up
+          const long long ktile = ((long long)b * p.Hkv + g) * TT + n / kBN;
+          qkv_atomic_max(p.nkc, ktile * CH + e / 32, sqrtf(ss) * (1.0f + 0x1p-16f) + 0x1p-6f, live_row);
+          ssum += ss;
+          if (e + 32 == D) {  // the head's last chunk: the whole row
+            qkv_atomic_max(p.nk, ktile, sqrtf(ssum) * (1.0f + 0x1p-16f), live_row);
+            ssum = 0.0f;
+          }
+        } else {
+          const int g = head - p.Hq - p.Hkv;
+          if (live_row) {
+            uint4* dst = reinterpret_cast<uint4*>(p.v + (((size_t)b * p.N + n) * p.Hkv + g) * D + e);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) d16[i] = make_uint4(h16[4 * i], h16[4 * i + 1], h16[4 * i + 2], h16[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
+            uint32_t h16[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) h16[i] = cvt_f16x2_sat(vals[2 * i + 1], vals[2 * i]);
+            uint4* d16 = reinterpret_cast<uint4*>(p.v16 + (((size_t)b * p.Hkv + g) * p.N + n) * D + e);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d16[i] = make_uint4(h16[4 * i], h16[4 * i + 1], h16[4 * i + 2], h16[4 * i + 3]);
+          }
         }
       }
     }
@@ -224,15 +268,21 @@ __global__ void __launch_bounds__(kQThreads, 1) lamp_qkv_kernel(const __grid_con
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kQBN);
+    tmem_dealloc(tmem, 2 * kQBN);
   }
 }
 
 cudaError_t launch_qkv(const QkvParams& p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(lamp_qkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((p.T + kQBM - 1) / kQBM), (unsigned)((p.ncols + kQBN - 1) / kQBN));
-  if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  const long long tiles = (long long)((p.T + kQBM - 1) / kQBM) * ((p.ncols + kQBN - 1) / kQBN);
+  if (tiles == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // persistent: one CTA per SM (the shared memory allows one), tiles strided over them
+  const dim3 grid((unsigned)(tiles < sms ? tiles : sms));
   lamp_qkv_kernel<<<grid, kQThreads, kQSmem, st>>>(p);
   return cudaGetLastError();
 }
