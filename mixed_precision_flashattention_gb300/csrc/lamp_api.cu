@@ -404,11 +404,11 @@ int qkv_project(const void* x, const void* w, int hidden, void* q, void* k, void
   QkvParams p;
   memset(&p, 0, sizeof(p));
   bool ok = true;
-  // x and W as 4-D maps (hidden, rows, 1, 1): 64-element K blocks of 128 x rows / 256 W rows
+  // x and W as 4-D maps (hidden, rows, 1, 1): 64-element K blocks of 128 rows (each CTA of a pair)
   ok &= make_map(&p.tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, hidden, (int)T, 1, 1, hidden, T * hidden, T * hidden,
                  64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   ok &= make_map(&p.tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, hidden, (int)ncols, 1, 1, hidden, ncols * hidden,
-                 ncols * hidden, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B);
+                 ncols * hidden, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return LAMP_ERR_CUDA;
   p.q = (uint16_t*)q; p.k = (uint16_t*)k; p.v = (uint16_t*)v;
   p.k8 = ws + wl.k8; p.v16 = (uint16_t*)(ws + wl.v16);

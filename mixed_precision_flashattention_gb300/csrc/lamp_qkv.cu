@@ -10,14 +10,18 @@
 // attention's pre-pass (lamp_prep.cu) writes, so the attention call that
 // follows runs with kv_prepared = 1 and no pre-pass.
 //
-// Tiles of 128 tokens x 256 columns (two heads at d = 128), the column
-// tiles of a token tile one after the other, over a persistent grid of one
-// CTA per SM: a TMA producer warp fills a ring of 4 stages of 64-element K
-// blocks (x 16 KB, W 32 KB, 128-byte swizzle), one thread of the MMA warp
-// issues four 128 x 256 x 16 kind::f16 MMAs per block into one of two
-// 256-column TMEM accumulators (a tile's epilogue overlaps the next tile's
-// main loop), and four epilogue warps read them back, one token row per
-// thread.  Every wait is bounded.
+// Tiles of 256 tokens x 256 columns (two heads at d = 128), the column
+// tiles of a token tile one after the other, over a persistent grid of CTA
+// pairs (clusters of two, one CTA per SM).  The pair computes a tile with
+// cta_group::2 MMAs: each CTA holds 128 token rows of x and 128 rows of W
+// per K block, so each SM streams half of the W tile it would need alone
+// (32 KB per 64-element K block instead of 48).  In each CTA a TMA producer
+// warp fills a ring of 6 stages (x 16 KB, W 16 KB, 128-byte swizzle) and
+// signals the first CTA's barrier; one thread of the first CTA issues four
+// 256 x 256 x 16 kind::f16 MMAs per block into one of two 256-column TMEM
+// accumulators (each CTA's TMEM holds its 128 rows; a tile's epilogue
+// overlaps the next tile's main loop), and four epilogue warps per CTA read
+// them back, one token row per thread.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -30,23 +34,90 @@
 
 namespace lamp {
 
-constexpr int kQBM = 128, kQBN = 256, kQBK = 64, kQST = 4;
+constexpr int kQBM = 128, kQBN = 256, kQBK = 64, kQST = 6;  // kQBM: token rows per CTA
 constexpr int kQA = kQBM * kQBK * 2;            // x stage: 16 KB
-constexpr int kQB = kQBN * kQBK * 2;            // W stage: 32 KB
+constexpr int kQB = (kQBN / 2) * kQBK * 2;      // W stage (this CTA's half): 16 KB
 constexpr int kQStage = kQA + kQB;
 constexpr int kQBar = kQST * kQStage;           // barriers after the stages
-constexpr int kQSmem = kQBar + 128 + 1024;      // + barriers, TMEM slot, alignment slack
+constexpr int kQSmem = kQBar + 256 + 1024 + kQB;  // + barriers, TMEM slot, alignment slack, a W stage of padding
 constexpr int kQThreads = 192;                  // producer, MMA, four epilogue warps
+
+// ---- the CTA-pair forms (cta_group::2) this kernel alone uses
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared-memory offset in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// TMA load into this CTA's shared memory; completion counted on `bar`, a
+// barrier of either CTA of the pair (shared::cluster address)
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(0), "r"(0), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on the barrier at shared-memory offset `bar` in both CTAs of the
+// pair once the MMAs this thread issued are done
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 
 // Bounded wait of the projection kernel: gives up after timeout_ns (status
 // word set to LAMP_ERR_TIMEOUT, 4) or when another thread of the grid gave up.
+// Barriers that the other CTA of the pair (or its copies and MMAs) signals
+// are waited on with cluster-scope acquire.
 __device__ __forceinline__ bool qkv_wait(uint32_t bar, uint32_t parity, const QkvParams& p) {
-  if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+  for (int i = 0; i < 64; ++i)
+    if (mbar_try_wait_cluster(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (;;) {
     if (*(volatile unsigned int*)p.abort) return false;
     if (globaltimer_ns() - t0 > p.timeout_ns) break;
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    __nanosleep(64);
   }
   atomicExch(p.abort, 1u);
   if (p.counters) atomicExch(&p.counters[9], 4ull);
@@ -67,49 +138,54 @@ __device__ __forceinline__ void qkv_atomic_max(float* base, long long slot, floa
   }
 }
 
-__global__ void __launch_bounds__(kQThreads, 1) lamp_qkv_kernel(const __grid_constant__ QkvParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQThreads, 1)
+    lamp_qkv_kernel(const __grid_constant__ QkvParams p) {
   extern __shared__ uint8_t smem_raw[];
+  // the same offset in both CTAs: the pair's MMAs address both with one descriptor
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   // barriers: full / empty per stage, and per accumulator: full (MMA ->
-  // epilogue) and empty (epilogue -> MMA)
+  // epilogue) and empty (epilogue -> MMA); the first CTA's full and
+  // accumulator-empty barriers serve the pair
   const uint32_t full = sbase + kQBar, empty = full + 8 * kQST, accf = empty + 8 * kQST, acce = accf + 16;
   uint32_t* tslot = (uint32_t*)(smem + kQBar + 8 * (2 * kQST + 4));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Persistent: CTA c takes tiles c, c + grid, ...  Tile id -> (token tile,
-  // column tile) with the column tiles of a token tile consecutive, so the
-  // tiles in flight share a few x tiles and all of W, which stay in L2
-  // (with the token tiles fastest, every column tile re-read x from DRAM).
+  const uint32_t rank = cluster_rank();  // 0: issues the pair's MMAs
+  // Persistent: pair c takes tiles c, c + pairs, ...  Tile id -> (token
+  // tile, column tile) with the column tiles of a token tile consecutive,
+  // so the tiles in flight share a few x tiles and all of W, which stay in L2.
+  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
   const int ntn = (p.ncols + kQBN - 1) / kQBN;
-  const int ntiles = ((p.T + kQBM - 1) / kQBM) * ntn;
+  const int ntiles = ((p.T + 2 * kQBM - 1) / (2 * kQBM)) * ntn;
   const int nkb = p.hidden / kQBK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQST; ++s) {
-      mbar_init(full + 8 * s, 1);
-      mbar_init(empty + 8 * s, 1);
+      mbar_init(full + 8 * s, 1);   // first CTA: its producer's arrival; both CTAs' bytes
+      mbar_init(empty + 8 * s, 1);  // the pair's MMA commit
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(accf + 8 * a, 1);
-      mbar_init(acce + 8 * a, 128);  // every epilogue thread, after its last load of the accumulator
+      mbar_init(accf + 8 * a, 1);  // the pair's MMA commit
+      mbar_init(acce + 8 * a, 8);  // first CTA: one lane of each epilogue warp of both CTAs
     }
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tslot), 2 * kQBN);  // two 256-column accumulators
+  if (warp == 1) tmem_alloc_pair(smem_u32(tslot), 2 * kQBN);  // two 256-column accumulators
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem = *(volatile uint32_t*)tslot;
 
   if (warp == 0) {
-    // ---- TMA producer: the K blocks of this CTA's tiles, one ring
+    // ---- TMA producer: this CTA's x rows and W half of each K block
     if (lane == 0) {
       prefetch_tmap(&p.tmX);
       prefetch_tmap(&p.tmW);
       int it = 0;  // K blocks issued so far (over all tiles)
       bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-        const int m0 = (tile / ntn) * kQBM, n0 = (tile % ntn) * kQBN;
+      for (int tile = pair; tile < ntiles && ok; tile += npairs) {
+        const int m0 = (tile / ntn) * (2 * kQBM) + (int)rank * kQBM;
+        const int n0 = (tile % ntn) * kQBN + (int)rank * (kQBN / 2);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kQST, u = it / kQST;
           if (u > 0 && !qkv_wait(empty + 8 * s, (u - 1) & 1, p)) {
@@ -117,28 +193,31 @@ __global__ void __launch_bounds__(kQThreads, 1) lamp_qkv_kernel(const __grid_con
             break;
           }
           const uint32_t st = sbase + s * kQStage;
-          mbar_expect_tx(full + 8 * s, kQStage);
-          tma_load_4d(st, &p.tmX, full + 8 * s, kb * kQBK, m0, 0, 0);
-          tma_load_4d(st + kQA, &p.tmW, full + 8 * s, kb * kQBK, n0, 0, 0);
+          const uint32_t fb = map_to_rank(full + 8 * s, 0);
+          if (rank == 0) mbar_expect_tx(full + 8 * s, 2 * kQStage);  // both CTAs' bytes
+          tma_load_4d_pair(st, &p.tmX, fb, kb * kQBK, m0);
+          tma_load_4d_pair(st + kQA, &p.tmW, fb, kb * kQBK, n0);
         }
       }
       // after a failure, let the copies in flight land before the CTA exits
-      for (int i = (it > kQST ? it - kQST : 0); i < it; ++i) {
-        const int s = i % kQST, u = i / kQST;
-        for (int n = 0; n < 100000 && !mbar_try_wait(full + 8 * s, u & 1); ++n) {
+      if (rank == 0) {
+        for (int i = (it > kQST ? it - kQST : 0); i < it; ++i) {
+          const int s = i % kQST, u = i / kQST;
+          for (int n = 0; n < 100000 && !mbar_try_wait_cluster(full + 8 * s, u & 1); ++n) {
+          }
         }
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer: D[128 x 256] (+)= X[128 x 64] . W[256 x 64]^T per block,
-    // tile lt of this CTA into accumulator lt & 1
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(1, 1, 0, kQBM, kQBN);
+    // ---- MMA issuer (first CTA): D[256 x 256] (+)= X[256 x 64] . W[256 x 64]^T
+    // per block, tile lt of this pair into accumulator lt & 1
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = make_idesc(1, 1, 0, 2 * kQBM, kQBN);
       bool ok = true;
       int it = 0, lt = 0;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++lt) {
+      for (int tile = pair; tile < ntiles && ok; tile += npairs, ++lt) {
         const int a = lt & 1;
-        // the epilogue has read this accumulator's previous tile
+        // both CTAs' epilogues have read this accumulator's previous tile
         if (lt >= 2 && !qkv_wait(acce + 8 * a, ((lt >> 1) - 1) & 1, p)) {
           ok = false;
           break;
@@ -157,29 +236,29 @@ __global__ void __launch_bounds__(kQThreads, 1) lamp_qkv_kernel(const __grid_con
           for (int kk = 0; kk < kQBK / 16; ++kk) {
             const uint64_t ad = make_sdesc(st + kk * 32, 16, 1024, kLayoutSW128);
             const uint64_t bd = make_sdesc(st + kQA + kk * 32, 16, 1024, kLayoutSW128);
-            mma_f16(acc, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            mma_f16_pair(acc, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(empty + 8 * s);
+          mma_commit_pair(empty + 8 * s);
         }
-        mma_commit(accf + 8 * a);  // also after a failure: the epilogue must not wait forever
+        mma_commit_pair(accf + 8 * a);  // also after a failure: the epilogues must not wait forever
       }
       // the accumulators are released below only once the last MMAs are done
       if (lt > 0) {
         const int a = (lt - 1) & 1;
-        for (int n = 0; n < 1000000 && !mbar_try_wait(accf + 8 * a, ((lt - 1) >> 1) & 1); ++n) {
+        for (int n = 0; n < 1000000 && !mbar_try_wait_cluster(accf + 8 * a, ((lt - 1) >> 1) & 1); ++n) {
         }
       }
     }
   } else {
-    // ---- epilogue: one token row per thread
+    // ---- epilogue: one token row per thread, this CTA's 128 rows of the tile
     const int quad = warp & 3;  // TMEM lanes 32 quad .. (warp w reads lanes of w % 4)
     const int r = quad * 32 + lane;
     const int D = p.D, CH = D / 32, TT = (p.N + kBN - 1) / kBN;
     bool ok = true;
     int lt = 0;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++lt) {
+    for (int tile = pair; tile < ntiles && ok; tile += npairs, ++lt) {
       const int a = lt & 1;
-      const int m0 = (tile / ntn) * kQBM, n0 = (tile % ntn) * kQBN;
+      const int m0 = (tile / ntn) * (2 * kQBM) + (int)rank * kQBM, n0 = (tile % ntn) * kQBN;
       const int t = m0 + r;
       const bool live_row = t < p.T;
       const int b = live_row ? t / p.N : 0, n = live_row ? t - b * p.N : 0;
@@ -193,9 +272,10 @@ __global__ void __launch_bounds__(kQThreads, 1) lamp_qkv_kernel(const __grid_con
         uint32_t acc[32];
         tmem_ld32(tmem + (uint32_t)(a * kQBN) + ((uint32_t)(quad * 32) << 16) + c0, acc);
         tmem_wait_ld();
-        if (c0 + 32 == kQBN) {  // the accumulator is read: the MMA warp may reuse it
+        if (c0 + 32 == kQBN) {  // the accumulator is read: the MMA thread may reuse it
           tc_fence_before();
-          mbar_arrive(acce + 8 * a);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(map_to_rank(acce + 8 * a, 0));
         }
         const int col = n0 + c0;
         if (col >= p.ncols) continue;  // warp-uniform
@@ -264,25 +344,40 @@ __global__ void __launch_bounds__(kQThreads, 1) lamp_qkv_kernel(const __grid_con
       }
     }
   }
+  // neither CTA leaves (or frees TMEM) while the pair's MMAs, copies or
+  // arrivals may still touch its shared memory or TMEM
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 2 * kQBN);
+    tmem_dealloc_pair(tmem, 2 * kQBN);
   }
 }
 
 cudaError_t launch_qkv(const QkvParams& p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(lamp_qkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
   if (e != cudaSuccess) return e;
-  const long long tiles = (long long)((p.T + kQBM - 1) / kQBM) * ((p.ncols + kQBN - 1) / kQBN);
+  const long long tiles = (long long)((p.T + 2 * kQBM - 1) / (2 * kQBM)) * ((p.ncols + kQBN - 1) / kQBN);
   if (tiles == 0) return cudaSuccess;
-  int dev = 0, sms = 0;
+  // persistent: as many CTA pairs as can be resident at once (one CTA per
+  // SM; a pair sits in one GPC), tiles strided over them
+  static int resident[64];
+  int dev = 0;
   e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // persistent: one CTA per SM (the shared memory allows one), tiles strided over them
-  const dim3 grid((unsigned)(tiles < sms ? tiles : sms));
+  int pairs = (dev >= 0 && dev < 64) ? resident[dev] : 0;
+  if (pairs <= 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 1024);
+    cfg.blockDim = dim3(kQThreads);
+    cfg.dynamicSmemBytes = kQSmem;
+    e = cudaOccupancyMaxActiveClusters(&pairs, (void*)lamp_qkv_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (pairs <= 0) return cudaErrorInvalidConfiguration;
+    if (dev >= 0 && dev < 64) resident[dev] = pairs;
+  }
+  const dim3 grid((unsigned)(2 * (tiles < pairs ? tiles : pairs)));
   lamp_qkv_kernel<<<grid, kQThreads, kQSmem, st>>>(p);
   return cudaGetLastError();
 }

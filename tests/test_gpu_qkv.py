@@ -105,6 +105,26 @@ def test_cache_equals_the_pre_pass():
     assert list(a[3][:8]) == list(cnt.cpu().numpy()[:8])
 
 
+def test_many_tiles_per_cta_pair():
+    """A persistent grid with several tiles per CTA pair (both TMEM
+    accumulators reused): every q, k, v value equals the oracle's, and the
+    epilogue's K/V cache gives the same attention as the pre-pass."""
+    B, N, Hq, Hkv, d, hidden = 2, 4096, 32, 8, 128, 256
+    x, w = _exact_inputs(B * N, hidden, (Hq + 2 * Hkv) * d, seed=21)
+    q, k, v, ws = _project(x, w, B, Hq, Hkv, d)
+    qo, ko, vo = oracle.qkv_projection(x, w, batch=B, heads_q=Hq, heads_kv=Hkv, head_dim=d)
+    for got, want in ((q, qo), (k, ko), (v, vo)):
+        assert np.array_equal(got.double().cpu().numpy(), want)
+    a = run_gpu(q, k, v, tau=0.5)
+    mb, cnt = lamp.new_stats(B, Hq, N)
+    out, lse, _, _ = lamp.lamp_attn_fwd(q, k, v, mask_bytes=mb, counters=cnt, workspace=ws, kv_prepared=True,
+                                        tau=0.5)
+    torch.cuda.synchronize()
+    assert np.array_equal(a[0], out.float().cpu().numpy().astype(np.float64))
+    assert np.array_equal(a[2], mb.cpu().numpy())
+    assert list(a[3][:8]) == list(cnt.cpu().numpy()[:8])
+
+
 def test_fp8_pv_cache():
     """With FP8 P.V the projection also writes the transposed E4M3 copy of v."""
     B, N, Hq, Hkv, d, hidden = 1, 192, 2, 1, 128, 256
