@@ -278,14 +278,16 @@ int lamp_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out
  * counterpart: this is a data-movement variant only, and the results are
  * bit-identical to lamp_attn_fwd on the same inputs.
  *
- * The batch -- and, while batch * groups < 8, the kv-head groups -- is cut
+ * The batch -- and, while batch * groups < 16, the kv-head groups -- is cut
  * into chunks; per chunk the inputs are copied to the device, the forward
- * pass runs and the outputs are copied back, on two internal copy streams
- * and two device slots, so the copies of one chunk overlap the computation
- * of its neighbours.  Chunks compute alternately on shapes->stream and on
- * an internal stream (joined back into shapes->stream before the call
- * returns), so one chunk's kernels start on the SMs the previous chunk's
- * tail leaves idle.
+ * pass runs and the outputs are copied back, on two internal copy streams,
+ * so the copies of one chunk overlap the computation of its neighbours.
+ * Each chunk has its own device slot while the slots fit 1 GiB (else at
+ * least two slots are reused in turn; the environment variable
+ * LAMP_HOST_MAX_SLOTS, >= 2, lowers the count).  Chunks compute in turn on
+ * shapes->stream and three internal streams (joined back into
+ * shapes->stream before the call returns), so one chunk's kernels start on
+ * the SMs the previous chunks' tails leave idle.
  *   q, k, v, out  HOST, BSHD with the strides of `shapes` (elements); the
  *                 head and head_dim dimensions must be dense
  *                 (stride[2] == head_dim).

@@ -1,13 +1,18 @@
 // lamp_host.cu -- lamp_attn_fwd on host buffers: the batch (and, for small
 // batches, the kv-head groups) is cut into chunks, and per chunk the
 // host->device copies, the forward pass and the device->host copies run on
-// their own streams with two device slots, so the transfers of one chunk
-// overlap the computation of its neighbours.  Consecutive chunks compute on
-// two streams (the caller's and an internal one), so the CTAs of the next
-// chunk fill the SMs that the tail of the current one leaves idle.
+// their own streams, so the transfers of one chunk overlap the computation
+// of its neighbours.  Each chunk has its own device slot while the slots fit
+// a 1 GiB budget (else slots are reused, at least two), so a chunk's copy in
+// never waits for an earlier chunk's computation.  Consecutive chunks
+// compute on four streams (the caller's and three internal ones): every
+// chunk holds causal rows that see the whole sequence, whose CTAs take
+// about as long as the chunk itself, so the next chunks' CTAs must fill the
+// SMs that those leave idle.
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -21,19 +26,25 @@ struct Plan {
   int nb, nh;       // chunks over the batch and over kv-head groups
   int hq_c, hkv_c;  // query and kv heads per chunk
   int nchunks;
+  int nslots;       // device slots (chunk c uses slot c % nslots)
   size_t q_bytes, kv_bytes, o_bytes, lse_bytes, ws_bytes, slot_bytes, total;
   lamp_shapes cs;   // shapes of one chunk (dense device layout)
 };
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// At least 8 chunks when possible: kv-head groups are split (a divisor of
-// heads_kv) until batch * groups reaches 8.
+constexpr int kMinChunks = 16;                     // measured: 16 beat 4, 8 and 32 at the Qwen3-8B shape
+constexpr int kMaxSlots = 32;
+constexpr size_t kSlotBudget = (size_t)1 << 30;    // device bytes for slots beyond the first two
+constexpr int kComputeStreams = 4;                 // the caller's stream + 3 internal ones
+
+// At least kMinChunks chunks when possible: kv-head groups are split (a
+// divisor of heads_kv) until batch * groups reaches it.
 bool make_plan(const lamp_shapes& s, Plan& p) {
   const int B = s.batch, Hq = s.heads_q, Hkv = s.heads_kv, N = s.seqlen, D = s.head_dim;
   if (B < 1 || N < 1 || Hkv < 1 || Hq < 1 || Hq % Hkv) return false;
   int nh = 1;
-  while (B * nh < 8 && nh < Hkv) {
+  while (B * nh < kMinChunks && nh < Hkv) {
     int next = nh + 1;
     while (next <= Hkv && Hkv % next) ++next;
     if (next > Hkv) break;
@@ -68,7 +79,15 @@ bool make_plan(const lamp_shapes& s, Plan& p) {
   p.ws_bytes = al256(lamp_attn_workspace_bytes(&c));
   if (p.ws_bytes == 0) return false;
   p.slot_bytes = p.q_bytes + 2 * p.kv_bytes + p.o_bytes + p.lse_bytes + p.ws_bytes;
-  p.total = 2 * p.slot_bytes + al256((size_t)p.nchunks * LAMP_NUM_COUNTERS * 8);
+  const size_t fit = kSlotBudget / p.slot_bytes;
+  p.nslots = (int)(fit < 2 ? 2 : (fit > (size_t)kMaxSlots ? kMaxSlots : fit));
+  // LAMP_HOST_MAX_SLOTS (>= 2) caps the slots, e.g. to exercise their reuse
+  if (const char* e = getenv("LAMP_HOST_MAX_SLOTS")) {
+    const int m = atoi(e);
+    if (m >= 2 && m < p.nslots) p.nslots = m;
+  }
+  if (p.nslots > p.nchunks) p.nslots = p.nchunks;
+  p.total = (size_t)p.nslots * p.slot_bytes + al256((size_t)p.nchunks * LAMP_NUM_COUNTERS * 8);
   return true;
 }
 
@@ -89,9 +108,9 @@ __global__ void sum_counters_kernel(unsigned long long* dst, const unsigned long
   dst[i] = acc;
 }
 
-// Two copy streams and a second compute stream per device, created once.
+// Two copy streams and the internal compute streams per device, created once.
 struct CopyStreams {
-  cudaStream_t h2d = nullptr, d2h = nullptr, comp = nullptr;
+  cudaStream_t h2d = nullptr, d2h = nullptr, comp[kComputeStreams - 1] = {};
 };
 std::mutex g_streams_mu;
 CopyStreams g_streams[64];
@@ -102,7 +121,8 @@ bool copy_streams(int dev, CopyStreams& out) {
   CopyStreams& cs = g_streams[dev];
   if (!cs.h2d && cudaStreamCreateWithFlags(&cs.h2d, cudaStreamNonBlocking) != cudaSuccess) return false;
   if (!cs.d2h && cudaStreamCreateWithFlags(&cs.d2h, cudaStreamNonBlocking) != cudaSuccess) return false;
-  if (!cs.comp && cudaStreamCreateWithFlags(&cs.comp, cudaStreamNonBlocking) != cudaSuccess) return false;
+  for (auto& c : cs.comp)
+    if (!c && cudaStreamCreateWithFlags(&c, cudaStreamNonBlocking) != cudaSuccess) return false;
   out = cs;
   return true;
 }
@@ -142,16 +162,27 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
 
   uint8_t* buf = (uint8_t*)dev_buffer;
   if (buf && (dev_buffer_bytes < p.total || ((uintptr_t)buf & 255u))) return LAMP_ERR_WORKSPACE;
-  cudaEvent_t ev[9] = {};  // per slot: inputs landed, computed, outputs read back; three joins
-  for (int i = 0; i < 9; ++i)
-    if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
-      for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
-      return LAMP_ERR_CUDA;
-    }
+  // per slot: inputs landed, computed, outputs read back; then the start
+  // and one join per internal stream
+  constexpr int kJoin = 3 * kMaxSlots;
+  const int nev = 3 * p.nslots;
+  cudaEvent_t ev[kJoin + 2 + kComputeStreams] = {};
+  auto make_ev = [&](int i) { return cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess; };
+  bool evs_ok = true;
+  for (int i = 0; i < nev && evs_ok; ++i) evs_ok = make_ev(i);
+  for (int i = kJoin; i < kJoin + 2 + kComputeStreams && evs_ok; ++i) evs_ok = make_ev(i);
+  auto free_evs = [&]() {
+    for (auto& e : ev)
+      if (e) cudaEventDestroy(e);
+  };
+  if (!evs_ok) {
+    free_evs();
+    return LAMP_ERR_CUDA;
+  }
   bool own = false;
   if (!buf) {
     if (cudaMallocAsync((void**)&buf, p.total, sc) != cudaSuccess) {
-      for (auto& e : ev) cudaEventDestroy(e);
+      free_evs();
       return LAMP_ERR_CUDA;
     }
     own = true;
@@ -161,28 +192,32 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
     if (e != cudaSuccess && rc == LAMP_OK) rc = LAMP_ERR_CUDA;
     return e == cudaSuccess;
   };
-  unsigned long long* cnt = (unsigned long long*)(buf + 2 * p.slot_bytes);
+  unsigned long long* cnt = (unsigned long long*)(buf + (size_t)p.nslots * p.slot_bytes);
   const size_t ei = s.in_dtype == LAMP_DT_FP32 ? 4 : 2, eo = s.out_dtype == LAMP_DT_FP32 ? 4 : 2;
   const int N = s.seqlen, Hq = s.heads_q, Hkv = s.heads_kv;
   const int T = (N + 63) / 64;
 
   // the other streams start after the work already queued on the caller's
-  // stream; chunks on slot 0 compute there, chunks on slot 1 on cps.comp
-  cuda_ok(cudaEventRecord(ev[6], sc));
-  cuda_ok(cudaStreamWaitEvent(cps.h2d, ev[6], 0));
-  cuda_ok(cudaStreamWaitEvent(cps.d2h, ev[6], 0));
-  cuda_ok(cudaStreamWaitEvent(cps.comp, ev[6], 0));
-  const cudaStream_t comp[2] = {sc, cps.comp};
+  // stream; chunk c computes on comp[c % kComputeStreams]
+  cuda_ok(cudaEventRecord(ev[kJoin], sc));
+  cuda_ok(cudaStreamWaitEvent(cps.h2d, ev[kJoin], 0));
+  cuda_ok(cudaStreamWaitEvent(cps.d2h, ev[kJoin], 0));
+  cudaStream_t comp[kComputeStreams] = {sc};
+  for (int i = 1; i < kComputeStreams; ++i) {
+    comp[i] = cps.comp[i - 1];
+    cuda_ok(cudaStreamWaitEvent(comp[i], ev[kJoin], 0));
+  }
   for (int c = 0; c < p.nchunks && rc == LAMP_OK; ++c) {
     const int b = c / p.nh, g0 = (c % p.nh) * p.hkv_c, h0 = g0 * (Hq / Hkv);
-    const int slot = c & 1;
+    const int slot = c % p.nslots;
+    const bool reuse = c >= p.nslots;
     uint8_t* sb = buf + slot * p.slot_bytes;
     uint8_t *dq = sb, *dk = sb + p.q_bytes, *dv = dk + p.kv_bytes, *dout = dv + p.kv_bytes;
     float* dlse = (float*)(dout + p.o_bytes);
     uint8_t* dws = (uint8_t*)dlse + p.lse_bytes;
     cudaEvent_t e_in = ev[3 * slot], e_done = ev[3 * slot + 1], e_out = ev[3 * slot + 2];
     // inputs: the slot's previous chunk must have been computed
-    if (c >= 2) cuda_ok(cudaStreamWaitEvent(cps.h2d, e_done, 0));
+    if (reuse) cuda_ok(cudaStreamWaitEvent(cps.h2d, e_done, 0));
     const char* hq = (const char*)q + ((size_t)b * s.q_stride[0] + (size_t)h0 * D) * ei;
     const char* hk = (const char*)k + ((size_t)b * s.k_stride[0] + (size_t)g0 * D) * ei;
     const char* hv = (const char*)v + ((size_t)b * s.v_stride[0] + (size_t)g0 * D) * ei;
@@ -194,9 +229,9 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
                               N, cudaMemcpyHostToDevice, cps.h2d));
     cuda_ok(cudaEventRecord(e_in, cps.h2d));
     // compute: inputs landed, and the slot's previous outputs were read back
-    const cudaStream_t cst = comp[slot];
+    const cudaStream_t cst = comp[c % kComputeStreams];
     cuda_ok(cudaStreamWaitEvent(cst, e_in, 0));
-    if (c >= 2) cuda_ok(cudaStreamWaitEvent(cst, e_out, 0));
+    if (reuse) cuda_ok(cudaStreamWaitEvent(cst, e_out, 0));
     if (rc != LAMP_OK) break;
     lamp_shapes cs = p.cs;
     cs.stream = cst;
@@ -222,13 +257,15 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
     cuda_ok(cudaEventRecord(e_out, cps.d2h));
   }
   // join: the caller's stream waits for the last read-back, the last copy
-  // in and the second compute stream
-  cuda_ok(cudaEventRecord(ev[7], cps.d2h));
-  cuda_ok(cudaStreamWaitEvent(sc, ev[7], 0));
-  cuda_ok(cudaEventRecord(ev[6], cps.h2d));
-  cuda_ok(cudaStreamWaitEvent(sc, ev[6], 0));
-  cuda_ok(cudaEventRecord(ev[8], cps.comp));
-  cuda_ok(cudaStreamWaitEvent(sc, ev[8], 0));
+  // in and the internal compute streams
+  cuda_ok(cudaEventRecord(ev[kJoin + 1], cps.d2h));
+  cuda_ok(cudaStreamWaitEvent(sc, ev[kJoin + 1], 0));
+  cuda_ok(cudaEventRecord(ev[kJoin], cps.h2d));
+  cuda_ok(cudaStreamWaitEvent(sc, ev[kJoin], 0));
+  for (int i = 1; i < kComputeStreams; ++i) {
+    cuda_ok(cudaEventRecord(ev[kJoin + 1 + i], comp[i]));
+    cuda_ok(cudaStreamWaitEvent(sc, ev[kJoin + 1 + i], 0));
+  }
   if (rc == LAMP_OK && stats && stats->counters) {
     sum_counters_kernel<<<1, 32, 0, sc>>>((unsigned long long*)stats->counters, cnt, p.nchunks);
     cuda_ok(cudaGetLastError());
@@ -236,7 +273,7 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
   if (own) cuda_ok(cudaFreeAsync(buf, sc));
   // the results are in host memory when the call returns
   cuda_ok(cudaStreamSynchronize(sc));
-  for (auto& e : ev) cudaEventDestroy(e);
+  free_evs();
   return rc;
 }
 

@@ -63,3 +63,20 @@ def test_host_buffer_given(lamp):
     small = torch.empty(nbytes // 2, dtype=torch.uint8, device="cuda")
     with pytest.raises(lamp.LampError):
         lamp.lamp_attn_fwd_host(qh, kh, vh, dev_buffer=small)
+
+
+def test_host_slot_reuse(lamp, monkeypatch):
+    """Two device slots for eight chunks: a chunk's copy in waits for the
+    computation of the chunk two before it, and the results stay the same."""
+    monkeypatch.setenv("LAMP_HOST_MAX_SLOTS", "2")
+    B, N, Hq, Hkv, d = 4, 700, 4, 2, 128
+    q, k, v = synth.gen_outlier_sink(B, N, Hq, Hkv, d, seed=17)
+    qh, kh, vh = (torch.from_numpy(x).to(torch.bfloat16).pin_memory() for x in (q, k, v))
+    mb_d, cnt_d = lamp.new_stats(B, Hq, N)
+    od, ld, _, _ = lamp.lamp_attn_fwd(qh.cuda(), kh.cuda(), vh.cuda(), mask_bytes=mb_d, counters=cnt_d)
+    mb_h, cnt_h = lamp.new_stats(B, Hq, N)
+    oh, lh, _, _ = lamp.lamp_attn_fwd_host(qh, kh, vh, mask_bytes=mb_h, counters=cnt_h)
+    torch.cuda.synchronize()
+    assert int(cnt_h[9]) == 0
+    assert torch.equal(od.cpu().view(torch.int16), oh.view(torch.int16)) and torch.equal(ld.cpu(), lh)
+    assert torch.equal(mb_d.cpu(), mb_h.cpu()) and torch.equal(cnt_d.cpu(), cnt_h.cpu())
