@@ -242,7 +242,7 @@ def qkv_fusion_leg(args, w, lamp, torch, dev, flush, bf16_peak):
     the layer input x [B N, hidden] (seeded, synthetic) to out: (a) cuBLAS
     (torch.matmul) writes y = x W^T, q / k / v are strided views of y, and
     the attention runs with its pre-pass; (b) lamp_qkv_project writes q, k,
-    v and the K/V cache, and the attention runs on the cache."""
+    v, the K/V cache and the E4M3 copy of q, and the attention runs on them."""
     hidden = args.qkv_fusion
     B, N, Hq, Hkv, d = w.batch, w.seqlen, w.heads_q, w.heads_kv, w.head_dim
     g = torch.Generator(device=dev).manual_seed(args.seed + 11)
@@ -262,7 +262,7 @@ def qkv_fusion_leg(args, w, lamp, torch, dev, flush, bf16_peak):
     def fused():
         q, k, v = lamp.qkv_project(x, wt, batch=B, heads_q=Hq, heads_kv=Hkv, head_dim=d, workspace=ws)
         lamp.lamp_attn_fwd(q, k, v, mask=w.mask, window=w.window, delta=args.delta, tau=args.tau, out=out,
-                           lse=lse, workspace=ws, kv_prepared=True)
+                           lse=lse, workspace=ws, kv_prepared=True, q_prepared=True)
 
     def proj_only_cublas():
         torch.matmul(x, wt.t())

@@ -150,6 +150,11 @@ typedef struct {
                             16-bit copies and key-tile norms, written by
                             lamp_kv_prepare with the same shapes (the forward
                             call then skips that work); 0: the call writes them */
+  int32_t q_prepared;    /* 1: `workspace` already holds this q's E4M3 copy and
+                            row / chunk norms, written by lamp_qkv_project with
+                            the same shapes (bf16 q only; the forward call then
+                            neither runs the query part of the pre-pass nor
+                            rounds Q in its CTAs); 0: the call derives them */
 } lamp_shapes;
 
 typedef struct {
@@ -199,11 +204,12 @@ int lamp_attn_fwd(const void* q, const void* k, const void* v, void* out,
  *   k, v      DEVICE, as for lamp_attn_fwd.
  *   shapes    workspace must be given (>= lamp_attn_workspace_bytes() of
  *             these shapes; the later calls check their own size);
- *             kv_prepared is ignored; q_stride / o_stride are not used.
+ *             kv_prepared and q_prepared are ignored; q_stride /
+ *             o_stride are not used.
  * Asynchronous on shapes->stream; LAMP_ERR_INVALID_ARG for a missing
  * workspace, otherwise errors as lamp_attn_fwd.  Not for
  * lamp_attn_fwd_host / lamp_attn_fwd_noalloc (their scratch is their own:
- * they return LAMP_ERR_INVALID_ARG for kv_prepared = 1).
+ * they return LAMP_ERR_INVALID_ARG for kv_prepared = 1 or q_prepared = 1).
  */
 int lamp_kv_prepare(const void* k, const void* v, const lamp_shapes* shapes);
 
@@ -213,9 +219,13 @@ int lamp_kv_prepare(const void* k, const void* v, const lamp_shapes* shapes);
  * operands, FP32 tensor-core accumulation, one rounding to BF16), its
  * columns split into q, k and v; for the key and value columns it also
  * writes what lamp_kv_prepare writes (the E4M3 copy of k, the fp16 copy of
- * v and the key-tile norms) into shapes->workspace, so that lamp_attn_fwd
- * on these q, k, v with shapes->kv_prepared = 1 and the same workspace runs
- * without a pre-pass.
+ * v and the key-tile norms) into shapes->workspace, and for the query
+ * columns the E4M3 copy of q and its row and chunk norms, so that
+ * lamp_attn_fwd on these q, k, v with shapes->kv_prepared = 1,
+ * shapes->q_prepared = 1 and the same workspace runs without a pre-pass
+ * and without rounding Q in its CTAs (the E4M3 copies of q and k are the
+ * projection's outputs rounded once more, as the pre-pass would round
+ * them).
  *   x        DEVICE bf16 [batch * seqlen, hidden], row-major (token-major).
  *   w        DEVICE bf16 [(heads_q + 2 heads_kv) * head_dim, hidden],
  *            row-major: the query heads' rows, then the key heads', then

@@ -196,6 +196,9 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   // keys and values prepared by lamp_kv_prepare in the caller's workspace
   const bool prepared = s.kv_prepared != 0;
   if (prepared && !s.workspace) return LAMP_ERR_INVALID_ARG;
+  // the E4M3 copy of bf16 q and its norms written by lamp_qkv_project
+  const bool q_prepared = s.q_prepared != 0;
+  if (q_prepared && (!s.workspace || s.in_dtype != LAMP_DT_BF16)) return LAMP_ERR_INVALID_ARG;
   if (mask_kind < LAMP_MASK_NONE || mask_kind > LAMP_MASK_SLIDING) return LAMP_ERR_INVALID_ARG;
   if (mask_kind == LAMP_MASK_SLIDING && s.window < 1) return LAMP_ERR_INVALID_ARG;
   if (!(delta >= 0.0f) || std::isnan(tau)) return LAMP_ERR_INVALID_ARG;
@@ -279,8 +282,9 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
   fp.force = s.force;
   fp.out_f32 = s.out_dtype == LAMP_DT_FP32;
   // bf16 q: the fused kernel rounds its Q16 tile (the input values) to E4M3
-  // itself; fp32 q must be rounded from the fp32 values, by the pre-pass
-  fp.q8_in_cta = s.in_dtype == LAMP_DT_BF16 && !sweep;
+  // itself, unless lamp_qkv_project wrote the E4M3 copy; fp32 q must be
+  // rounded from the fp32 values, by the pre-pass
+  fp.q8_in_cta = s.in_dtype == LAMP_DT_BF16 && !sweep && !q_prepared;
   fp.sigma_f = (float)sigma_d;
   fp.sigma_d = sigma_d;
   fp.sig18 = std::ldexp(sigma_d, -18);
@@ -307,7 +311,7 @@ int run_pass(const void* q, const void* k, const void* v, void* out, float* lse,
 
   PrepParams pp{};
   pp.q = q; pp.k = k; pp.v = sweep ? nullptr : v;  // the sweep needs no V
-  pp.skip_q = fp.q8_in_cta;
+  pp.skip_q = fp.q8_in_cta || q_prepared;
   pp.skip_kv = prepared;  // with bf16 q as well, nothing is left for the pre-pass
   for (int i = 0; i < 3; ++i) { pp.qs[i] = s.q_stride[i]; pp.ks[i] = s.k_stride[i]; pp.vs[i] = s.v_stride[i]; }
   pp.q8 = ws + w.q8; pp.k8 = ws + w.k8; pp.v16 = ws + w.v16;
@@ -412,6 +416,7 @@ int qkv_project(const void* x, const void* w, int hidden, void* q, void* k, void
   if (!ok) return LAMP_ERR_CUDA;
   p.q = (uint16_t*)q; p.k = (uint16_t*)k; p.v = (uint16_t*)v;
   p.k8 = ws + wl.k8; p.v16 = (uint16_t*)(ws + wl.v16);
+  p.q8 = ws + wl.q8; p.nq = (float*)(ws + wl.nq); p.nqc = (float*)(ws + wl.nqc);
   p.nk = (float*)(ws + wl.nk); p.nkc = (float*)(ws + wl.nkc);
   p.abort = (unsigned int*)(ws + wl.abort);
   p.counters = stats ? (unsigned long long*)stats->counters : nullptr;

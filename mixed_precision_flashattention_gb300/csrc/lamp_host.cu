@@ -144,7 +144,7 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
                        const lamp_shapes* shapes, int mask_kind, float delta, float tau, lamp_stats* stats,
                        void* dev_buffer, size_t dev_buffer_bytes) {
   // (the device scratch of each chunk is this call's own: nothing prepared in it)
-  if (!q || !k || !v || !out || !shapes || shapes->kv_prepared) return LAMP_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || !shapes || shapes->kv_prepared || shapes->q_prepared) return LAMP_ERR_INVALID_ARG;
   const lamp_shapes& s = *shapes;
   const int D = s.head_dim;
   if (D != 64 && D != 128 && D != 256) return LAMP_ERR_UNSUPPORTED;

@@ -53,7 +53,7 @@ int scratch_on_current_device(void** out) {
 extern "C" int lamp_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
                                      const lamp_shapes* shapes, int mask_kind, float delta, float tau,
                                      lamp_stats* stats) {
-  if (!shapes || shapes->kv_prepared) return LAMP_ERR_INVALID_ARG;  // the scratch is this call's own
+  if (!shapes || shapes->kv_prepared || shapes->q_prepared) return LAMP_ERR_INVALID_ARG;  // the scratch is this call's own
   const size_t need = lamp_attn_workspace_bytes(shapes);
   if (need == 0) {
     // the same status lamp_attn_fwd gives: shapes that are valid except for

@@ -7,8 +7,10 @@
 // key columns the epilogue also writes the E4M3 copy of k, the per-chunk
 // and per-row norms of that copy (as atomic maxima over each 64-key tile),
 // and for the value columns the fp16 copy of v: the same K/V cache the
-// attention's pre-pass (lamp_prep.cu) writes, so the attention call that
-// follows runs with kv_prepared = 1 and no pre-pass.
+// attention's pre-pass (lamp_prep.cu) writes; for the query columns it
+// writes the E4M3 copy of q and its row and chunk norms, which the fused
+// kernel otherwise derives in its CTAs.  The attention call that follows
+// runs with kv_prepared = 1 and q_prepared = 1, without a pre-pass.
 //
 // Tiles of 256 tokens x 256 columns (two heads at d = 128), the column
 // tiles of a token tile one after the other, over a persistent grid of CTA
@@ -266,7 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQThreads, 1)
       ok = __all_sync(0xffffffffu, ok);  // warp-uniform: TMEM loads and shuffles below
       if (!ok) break;
       tc_fence_after();
-      float ssum = 0.0f;  // sum of squares of the E4M3 key row of the current head
+      float ssum = 0.0f;  // sum of squares of the E4M3 query or key row of the current head
 #pragma unroll 1
       for (int c0 = 0; c0 < kQBN; c0 += 32) {
         uint32_t acc[32];
@@ -291,11 +293,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQThreads, 1)
           vals[2 * i + 1] = __high2float(h2);
         }
         if (head < p.Hq) {
+          // E4M3 copy and its norms: one writer per element (upper bounds:
+          // the float sums of squares rounded up, as the pre-pass takes them)
+          const size_t qrow = ((size_t)b * p.Hq + head) * p.N + n;  // row of the [B, Hq, N, D] copy
+          uint32_t c8[8];
+          float ss = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint16_t c = cvt_e4m3x2(vals[2 * i + 1], vals[2 * i]);
+            const uint32_t hv = e4m3x2_to_f16x2(c);
+            __half2 h2;
+            memcpy(&h2, &hv, 4);
+            const float a0 = __low2float(h2), a1 = __high2float(h2);
+            ss = fmaf(a0, a0, fmaf(a1, a1, ss));
+            if (i & 1) c8[i >> 1] |= (uint32_t)c << 16; else c8[i >> 1] = c;
+          }
+          ssum += ss;
           if (live_row) {
             uint4* dst = reinterpret_cast<uint4*>(p.q + (((size_t)b * p.N + n) * p.Hq + head) * D + e);
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
+            uint4* d8 = reinterpret_cast<uint4*>(p.q8 + qrow * D + e);
+            d8[0] = make_uint4(c8[0], c8[1], c8[2], c8[3]);
+            d8[1] = make_uint4(c8[4], c8[5], c8[6], c8[7]);
+            p.nqc[qrow * CH + e / 32] = sqrtf(ss) * (1.0f + 0x1p-16f);
+            if (e + 32 == D) p.nq[qrow] = sqrtf(ssum) * (1.0f + 0x1p-16f);
           }
+          if (e + 32 == D) ssum = 0.0f;
         } else if (head < p.Hq + p.Hkv) {
           const int g = head - p.Hq;
           const size_t krow = ((size_t)b * p.Hkv + g) * p.N + n;  // row of the [B, Hkv, N, D] copies

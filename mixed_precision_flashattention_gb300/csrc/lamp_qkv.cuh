@@ -13,6 +13,9 @@ struct QkvParams {
   uint16_t* v;                   // [B, N, Hkv, D] BF16
   uint8_t* k8;                   // workspace [B, Hkv, N, D] E4M3
   uint16_t* v16;                 // workspace [B, Hkv, N, D] fp16
+  uint8_t* q8;                   // workspace [B, Hq, N, D] E4M3
+  float* nq;                     // workspace [B, Hq, N]: norm of each E4M3 query row
+  float* nqc;                    // workspace [B, Hq, N, D/32]: norms of its 32-element chunks
   float* nk;                     // workspace [B, Hkv, T_k] (zeroed before the launch)
   float* nkc;                    // workspace [B, Hkv, T_k, D/32] (zeroed before the launch)
   unsigned int* abort;           // grid abort word (zeroed before the launch)

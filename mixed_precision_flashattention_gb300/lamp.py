@@ -43,6 +43,7 @@ class LampShapes(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("stream", ctypes.c_void_p), ("stage_events", ctypes.c_void_p * 3),
         ("pv_mode", ctypes.c_int32), ("qk_accum", ctypes.c_int32), ("kv_prepared", ctypes.c_int32),
+        ("q_prepared", ctypes.c_int32),
     ]
 
 
@@ -111,7 +112,7 @@ def _check(code: int):
 
 
 def make_shapes(q, k, v, out, *, window=0, scale=0.0, force="off", workspace=None, stream=None,
-                stage_events=None, pv="fp16", qk="exact", kv_prepared=False):
+                stage_events=None, pv="fp16", qk="exact", kv_prepared=False, q_prepared=False):
     B, N, Hq, d = q.shape
     sh = LampShapes()
     sh.batch, sh.seqlen, sh.heads_q, sh.heads_kv, sh.head_dim = B, N, Hq, k.shape[2], d
@@ -128,6 +129,7 @@ def make_shapes(q, k, v, out, *, window=0, scale=0.0, force="off", workspace=Non
     sh.pv_mode = PV[pv]
     sh.qk_accum = QK[qk]
     sh.kv_prepared = int(bool(kv_prepared))
+    sh.q_prepared = int(bool(q_prepared))
     if workspace is not None:
         sh.workspace = workspace.data_ptr()
         sh.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -147,7 +149,7 @@ def workspace_bytes(q, k, v, out=None, **kw) -> int:
 def lamp_attn_fwd(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -8, tau=2.0 ** -1,
                   force="off", out=None, out_dtype=None, lse=None, want_lse=True, mask_bytes=None,
                   counters=None, workspace=None, stream=None, stage_events=None, pv="fp16", qk="exact",
-                  kv_prepared=False):
+                  kv_prepared=False, q_prepared=False):
     """Forward pass.  q [B, N, Hq, d], k/v [B, N, Hkv, d] CUDA tensors (bf16
     or fp32, d contiguous).  Returns (out, lse, mask_bytes, counters); the
     last three may be None when not requested.  Asynchronous on ``stream``
@@ -155,7 +157,9 @@ def lamp_attn_fwd(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -
     torch.cuda.Event recorded around the pre-pass and the fused kernel.
     ``pv``: "fp16" or "fp8", the P.V precision of unflagged sub-blocks.
     ``qk``: "exact" or "chunk32", how the 8-bit logits accumulate.
-    ``kv_prepared``: ``workspace`` holds this k / v prepared by kv_prepare."""
+    ``kv_prepared``: ``workspace`` holds this k / v prepared by kv_prepare.
+    ``q_prepared``: ``workspace`` holds this q's E4M3 copy and norms, written
+    by qkv_project."""
     lib = load()
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
         raise LampError("q, k, v must be CUDA tensors")
@@ -167,7 +171,8 @@ def lamp_attn_fwd(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, N), device=q.device, dtype=torch.float32)
     sh = make_shapes(q, k, v, out, window=window, scale=scale, force=force, workspace=workspace,
-                     stream=stream, stage_events=stage_events, pv=pv, qk=qk, kv_prepared=kv_prepared)
+                     stream=stream, stage_events=stage_events, pv=pv, qk=qk, kv_prepared=kv_prepared,
+                     q_prepared=q_prepared)
     stats = LampStats()
     stats.mask = mask_bytes.data_ptr() if mask_bytes is not None else None
     stats.counters = counters.data_ptr() if counters is not None else None
@@ -192,8 +197,9 @@ def qkv_project(x, w, *, batch, heads_q, heads_kv, head_dim, workspace, pv="fp16
     """The QKV projection with the attention's K/V cache in its epilogue:
     x [batch * N, hidden] and w [(heads_q + 2 heads_kv) head_dim, hidden]
     bf16 CUDA tensors.  Returns dense q [B, N, Hq, d], k and v [B, N, Hkv, d]
-    (bf16); ``workspace`` then holds their prepared keys and values, for
-    lamp_attn_fwd(..., workspace=workspace, kv_prepared=True)."""
+    (bf16); ``workspace`` then holds their prepared keys and values and the
+    E4M3 copy of q with its norms, for lamp_attn_fwd(..., workspace=workspace,
+    kv_prepared=True, q_prepared=True)."""
     lib = load()
     if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16 or not (x.is_cuda and w.is_cuda):
         raise LampError("x and w must be bf16 CUDA tensors")
@@ -274,13 +280,14 @@ def lamp_attn_fwd_host(q, k, v, *, mask="causal", window=0, scale=0.0, delta=2.0
 
 
 def lamp_tau_sweep(q, k, taus, *, mask="causal", window=0, scale=0.0, delta=2.0 ** -8, records=None,
-                   counters=None, stream=None, workspace=None, kv_prepared=False):
+                   counters=None, stream=None, workspace=None, kv_prepared=False, q_prepared=False):
     """Histograms of 16-bit sub-blocks per tile for up to 8 tau values from
     one pass.  q [B, N, Hq, d], k [B, N, Hkv, d] CUDA tensors.  Returns
     (hist [ntau, 4] int64 CUDA tensor: visited tiles, tiles with 0 / 1 / 2+
     flagged sub-blocks; records [B, Hq, T, T] int32 CUDA tensor of the tile
-    records).  Asynchronous on ``stream``.  ``workspace`` / ``kv_prepared``: as
-    for lamp_attn_fwd (keys prepared by kv_prepare, whose v is then unused)."""
+    records).  Asynchronous on ``stream``.  ``workspace`` / ``kv_prepared`` /
+    ``q_prepared``: as for lamp_attn_fwd (keys prepared by kv_prepare, whose
+    v is then unused)."""
     lib = load()
     if not (q.is_cuda and k.is_cuda):
         raise LampError("q, k must be CUDA tensors")
@@ -293,7 +300,7 @@ def lamp_tau_sweep(q, k, taus, *, mask="causal", window=0, scale=0.0, delta=2.0 
         records = torch.empty((B, Hq, T, T), dtype=torch.int32, device=q.device)
     hist = torch.zeros((max(1, len(taus)), 4), dtype=torch.int64, device=q.device)
     sh = make_shapes(q, k, k, q, window=window, scale=scale, stream=stream, workspace=workspace,
-                     kv_prepared=kv_prepared)
+                     kv_prepared=kv_prepared, q_prepared=q_prepared)
     stats = LampStats()
     stats.mask = None
     stats.counters = counters.data_ptr() if counters is not None else None

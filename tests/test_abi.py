@@ -88,16 +88,17 @@ def test_workspace_bytes(lib):
 
 def test_shapes_struct_matches_the_header():
     """The ctypes mirror ends with the same fields as the C struct, at the
-    offsets the C layout gives them (pv_mode, qk_accum and kv_prepared after
-    the three event handles)."""
-    assert [f[0] for f in lamp.LampShapes._fields_[-3:]] == ["pv_mode", "qk_accum", "kv_prepared"]
+    offsets the C layout gives them (pv_mode, qk_accum, kv_prepared and
+    q_prepared after the three event handles)."""
+    assert [f[0] for f in lamp.LampShapes._fields_[-4:]] == ["pv_mode", "qk_accum", "kv_prepared", "q_prepared"]
     assert lamp.LampShapes.pv_mode.offset == lamp.LampShapes.stage_events.offset + 3 * ctypes.sizeof(ctypes.c_void_p)
     assert lamp.LampShapes.qk_accum.offset == lamp.LampShapes.pv_mode.offset + 4
     assert lamp.LampShapes.kv_prepared.offset == lamp.LampShapes.qk_accum.offset + 4
+    assert lamp.LampShapes.q_prepared.offset == lamp.LampShapes.kv_prepared.offset + 4
     src = open(os.path.join(ROOT, "include", "lamp_attn.h")).read()
     body = src[src.index("typedef struct {\n  int32_t batch"):src.index("} lamp_shapes;")]
     fields = [ln.strip() for ln in body.splitlines() if ln.strip().startswith(("int32_t", "void*", "size_t"))]
-    assert [f.split()[1].rstrip(";") for f in fields[-3:]] == ["pv_mode", "qk_accum", "kv_prepared"]
+    assert [f.split()[1].rstrip(";") for f in fields[-4:]] == ["pv_mode", "qk_accum", "kv_prepared", "q_prepared"]
 
 
 def _call(lib, sh, ptrs=(16, 32, 48, 64), mask=1, delta=2 ** -8, tau=0.5):
@@ -141,6 +142,15 @@ def test_argument_errors_before_launch(lib):
                                      ctypes.byref(st)) == lamp.LAMP_ERR_INVALID_ARG
     assert lib.lamp_attn_fwd_host(16, 32, 48, 64, None, ctypes.byref(sh), 1, 2 ** -8, 0.5, ctypes.byref(st),
                                   None, 0) == lamp.LAMP_ERR_INVALID_ARG
+    sh = _shapes()
+    sh.q_prepared = 1  # the E4M3 copy of q lives in a caller workspace: none given
+    assert _call(lib, sh) == lamp.LAMP_ERR_INVALID_ARG
+    assert lib.lamp_attn_fwd_noalloc(16, 32, 48, 64, None, ctypes.byref(sh), 1, 2 ** -8, 0.5,
+                                     ctypes.byref(st)) == lamp.LAMP_ERR_INVALID_ARG
+    assert lib.lamp_attn_fwd_host(16, 32, 48, 64, None, ctypes.byref(sh), 1, 2 ** -8, 0.5, ctypes.byref(st),
+                                  None, 0) == lamp.LAMP_ERR_INVALID_ARG
+    sh.workspace, sh.workspace_bytes, sh.in_dtype = 256, 1 << 30, 1  # fp32 q: no prepared copy
+    assert _call(lib, sh) == lamp.LAMP_ERR_INVALID_ARG
     # lamp_kv_prepare: a workspace is required
     assert lib.lamp_kv_prepare(32, 48, ctypes.byref(_shapes())) == lamp.LAMP_ERR_INVALID_ARG
     assert lib.lamp_kv_prepare(None, 48, ctypes.byref(_shapes())) == lamp.LAMP_ERR_INVALID_ARG

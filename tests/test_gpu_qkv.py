@@ -62,7 +62,7 @@ def test_projection_and_attention_on_the_cache(case):
         assert np.array_equal(got.double().cpu().numpy(), want)
     mb, cnt = lamp.new_stats(B, Hq, N)
     out, lse, _, _ = lamp.lamp_attn_fwd(q, k, v, mask_bytes=mb, counters=cnt, workspace=ws, kv_prepared=True,
-                                        out_dtype=torch.float32, tau=0.5)
+                                        q_prepared=True, out_dtype=torch.float32, tau=0.5)
     torch.cuda.synchronize()
     ref = oracle.lamp_forward(qo, ko, vo, out_dtype="fp32", tau=0.5)
     c = cnt.cpu().numpy()
@@ -73,8 +73,9 @@ def test_projection_and_attention_on_the_cache(case):
 
 
 def test_cache_equals_the_pre_pass():
-    """Random inputs: the epilogue's K/V cache gives the same attention as
-    the pre-pass run on the same q, k, v (bit for bit), and q, k, v stay
+    """Random inputs: the epilogue's K/V cache, alone and with its E4M3 copy
+    of q, gives the same attention as the pre-pass run on the same q, k, v
+    (bit for bit), and q, k, v stay
     within one BF16 step of the oracle's projection (an FP32 sum may round
     the other way near a BF16 boundary)."""
     B, N, Hq, Hkv, d, hidden = 2, 320, 4, 2, 128, 1024
@@ -95,14 +96,15 @@ def test_cache_equals_the_pre_pass():
         assert np.all(np.abs(g - want) <= ulp + 2.0 ** -20 * m)
         assert np.mean(g != want) < 1e-3
     a = run_gpu(q, k, v, tau=0.5)
-    mb, cnt = lamp.new_stats(B, Hq, N)
-    out, lse, _, _ = lamp.lamp_attn_fwd(q, k, v, mask_bytes=mb, counters=cnt, workspace=ws, kv_prepared=True,
-                                        tau=0.5)
-    torch.cuda.synchronize()
-    assert np.array_equal(a[0], out.float().cpu().numpy().astype(np.float64))
-    assert np.array_equal(a[1], lse.cpu().numpy().astype(np.float64))
-    assert np.array_equal(a[2], mb.cpu().numpy())
-    assert list(a[3][:8]) == list(cnt.cpu().numpy()[:8])
+    for qp in (False, True):
+        mb, cnt = lamp.new_stats(B, Hq, N)
+        out, lse, _, _ = lamp.lamp_attn_fwd(q, k, v, mask_bytes=mb, counters=cnt, workspace=ws, kv_prepared=True,
+                                            q_prepared=qp, tau=0.5)
+        torch.cuda.synchronize()
+        assert np.array_equal(a[0], out.float().cpu().numpy().astype(np.float64))
+        assert np.array_equal(a[1], lse.cpu().numpy().astype(np.float64))
+        assert np.array_equal(a[2], mb.cpu().numpy())
+        assert list(a[3][:8]) == list(cnt.cpu().numpy()[:8])
 
 
 def test_many_tiles_per_cta_pair():
@@ -118,7 +120,7 @@ def test_many_tiles_per_cta_pair():
     a = run_gpu(q, k, v, tau=0.5)
     mb, cnt = lamp.new_stats(B, Hq, N)
     out, lse, _, _ = lamp.lamp_attn_fwd(q, k, v, mask_bytes=mb, counters=cnt, workspace=ws, kv_prepared=True,
-                                        tau=0.5)
+                                        q_prepared=True, tau=0.5)
     torch.cuda.synchronize()
     assert np.array_equal(a[0], out.float().cpu().numpy().astype(np.float64))
     assert np.array_equal(a[2], mb.cpu().numpy())
@@ -131,6 +133,7 @@ def test_fp8_pv_cache():
     x, w = _exact_inputs(B * N, hidden, (Hq + 2 * Hkv) * d, seed=9)
     q, k, v, ws = _project(x, w, B, Hq, Hkv, d, pv="fp8")
     a = run_gpu(q, k, v, tau=4.0, pv="fp8")
-    out, lse, _, _ = lamp.lamp_attn_fwd(q, k, v, workspace=ws, kv_prepared=True, tau=4.0, pv="fp8")
+    out, lse, _, _ = lamp.lamp_attn_fwd(q, k, v, workspace=ws, kv_prepared=True, q_prepared=True, tau=4.0,
+                                        pv="fp8")
     torch.cuda.synchronize()
     assert np.array_equal(a[0], out.float().cpu().numpy().astype(np.float64))
