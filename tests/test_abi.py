@@ -86,6 +86,33 @@ def test_workspace_bytes(lib):
     assert lib.lamp_attn_workspace_bytes(ctypes.byref(sh)) == 0
 
 
+def test_host_buffer_plan(lib, monkeypatch):
+    """lamp_attn_fwd_host's device buffer: at least 16 chunks (kv-head groups
+    split while batch * groups < 16), one slot per chunk within a 1 GiB
+    budget, at least two; LAMP_HOST_MAX_SLOTS lowers the count."""
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+
+    def slot(B, N, Hq, Hkv, d, nh):
+        hq, hkv = Hq // nh, Hkv // nh
+        ws = lib.lamp_attn_workspace_bytes(ctypes.byref(_shapes(B=1, N=N, Hq=hq, Hkv=hkv, d=d)))
+        return al(N * hq * d * 2) * 2 + 2 * al(N * hkv * d * 2) + al(hq * N * 4) + al(ws)
+
+    monkeypatch.delenv("LAMP_HOST_MAX_SLOTS", raising=False)
+    # Qwen3-8B shape: 4 batches x 4 groups = 16 chunks of ~29 MB, all resident
+    s8 = slot(4, 4096, 32, 8, 128, 4)
+    cnt = al(16 * 16 * 8)
+    assert lib.lamp_attn_host_buffer_bytes(ctypes.byref(_shapes())) == 16 * s8 + cnt
+    monkeypatch.setenv("LAMP_HOST_MAX_SLOTS", "2")
+    assert lib.lamp_attn_host_buffer_bytes(ctypes.byref(_shapes())) == 2 * s8 + cnt
+    monkeypatch.setenv("LAMP_HOST_MAX_SLOTS", "1")  # below two: ignored
+    assert lib.lamp_attn_host_buffer_bytes(ctypes.byref(_shapes())) == 16 * s8 + cnt
+    monkeypatch.delenv("LAMP_HOST_MAX_SLOTS")
+    # one long sequence: 8 groups (every kv head its own chunk) of ~400 MB: two slots
+    sl = slot(1, 65536, 64, 8, 128, 8)
+    assert 2 * sl <= (1 << 30) < 3 * sl
+    assert lib.lamp_attn_host_buffer_bytes(ctypes.byref(_shapes(B=1, N=65536, Hq=64, Hkv=8))) == 2 * sl + al(8 * 16 * 8)
+
+
 def test_shapes_struct_matches_the_header():
     """The ctypes mirror ends with the same fields as the C struct, at the
     offsets the C layout gives them (pv_mode, qk_accum, kv_prepared and
