@@ -268,11 +268,10 @@ size_t lamp_attn_workspace_bytes(const lamp_shapes* shapes);
  * are rejected with LAMP_ERR_TOO_LARGE before anything is enqueued.  No
  * cudaMalloc, cudaFree or other allocating call is made.
  *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress with that device current) and keeps it for the life
- * of the process; make that first call before any stream capture, and do
- * not call this entry point again after a cudaDeviceReset of that device
- * (the kept address would be stale).  Status codes as lamp_attn_fwd
+ * Every call looks up the array's device address in the current context
+ * (cudaGetSymbolAddress), so a cudaDeviceReset between calls is harmless;
+ * make the first call on each device before any stream capture (that
+ * lookup may load the module).  Status codes as lamp_attn_fwd
  * (LAMP_ERR_UNSUPPORTED for a head_dim other than 64, 128, 256).  All calls share the array and it keeps the
  * last call's contents (each call clears what must start at zero); calls
  * whose work overlaps on the GPU race on it and must be serialised.

@@ -18,33 +18,21 @@
 // on one device) race on the array: serialise them.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "../../include/lamp_attn.h"
 
 namespace {
 
 __device__ __align__(256) static unsigned char g_noalloc_scratch[LAMP_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
-
 // Device address of the array on the current device.  In host code the
-// array's name only stands in for the symbol; the address has to come from
-// cudaGetSymbolAddress with that device current (once per device, kept for
-// the life of the process: a cudaDeviceReset of that device would leave it
-// stale, so after a reset this entry point must not be used again).
+// array's name only stands in for the symbol; the address comes from
+// cudaGetSymbolAddress in the current context, looked up on every call (a
+// host-side lookup once the module is loaded), so no address outlives a
+// cudaDeviceReset or belongs to another context.
 int scratch_on_current_device(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LAMP_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return LAMP_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return LAMP_ERR_CUDA;
+  *out = p;
   return LAMP_OK;
 }
 
