@@ -137,3 +137,16 @@ def test_fp8_pv_cache():
                                         pv="fp8")
     torch.cuda.synchronize()
     assert np.array_equal(a[0], out.float().cpu().numpy().astype(np.float64))
+
+
+def test_tau_sweep_on_the_projection_outputs():
+    """The tau-sweep pass on the projection's prepared keys and E4M3 query
+    copy: the same records and histograms as a sweep that prepares them."""
+    B, N, Hq, Hkv, d, hidden = 1, 320, 4, 2, 128, 256
+    x, w = _exact_inputs(B * N, hidden, (Hq + 2 * Hkv) * d, seed=31)
+    q, k, v, ws = _project(x, w, B, Hq, Hkv, d)
+    taus = [2.0 ** -i for i in range(6)]
+    h_ref, r_ref = lamp.lamp_tau_sweep(q, k, taus)
+    h, r = lamp.lamp_tau_sweep(q, k, taus, workspace=ws, kv_prepared=True, q_prepared=True)
+    torch.cuda.synchronize()
+    assert torch.equal(h.cpu(), h_ref.cpu()) and torch.equal(r.cpu(), r_ref.cpu())
