@@ -309,6 +309,9 @@ int lamp_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out
  *                 not used.
  * Synchronous: returns after out and lse hold the results (the status of
  * the device side is in counters[LAMP_CNT_STATUS] when counters are given).
+ * The internal streams and events are created once per device (anew after
+ * the device's context changes, e.g. a cudaDeviceReset); calls on one
+ * device from several host threads run one after the other.
  * Errors as lamp_attn_fwd; LAMP_ERR_WORKSPACE if dev_buffer is too small or
  * misaligned.
  */

@@ -9,6 +9,7 @@
 // chunk holds causal rows that see the whole sequence, whose CTAs take
 // about as long as the chunk itself, so the next chunks' CTAs must fill the
 // SMs that those leave idle.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -108,22 +109,55 @@ __global__ void sum_counters_kernel(unsigned long long* dst, const unsigned long
   dst[i] = acc;
 }
 
-// Two copy streams and the internal compute streams per device, created once.
-struct CopyStreams {
+// Per device: two copy streams, the internal compute streams and the events
+// of one call (per slot: inputs landed, computed, outputs read back; then
+// the start and one join per internal stream), created once in the
+// device's current context and created anew when that context changes
+// (after a cudaDeviceReset the old handles are dropped, not used).  A call
+// holds the device's lock from start to end -- it is synchronous -- so
+// calls on one device run one after the other.
+constexpr int kJoin = 3 * kMaxSlots;
+constexpr int kEvents = kJoin + 2 + kComputeStreams;
+struct HostCtx {
+  std::mutex mu;
+  CUcontext ctx = nullptr;
   cudaStream_t h2d = nullptr, d2h = nullptr, comp[kComputeStreams - 1] = {};
+  cudaEvent_t ev[kEvents] = {};
 };
-std::mutex g_streams_mu;
-CopyStreams g_streams[64];
+HostCtx g_ctx[64];
 
-bool copy_streams(int dev, CopyStreams& out) {
-  if (dev < 0 || dev >= 64) return false;
-  std::lock_guard<std::mutex> lk(g_streams_mu);
-  CopyStreams& cs = g_streams[dev];
-  if (!cs.h2d && cudaStreamCreateWithFlags(&cs.h2d, cudaStreamNonBlocking) != cudaSuccess) return false;
-  if (!cs.d2h && cudaStreamCreateWithFlags(&cs.d2h, cudaStreamNonBlocking) != cudaSuccess) return false;
-  for (auto& c : cs.comp)
-    if (!c && cudaStreamCreateWithFlags(&c, cudaStreamNonBlocking) != cudaSuccess) return false;
-  out = cs;
+using CtxFn = CUresult (*)(CUcontext*);
+CUcontext current_context() {
+  static CtxFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (CtxFn)f;
+  });
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
+// With c.mu held and the device's primary context current.
+bool ctx_ready(HostCtx& c) {
+  const CUcontext now = current_context();
+  if (!now) return false;
+  if (now != c.ctx) {
+    c.h2d = c.d2h = nullptr;
+    for (auto& s : c.comp) s = nullptr;
+    for (auto& e : c.ev) e = nullptr;
+    c.ctx = now;
+  }
+  if (!c.h2d && cudaStreamCreateWithFlags(&c.h2d, cudaStreamNonBlocking) != cudaSuccess) return false;
+  if (!c.d2h && cudaStreamCreateWithFlags(&c.d2h, cudaStreamNonBlocking) != cudaSuccess) return false;
+  for (auto& s : c.comp)
+    if (!s && cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return false;
+  for (auto& e : c.ev)
+    if (!e && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
   return true;
 }
 
@@ -154,37 +188,20 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
     return LAMP_ERR_INVALID_ARG;
   Plan p;
   if (!make_plan(s, p)) return LAMP_ERR_INVALID_ARG;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return LAMP_ERR_CUDA;
-  CopyStreams cps;
-  if (!copy_streams(dev, cps)) return LAMP_ERR_CUDA;
-  cudaStream_t sc = (cudaStream_t)s.stream;
-
   uint8_t* buf = (uint8_t*)dev_buffer;
   if (buf && (dev_buffer_bytes < p.total || ((uintptr_t)buf & 255u))) return LAMP_ERR_WORKSPACE;
-  // per slot: inputs landed, computed, outputs read back; then the start
-  // and one join per internal stream
-  constexpr int kJoin = 3 * kMaxSlots;
-  const int nev = 3 * p.nslots;
-  cudaEvent_t ev[kJoin + 2 + kComputeStreams] = {};
-  auto make_ev = [&](int i) { return cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess; };
-  bool evs_ok = true;
-  for (int i = 0; i < nev && evs_ok; ++i) evs_ok = make_ev(i);
-  for (int i = kJoin; i < kJoin + 2 + kComputeStreams && evs_ok; ++i) evs_ok = make_ev(i);
-  auto free_evs = [&]() {
-    for (auto& e : ev)
-      if (e) cudaEventDestroy(e);
-  };
-  if (!evs_ok) {
-    free_evs();
-    return LAMP_ERR_CUDA;
-  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return LAMP_ERR_CUDA;
+  if (cudaSetDevice(dev) != cudaSuccess) return LAMP_ERR_CUDA;  // binds the primary context to this thread
+  HostCtx& hc = g_ctx[dev];
+  std::lock_guard<std::mutex> lock(hc.mu);
+  if (!ctx_ready(hc)) return LAMP_ERR_CUDA;
+  const HostCtx& cps = hc;
+  cudaEvent_t* ev = hc.ev;
+  cudaStream_t sc = (cudaStream_t)s.stream;
   bool own = false;
   if (!buf) {
-    if (cudaMallocAsync((void**)&buf, p.total, sc) != cudaSuccess) {
-      free_evs();
-      return LAMP_ERR_CUDA;
-    }
+    if (cudaMallocAsync((void**)&buf, p.total, sc) != cudaSuccess) return LAMP_ERR_CUDA;
     own = true;
   }
   int rc = LAMP_OK;
@@ -273,7 +290,6 @@ int lamp_attn_fwd_host(const void* q, const void* k, const void* v, void* out, f
   if (own) cuda_ok(cudaFreeAsync(buf, sc));
   // the results are in host memory when the call returns
   cuda_ok(cudaStreamSynchronize(sc));
-  free_evs();
   return rc;
 }
 
