@@ -41,7 +41,7 @@ constexpr int kQA = kQBM * kQBK * 2;            // x stage: 16 KB
 constexpr int kQB = (kQBN / 2) * kQBK * 2;      // W stage (this CTA's half): 16 KB
 constexpr int kQStage = kQA + kQB;
 constexpr int kQBar = kQST * kQStage;           // barriers after the stages
-constexpr int kQSmem = kQBar + 256 + 1024 + kQB;  // + barriers, TMEM slot, alignment slack, a W stage of padding
+constexpr int kQSmem = kQBar + 256 + 1024;      // + barriers, TMEM slot, alignment slack
 constexpr int kQThreads = 192;                  // producer, MMA, four epilogue warps
 
 // ---- the CTA-pair forms (cta_group::2) this kernel alone uses
