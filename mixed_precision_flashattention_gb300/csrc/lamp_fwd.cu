@@ -456,11 +456,14 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
       for (int j = J0; j < J1 && !*cx.abort && !(C::NS == 1 && !kSweep); ++j) {
         const int s = (j - J0) % C::NS, u = (j - J0) / C::NS;
         bool ok = true;
-        if (u >= 1) {  // the stage held key j - NS: wait until every tile that used it is done
+        if (u >= 1) {  // the stage held key j - NS: wait until every tile is done with it
+          // (a tile whose keys start after J0 releases the keys before its
+          // first one unused, so that no stage runs two phases ahead of the
+          // tile's parity waits)
           const int jr = j - C::NS;
 #pragma unroll
           for (int t = 0; t < C::NT; ++t) {
-            if (jr < JLO(t) || jr >= JHI(t)) continue;
+            if (JHI(t) <= JLO(t) || jr >= JHI(t)) continue;
             const uint32_t bit = 1u << (2 * t + s);
             ok = ok && wait_bar(cx, bar(M_KV_EMPTY + 16 * s + 8 * t), (rel & bit) ? 1u : 0u);
             rel ^= bit;
@@ -530,6 +533,13 @@ __global__ void __launch_bounds__(Cfg<D, kOpt>::THREADS, 1) lamp_fwd_kernel(cons
       };
       bool ok = wait_bar(cx, bar(M_Q_FULL), 0);
       if (ok && !kSweep && p.q8_in_cta) ok = wait_bar(cx, bar(M_Q8_READY + 8 * t), 0);
+      // keys of the CTA before this tile's first one (a sliding window's
+      // second tile): wait for each to land and hand its stage back unused,
+      // so the stage's phases stay in step with this tile's parity waits
+      for (int j = J0; ok && j < jlo; ++j) {
+        ok = wait_bar(cx, bar(M_KV_FULL + 8 * stage_of(j)), ((j - J0) / C::NS) & 1);
+        if (ok) mbar_arrive(bar(M_KV_EMPTY + 16 * stage_of(j) + 8 * t));
+      }
       if (kSweep) {
         // QK8 only.  A key's stage is handed back once the softmax has
         // published the step (DEC): its exact re-derivations read K8 from
