@@ -290,3 +290,223 @@ def test_model_catches_a_missing_wait(drop):
         except AssertionError:
             failures += 1
     assert failures > 0
+
+
+# ---------------------------------------------------------------------------
+# The one-stage path (d = 256, one query tile per CTA): K8 in two slots by
+# key parity, K16 and V in their own parts of the stage with their own
+# barriers, two S16 buffers (one barrier each); the producer loads K16(j),
+# K8(j + 1), V(j) in that order; the MMA thread issues QK8(i), then step
+# i - 1's late QK16 or its K16 release, step i's speculative QK16, then
+# P.V(i - 1).
+
+def run_one_stage(seed, n, flags, drop=None):
+    rng = random.Random(seed)
+    K8_FULL, K8_EMPTY = [Bar(), Bar()], [Bar(), Bar()]
+    K16_FULL, K16_EMPTY, V_FULL, V_EMPTY = Bar(), Bar(), Bar(), Bar()
+    S_FULL, DEC, P_FULL, PV_DONE = Bar(), Bar(), Bar(), Bar()
+    S16_FULL = [Bar(), Bar()]
+    k8 = [None, None]                 # key in each K8 slot
+    k16 = [None]
+    vv = [None]
+    S8, S16, P = [None], [None, None], [None]
+    s8_read = [-1]
+    ANY = [None, None]
+    reads = {"k8": {}, "k16": {}, "v": {}}
+    mq = []                           # MMA ops and commits in issue order
+    copies = []                       # (part, slot, key) in issue order
+    issued16 = [0, 0]
+    pv_done = [-1]
+
+    def producer():
+        def load_k8(u):
+            K8_FULL[u & 1].expect_tx(1)
+            copies.append(("k8", u & 1, u))
+
+        if n > 0:
+            load_k8(0)
+        for u in range(n):
+            if u >= 1:
+                while not K16_EMPTY.passed((u - 1) & 1):
+                    yield
+                assert reads["k16"].get(u - 1, 0) == 0
+            K16_FULL.expect_tx(1)
+            copies.append(("k16", 0, u))
+            yield
+            if u + 1 < n:
+                v = u + 1  # its slot held key v - 2
+                if v >= 2:
+                    while drop != "k8_empty" and not K8_EMPTY[v & 1].passed(((v - 2) >> 1) & 1):
+                        yield
+                    assert reads["k8"].get(v - 2, 0) == 0, "K8 slot refilled while still read"
+                load_k8(v)
+                yield
+            if u >= 1:
+                while not V_EMPTY.passed((u - 1) & 1):
+                    yield
+                assert reads["v"].get(u - 1, 0) == 0
+            V_FULL.expect_tx(1)
+            copies.append(("v", 0, u))
+            yield
+
+    def issue(kind, i=None, bar=None):
+        for part in {"qk8": ("k8",), "qk16": ("k16",), "pv": ("v",)}.get(kind, ()):
+            reads[part][i] = reads[part].get(i, 0) + 1
+        mq.append((kind, i, bar))
+
+    def mma():
+        if n <= 0:
+            return
+        counts = [0, 0, 0]
+
+        def qk16(i):
+            issue("qk16", i)
+            issue("commit", bar=S16_FULL[i & 1])
+            issue("commit", bar=K16_EMPTY)
+            issued16[i & 1] += 1
+
+        def decided(i):
+            while not K16_FULL.passed(i & 1):
+                yield
+            step, f = ANY[i & 1]
+            assert step == i
+            if f:
+                qk16(i)
+            else:
+                K16_EMPTY.arrive()
+
+        spec = True
+        for i in range(n):
+            ph = i & 1
+            if i > 0:
+                while not DEC.passed((i - 1) & 1):
+                    yield
+                K8_EMPTY[(i - 1) & 1].arrive()  # K8 slot of key i - 1
+            while not K8_FULL[i & 1].passed((i >> 1) & 1):
+                yield
+            issue("qk8", i)
+            issue("commit", bar=S_FULL)
+            if i > 0:
+                step, prev = ANY[(i - 1) & 1]
+                assert step == i - 1
+                if not spec:
+                    yield from decided(i - 1)
+                spec = prev
+            if spec:
+                while not K16_FULL.passed(ph):
+                    yield
+                qk16(i)
+            if i > 0:
+                while not P_FULL.passed((i - 1) & 1):
+                    yield
+                while not V_FULL.passed(ph ^ 1):
+                    yield
+                issue("pv", i - 1)
+                issue("commit", bar=PV_DONE)
+                issue("commit", bar=V_EMPTY)
+            yield
+        while not DEC.passed((n - 1) & 1):
+            yield
+        if not spec:
+            yield from decided(n - 1)
+        while not P_FULL.passed((n - 1) & 1):
+            yield
+        while not V_FULL.passed((n - 1) & 1):
+            yield
+        issue("pv", n - 1)
+        issue("commit", bar=PV_DONE)
+
+    def softmax():
+        n16, prev_any = [0, 0], True
+        for jj in range(n):
+            while not S_FULL.passed(jj & 1):
+                yield
+            assert S8[0] == jj
+            assert k8[jj & 1] == jj, "K8 of the step's key gone before its decision"
+            s8_read[0] = jj
+            yield
+            any_ = flags[jj]
+            ANY[jj & 1] = (jj, any_)
+            DEC.arrive()
+            yield
+            if jj > 0:
+                while not PV_DONE.passed((jj - 1) & 1):
+                    yield
+            b = jj & 1
+            if any_:
+                while not S16_FULL[b].passed(n16[b] & 1):
+                    yield
+                assert S16[b] == jj, "S16 of another step"
+            n16[b] += 1 if (any_ or prev_any) else 0
+            prev_any = any_
+            yield
+            assert jj == 0 or pv_done[0] >= jj - 1
+            P[0] = jj
+            P_FULL.arrive()
+            yield
+        assert n16 == issued16
+
+    def complete_mma():
+        kind, i, bar = mq.pop(0)
+        if kind == "commit":
+            bar.arrive()
+            return
+        if kind == "qk8":
+            assert k8[i & 1] == i and s8_read[0] == i - 1
+            reads["k8"][i] -= 1
+            S8[0] = i
+        elif kind == "qk16":
+            assert k16[0] == i
+            reads["k16"][i] -= 1
+            S16[i & 1] = i
+        else:
+            assert vv[0] == i and P[0] == i
+            reads["v"][i] -= 1
+            pv_done[0] = i
+
+    live = [producer(), mma(), softmax()]
+    steps = 0
+    while live or copies or mq:
+        steps += 1
+        assert steps < 300000, "no progress"
+        choices = [("actor", x) for x in live] + ([("copy", None)] if copies else []) + \
+            ([("mma", None)] if mq else [])
+        kind, x = rng.choice(choices)
+        if kind == "actor":
+            try:
+                next(x)
+            except StopIteration:
+                live.remove(x)
+        elif kind == "copy":
+            part, slot, key = copies.pop(0)
+            if part == "k8":
+                k8[slot] = key
+                K8_FULL[slot].complete_tx(1)
+            elif part == "k16":
+                k16[0] = key
+                K16_FULL.complete_tx(1)
+            else:
+                vv[0] = key
+                V_FULL.complete_tx(1)
+        else:
+            complete_mma()
+
+
+@pytest.mark.parametrize("density", [0.0, 0.15, 0.5, 0.85, 1.0])
+def test_one_stage_protocol_random_interleavings(density):
+    rng = random.Random(int(density * 100) + 29)
+    for k in range(150):
+        n = rng.randint(1, 9)
+        run_one_stage(rng.randrange(1 << 30), n, [rng.random() < density for _ in range(n)])
+
+
+def test_one_stage_model_catches_a_missing_wait():
+    rng = random.Random(3)
+    failures = 0
+    for k in range(300):
+        n = rng.randint(3, 9)
+        try:
+            run_one_stage(rng.randrange(1 << 30), n, [rng.random() < 0.5 for _ in range(n)], drop="k8_empty")
+        except AssertionError:
+            failures += 1
+    assert failures > 0
