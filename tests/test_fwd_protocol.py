@@ -271,6 +271,8 @@ def test_fwd_protocol_random_interleavings(density):
     for k in range(120):
         ranges, flags = _case(rng, density)
         run(rng.randrange(1 << 30), ranges, flags)
+        # one query tile per CTA (the optional modes at d = 128)
+        run(rng.randrange(1 << 30), ranges[:1], flags[:1])
 
 
 @pytest.mark.parametrize("drop", ["kv_empty", "pv_done", "skip"])
