@@ -512,3 +512,133 @@ def test_one_stage_model_catches_a_missing_wait():
         except AssertionError:
             failures += 1
     assert failures > 0
+
+
+# ---------------------------------------------------------------------------
+# The detector-only tau-sweep pass on the two-stage path: QK8 only, a key's
+# stage handed back once the softmax has published its step (its exact
+# re-derivations read K8 until then), a late-starting tile's earlier keys
+# handed back unused.
+
+def run_sweep(seed, ranges, drop=None):
+    rng = random.Random(seed)
+    NT = len(ranges)
+    J0 = min(r[0] for r in ranges)
+    J1 = max(r[1] for r in ranges)
+    stage_of = lambda j: (j - J0) % NS  # noqa: E731
+    KV_FULL = [Bar() for _ in range(NS)]
+    KV_EMPTY = [[Bar() for _ in range(NT)] for _ in range(NS)]
+    S_FULL, DEC = [Bar() for _ in range(NT)], [Bar() for _ in range(NT)]
+    stage = [None] * NS
+    S8 = [None] * NT
+    in_use = {}  # key -> tiles that have not released it
+    mq = [[] for _ in range(NT)]
+    copies = []
+
+    def producer():
+        rel = 0
+        for j in range(J0, J1):
+            s, u = stage_of(j), (j - J0) // NS
+            if u >= 1:
+                jr = j - NS
+                for t in range(NT):
+                    used = ranges[t][0] <= jr < ranges[t][1] if drop == "skip" else \
+                        (ranges[t][1] > ranges[t][0] and jr < ranges[t][1])
+                    if not used:
+                        continue
+                    bit = 1 << (2 * t + s)
+                    while not KV_EMPTY[s][t].passed(1 if rel & bit else 0):
+                        yield
+                    rel ^= bit
+                assert not in_use.get(jr), "stage refilled while a tile still reads its key"
+            KV_FULL[s].expect_tx(1)
+            copies.append((s, j))
+            yield
+
+    def mma(t):
+        jlo, jhi = ranges[t]
+        n = jhi - jlo
+        if n <= 0:
+            return
+        if drop != "skip":
+            for j in range(J0, jlo):
+                while not KV_FULL[stage_of(j)].passed(((j - J0) // NS) & 1):
+                    yield
+                KV_EMPTY[stage_of(j)][t].arrive()
+                yield
+        for i in range(n):
+            j = jlo + i
+            if i > 0:
+                while not DEC[t].passed((i - 1) & 1):
+                    yield
+                in_use[j - 1].discard(t)
+                KV_EMPTY[stage_of(j - 1)][t].arrive()
+            while not KV_FULL[stage_of(j)].passed(((j - J0) // NS) & 1):
+                yield
+            in_use.setdefault(j, set()).add(t)
+            mq[t].append(("qk8", i))
+            mq[t].append(("commit", S_FULL[t]))
+            yield
+        while not DEC[t].passed((n - 1) & 1):
+            yield
+        in_use[jhi - 1].discard(t)
+        KV_EMPTY[stage_of(jhi - 1)][t].arrive()
+
+    def softmax(t):
+        jlo, jhi = ranges[t]
+        for jj in range(jhi - jlo):
+            while not S_FULL[t].passed(jj & 1):
+                yield
+            assert S8[t] == jj
+            assert stage[stage_of(jlo + jj)] == jlo + jj, "K8 of the step's key gone before its decision"
+            yield
+            DEC[t].arrive()
+            yield
+
+    def complete(t):
+        kind, x = mq[t].pop(0)
+        if kind == "commit":
+            x.arrive()
+            return
+        j = ranges[t][0] + x
+        assert stage[stage_of(j)] == j, "QK8 on a stage that does not hold its key"
+        S8[t] = x
+
+    live = [producer()] + [mma(t) for t in range(NT)] + [softmax(t) for t in range(NT)]
+    steps = 0
+    while live or copies or any(mq):
+        steps += 1
+        assert steps < 300000, "no progress"
+        choices = [("actor", x) for x in live] + ([("copy", None)] if copies else []) + \
+            [("mma", t) for t in range(NT) if mq[t]]
+        kind, x = rng.choice(choices)
+        if kind == "actor":
+            try:
+                next(x)
+            except StopIteration:
+                live.remove(x)
+        elif kind == "copy":
+            s, j = copies.pop(0)
+            stage[s] = j
+            KV_FULL[s].complete_tx(1)
+        else:
+            complete(x)
+
+
+def test_sweep_protocol_random_interleavings():
+    rng = random.Random(41)
+    for k in range(300):
+        ranges, _ = _case(rng, 0.0)
+        run_sweep(rng.randrange(1 << 30), ranges)
+
+
+def test_sweep_model_catches_the_early_parity_pass():
+    rng = random.Random(43)
+    failures = 0
+    for k in range(300):
+        ranges, _ = _case(rng, 0.0)
+        try:
+            run_sweep(rng.randrange(1 << 30), ranges, drop="skip")
+        except AssertionError:
+            failures += 1
+    assert failures > 0
