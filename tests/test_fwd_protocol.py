@@ -1,6 +1,7 @@
-"""A CPU model of the fused attention kernel's protocol (lamp_fwd.cu, the
-two-stage path: d <= 128, two query tiles per CTA) under random
-interleavings.  The TMA producer, each tile's MMA-issuing thread and each
+"""CPU models of the fused attention kernel's protocol (lamp_fwd.cu) under
+random interleavings: the two-stage path (d <= 128, one or two query tiles
+per CTA), the one-stage path (d = 256; below) and the detector-only tau
+sweep (below).  For the two-stage path:  The TMA producer, each tile's MMA-issuing thread and each
 tile's softmax (one actor per tile: its warps meet at the step's tile
 barrier anyway) run the kernel's loops with its phase / parity formulas
 against mbarriers with the hardware's semantics, while copies and MMAs
